@@ -1,0 +1,177 @@
+// Device-side building blocks shared by the libmoeq kernels (sm_103a):
+// inline-PTX wrappers for mbarriers, TMA bulk-tensor loads, the global timer,
+// and the E4M3 conversions, plus the per-group live activation quantiser.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moeq.h"
+
+namespace moeq {
+
+constexpr int kGroup = MOEQ_GROUP;
+constexpr int kMaxTok = MOEQ_MAX_TOKENS;
+// Bounded waits: a wait that has not finished after this long records
+// MOEQ_ERR_TIMEOUT in the device status word and gives up.
+constexpr unsigned long long kWaitLimitNs = 2000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Gives up (returns
+// false) when *abort becomes non-zero or after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled bulk-tensor load of one box into shared memory, completing on `bar`.
+// x is the innermost (byte) coordinate and must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Named barrier over the consumer warps only (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- E4M3
+// Two fp32 -> two E4M3 codes, round to nearest even, saturating to +-448.
+// Returns (code(hi) << 8) | code(lo).
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two E4M3 codes (low byte first) -> two exact fp16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(v);
+}
+
+// Four E4M3 codes packed in a u32 (byte 0 = lowest k) -> four exact floats.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float2& a, float2& b) {
+    a = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)));
+    b = f16x2_to_f32x2(e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Load 4 consecutive activation elements (k .. k+3) of row `row` as fp32.
+template <bool kF32>
+__device__ __forceinline__ float4 load_act4(const void* a, size_t ld, int row, int k) {
+    if (kF32) {
+        const float* p = static_cast<const float*>(a) + static_cast<size_t>(row) * ld + k;
+        return __ldg(reinterpret_cast<const float4*>(p));
+    } else {
+        const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(a) + static_cast<size_t>(row) * ld + k;
+        uint2 raw = __ldg(reinterpret_cast<const uint2*>(p));
+        float4 r;
+        r.x = __uint_as_float(raw.x << 16);
+        r.y = __uint_as_float(raw.x & 0xFFFF0000u);
+        r.z = __uint_as_float(raw.y << 16);
+        r.w = __uint_as_float(raw.y & 0xFFFF0000u);
+        return r;
+    }
+}
+
+// One warp quantises one 1 x 128 group (GLM-5.2 x10 §1, §8c: live FP8
+// activation quantisation).  Lane l holds elements 4l .. 4l+3 in v.
+//   s = fl32(amax / 448); code = RNE_satfinite(fl32(x / s)); s == 0 -> signed zero.
+// Returns the 4 codes packed little-endian (element 4l in byte 0) and the
+// scale through *s_out; also writes the 4 decoded (exact) values to dec.
+__device__ __forceinline__ uint32_t quant_group_warp(float4 v, float* s_out, float4* dec) {
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint32_t codes;
+    if (s == 0.0f) {
+        codes = (signbit(v.x) ? 0x80u : 0u) | (signbit(v.y) ? 0x8000u : 0u) |
+                (signbit(v.z) ? 0x800000u : 0u) | (signbit(v.w) ? 0x80000000u : 0u);
+    } else {
+        const uint16_t c01 = e4m3x2_from_f32(__fdiv_rn(v.x, s), __fdiv_rn(v.y, s));
+        const uint16_t c23 = e4m3x2_from_f32(__fdiv_rn(v.z, s), __fdiv_rn(v.w, s));
+        codes = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+    }
+    float2 d01, d23;
+    e4m3x4_to_f32(codes, d01, d23);
+    *dec = make_float4(d01.x, d01.y, d23.x, d23.y);
+    *s_out = s;
+    return codes;
+}
+
+}  // namespace moeq

@@ -1,0 +1,225 @@
+/*
+ * libmoeq -- FP8 live-quantised MoE expert projection for small decode
+ * batches (M = 1..16 tokens: plain decode and multi-token draft
+ * verification), written for NVIDIA GB300 (sm_103a).
+ *
+ * Citations.  "GLM-5.2 x10" is the blog.sionic.ai page titled
+ * "GPU 커널부터 새로 짜서 GLM-5.2 속도 10배 올리기"; "§n" is its numbered
+ * section.  The page states the problem this library solves -- decode is a
+ * stream of FP8 expert weights from HBM with very little arithmetic on top
+ * (bandwidth model), the activations are quantised to FP8 live in front of
+ * each GEMM (§1, §8c), that quantisation is fused into the GEMM instead of
+ * round-tripping through HBM (§4, "PQ-GEMM"), K is split across the SMs so
+ * that enough of them stream weights (§1, split-K), and several tokens
+ * verified together share one read of each expert (§5-§6) -- but it prints no
+ * interface.  The calls below are this library's own statement of it.
+ *
+ * Numeric contract (the page fixes none of it; these are this library's
+ * choices, applied identically by every call):
+ *   - FP8 is OCP E4M3FN (bias 7, max 448, no infinities);
+ *   - activations are quantised per token in groups of 1 x 128 along K:
+ *     s = fl32(amax / 448), q = RNE_satfinite(fl32(x / s)); a group whose
+ *     s is 0 gets signed-zero codes;
+ *   - weights carry one fp32 scale per 128 x 128 block;
+ *   - GEMMs accumulate in fp32: y = sum_g s_a * s_w * sum_{k in g} q_a * q_w.
+ *
+ * Conventions for every call:
+ *   - tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *     16-byte aligned (fp32 scale arrays and routing arrays: 4-byte);
+ *     `stream` is a cudaStream_t passed as void*;
+ *   - calls are asynchronous on `stream` and never synchronise the host
+ *     (except moeq_read_device_status, which says so);
+ *   - the library allocates no device memory: the caller passes a
+ *     workspace sized by moeq_workspace_size / moeq_gemm_workspace_size,
+ *     zeroed once with moeq_workspace_init; kernels leave it reusable; one
+ *     workspace must not be used by two calls that may run concurrently;
+ *   - arguments are validated on the host first; on any error nothing is
+ *     launched and the status says why;
+ *   - inputs must be finite (NaN/Inf inputs give unspecified results).
+ */
+#ifndef MOEQ_H
+#define MOEQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moeq_status {
+    MOEQ_OK = 0,
+    MOEQ_ERR_INVALID_ARG = 1,       /* null pointer, misaligned pointer, bad enum, M out of range */
+    MOEQ_ERR_UNSUPPORTED_SHAPE = 2, /* K, N, H or I not a multiple of 128, or above the limits */
+    MOEQ_ERR_WORKSPACE = 3,         /* workspace null or smaller than required */
+    MOEQ_ERR_CUDA = 4,              /* a CUDA runtime call failed (launch, attribute, memset) */
+    MOEQ_ERR_TIMEOUT = 5,           /* a bounded device-side wait gave up (device status word) */
+    MOEQ_ERR_DEVICE = 6             /* no CUDA device, or not a compute capability 10.3 part */
+} moeq_status;
+
+typedef enum moeq_dtype { MOEQ_BF16 = 0, MOEQ_F32 = 1 } moeq_dtype;
+
+#define MOEQ_GROUP 128          /* quantisation group along K, and weight block edge */
+#define MOEQ_MAX_TOKENS 16      /* M limit: decode plus draft verification */
+#define MOEQ_MAX_EXPERTS 1024   /* routed experts limit of moeq_route */
+#define MOEQ_MAX_TOPK 16
+#define MOEQ_MAX_K 32768        /* K (H or I) limit of the GEMM calls */
+
+/* Human-readable text of a status (static storage, never NULL). */
+const char* moeq_status_string(moeq_status s);
+
+/* ABI version, bumped whenever a signature or struct below changes. */
+int moeq_abi_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Routing plan (GLM-5.2 x10, bandwidth model: top-8 experts per token;     */
+/* §5-§6: tokens verified together share one weight read, so experts are    */
+/* deduplicated).  All members point to caller-owned device memory.         */
+/*   topk_id [M, top_k]   j-th largest logit of token m, ties -> lower id   */
+/*   topk_w  [M, top_k]   softmax over the top_k picked logits              */
+/*   n_uniq  [1]          U = unique routed experts + 1 (the shared one)    */
+/*   uniq    [max_uniq]   routed expert ids ascending, then E_routed        */
+/*                        (the shared expert's id) last                     */
+/*   offs    [max_uniq+1] pairs of unique expert u are offs[u]..offs[u+1]-1 */
+/*   pair_tok[max_pairs]  token of each (token, expert) pair, ascending     */
+/*                        within an expert                                  */
+/*   pair_of [M, top_k+1] pair of (token m, slot j); slot top_k = shared    */
+/* ------------------------------------------------------------------------ */
+typedef struct moeq_route_plan {
+    int32_t* topk_id;
+    float* topk_w;
+    int32_t* n_uniq;
+    int32_t* uniq;
+    int32_t* offs;
+    int32_t* pair_tok;
+    int32_t* pair_of;
+} moeq_route_plan;
+
+/* min(E_routed, M * top_k) + 1: the most unique experts a plan can hold. */
+int moeq_max_uniq(int M, int E_routed, int top_k);
+/* M * top_k + M: (token, expert) pairs including the shared expert. */
+int moeq_max_pairs(int M, int top_k);
+/* Bytes of one device buffer that moeq_route_plan_carve splits into a plan. */
+size_t moeq_route_plan_bytes(int M, int E_routed, int top_k);
+/* Point the members of *plan into `base` (device memory of at least
+ * moeq_route_plan_bytes bytes, 16-byte aligned).  Host-only, no launch. */
+moeq_status moeq_route_plan_carve(void* base, size_t bytes, int M, int E_routed, int top_k,
+                                  moeq_route_plan* plan);
+
+/* ------------------------------------------------------------------------ */
+/* Workspace.                                                               */
+/* ------------------------------------------------------------------------ */
+/* Bytes needed by moeq_moe_layer for M tokens, hidden H, expert
+ * intermediate I, n_experts_incl_shared = E_routed + 1, top_k.  Depends on
+ * the current device's SM count; returns 0 on invalid arguments or when no
+ * device is present. */
+size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int top_k);
+/* Bytes needed by one standalone GEMM call.  rows_out = I for
+ * moeq_expert_gemm_gateup_swiglu (is_gate_up = 1), N for moeq_expert_gemm_down
+ * (is_gate_up = 0); max_uniq as for the plan the call is given. */
+size_t moeq_gemm_workspace_size(int rows_out, int max_uniq, int is_gate_up);
+/* Zero the workspace (split-K tickets and the device status word) on
+ * `stream`.  Needed once after allocation; kernels leave it zeroed. */
+moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream);
+/* SYNCHRONOUS: copy the device status word (0 or a moeq_status that a
+ * kernel recorded, e.g. MOEQ_ERR_TIMEOUT) to *device_status.  Waits for the
+ * work already queued on the current device. */
+moeq_status moeq_read_device_status(const void* ws, size_t ws_bytes, int* device_status);
+
+/* ------------------------------------------------------------------------ */
+/* moeq_quant_act -- live activation quantisation (GLM-5.2 x10 §1, §8c).   */
+/* x [M, K] (bf16 or fp32) -> q [M, K] E4M3 codes, s [M, K/128] fp32.       */
+/* Standalone form of the prologue that the GEMM calls fuse.                */
+/* M in [1, 4096], K a multiple of 128 up to MOEQ_MAX_K.                    */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_quant_act(const void* x, moeq_dtype x_dtype, int M, int K,
+                           uint8_t* q, float* s, void* stream);
+
+/* moeq_quant_weight -- offline block quantisation of E expert matrices.    */
+/* w [E, N, K] fp32 -> q [E, N, K] codes, s [E, N/128, K/128] fp32, one     */
+/* scale per 128 x 128 block with the same codec as the activations.        */
+moeq_status moeq_quant_weight(const float* w, int E, int N, int K,
+                              uint8_t* q, float* s, void* stream);
+
+/* moeq_route -- top-k routing plus expert deduplication for M tokens.     */
+/* logits [M, E_routed] fp32 -> *plan (see moeq_route_plan).                */
+/* M in [1, MOEQ_MAX_TOKENS], E_routed <= MOEQ_MAX_EXPERTS,                 */
+/* top_k in [1, min(E_routed, MOEQ_MAX_TOPK)].                              */
+moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k,
+                       const moeq_route_plan* plan, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moeq_expert_gemm_gateup_swiglu -- quant(x) fused into the gate_up FP8    */
+/* GEMM of every unique expert of a plan, split-K over all SMs with a       */
+/* deterministic fp32 reduction, and the SwiGLU epilogue                    */
+/* (GLM-5.2 x10 §1: split-K; §4: quantisation fused into the GEMM).         */
+/*   x       [M, H] bf16 or fp32, M <= MOEQ_MAX_TOKENS                      */
+/*   w_gu    [n_experts, 2I, H] E4M3: gate rows [0, I), up rows [I, 2I)     */
+/*   s_gu    [n_experts, 2I/128, H/128] fp32                                */
+/*   uniq/offs/pair_tok/n_uniq_dev: the plan (device), U read on the device */
+/*   h       [max_pairs, I] fp32: h[p] = silu(gate . x[tok(p)]) * (up . x)  */
+/*   q_x_opt [M, H], s_x_opt [M, H/128]: optional dump of the codes and     */
+/*           scales the fused prologue used, for the tokens of the plan's   */
+/*           last unique expert (the shared expert, which serves them all)  */
+/* H and I multiples of 128, H <= MOEQ_MAX_K.                               */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_expert_gemm_gateup_swiglu(
+    const void* x, moeq_dtype x_dtype, int M, int H, int I,
+    const uint8_t* w_gu, const float* s_gu, int n_experts,
+    const int32_t* uniq, const int32_t* offs, const int32_t* pair_tok,
+    const int32_t* n_uniq_dev, int max_uniq, int max_pairs,
+    float* h, uint8_t* q_x_opt, float* s_x_opt,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moeq_expert_gemm_down -- quant(a) fused into the down FP8 GEMM of every  */
+/* unique expert, split-K, deterministic fp32 reduction.                    */
+/*   a       [max_pairs, K] bf16 or fp32; row p is the input of pair p      */
+/*           (h from the gate_up call, or x for a dense projection)         */
+/*   w_d     [n_experts, N, K] E4M3;  s_d [n_experts, N/128, K/128] fp32    */
+/*   y       [max_pairs, N] fp32, row p = W_d[expert(p)] applied to a[p]    */
+/*   q_a_opt [max_pairs, K], s_a_opt [max_pairs, K/128]: optional dump of   */
+/*           the fused prologue's codes and scales                          */
+/* A plan for a dense layer is uniq = {0}, offs = {0, M}, n_uniq = 1.       */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_expert_gemm_down(
+    const void* a, moeq_dtype a_dtype, int K, int N,
+    const uint8_t* w_d, const float* s_d, int n_experts,
+    const int32_t* uniq, const int32_t* offs, const int32_t* n_uniq_dev,
+    int max_uniq, int max_pairs,
+    float* y, uint8_t* q_a_opt, float* s_a_opt,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* moeq_combine -- out[m] = bf16_RNE(y[pair_of[m][top_k]] +                 */
+/*   sum_{j < top_k} topk_w[m][j] * y[pair_of[m][j]]), fp32, in slot order. */
+/* y [max_pairs, N] fp32, out [M, N] bf16.  top_k may be 0 (dense layer:    */
+/* pair_of[m][0] is then the only term, weight 1).                          */
+moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k,
+                         void* out_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moeq_moe_layer -- one MoE FFN layer for M tokens:                        */
+/*   route -> [quant x + gate_up + SwiGLU] -> [quant h + down] -> combine   */
+/*   x      [M, H] bf16; logits [M, E_routed] fp32                          */
+/*   w_gu/s_gu, w_d/s_d: E_routed + 1 experts, the shared expert last       */
+/*   out    [M, H] bf16                                                     */
+/*   plan_opt, h_opt [max_pairs, I], y_opt [max_pairs, H]: optional         */
+/*           caller buffers that receive the plan and the intermediates     */
+/*           (NULL: kept in the workspace)                                  */
+/*   events_opt: NULL, or 5 cudaEvent_t recorded on `stream` before the     */
+/*           first kernel and after each of the four stages, for per-stage  */
+/*           timing by the caller                                           */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_moe_layer(const void* x, const float* logits,
+                           int M, int H, int I, int E_routed, int top_k,
+                           const uint8_t* w_gu, const float* s_gu,
+                           const uint8_t* w_d, const float* s_d,
+                           void* out, const moeq_route_plan* plan_opt,
+                           float* h_opt, float* y_opt, void* const* events_opt,
+                           void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEQ_H */

@@ -71,6 +71,7 @@ def lib():
                                 _i32p, _f64p, _i32p, _i32p, _i32p, _i32p, _i32p]
         L.orc_swiglu.restype = ctypes.c_float
         L.orc_swiglu.argtypes = [ctypes.c_double, ctypes.c_double]
+        L.orc_swiglu_vec.argtypes = [_f64p, _f64p, ctypes.c_int, _f32p]
         L.orc_moe_layer.argtypes = [
             _u16p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             _vpp, _vpp, _vpp, _vpp,
@@ -197,6 +198,14 @@ def route(logits: np.ndarray, k: int) -> Route:
 
 def swiglu(gate: float, up: float) -> float:
     return float(lib().orc_swiglu(float(gate), float(up)))
+
+
+def swiglu_vec(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(gate, np.float64).ravel()
+    u = np.ascontiguousarray(up, np.float64).ravel()
+    h = np.zeros(g.size, np.float32)
+    lib().orc_swiglu_vec(g, u, g.size, h)
+    return h.reshape(np.shape(gate))
 
 
 class LayerResult:

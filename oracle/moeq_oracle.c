@@ -88,21 +88,29 @@ uint8_t orc_e4m3_encode_scan(double v)
 }
 
 /* Same result as orc_e4m3_encode_scan, found by bisection over the 126
- * midpoints instead of a scan (used for the large weight tensors). */
+ * midpoints instead of a scan (used for the large weight tensors).  The
+ * midpoints are tabulated from mid_above on every call's entry check, so
+ * the table always reflects the decode definition in force. */
 uint8_t orc_e4m3_encode(double v)
 {
+    static double mids[0x7E];
+    static int mids_fault = -1;
     int neg = signbit(v) ? 1 : 0;
     double a = fabs(v);
     int lo = 0, hi = 0x7D;  /* answer in [lo, hi]: smallest c with a <= mid(c) */
     int c;
-    if (a > mid_above(0x7D)) return (uint8_t)((neg << 7) | 0x7E);
+    if (mids_fault != g_fault) {
+        for (c = 0; c < 0x7E; ++c) mids[c] = mid_above(c);
+        mids_fault = g_fault;
+    }
+    if (a > mids[0x7D]) return (uint8_t)((neg << 7) | 0x7E);
     while (lo < hi) {
         int mc = (lo + hi) / 2;
-        if (a <= mid_above(mc)) hi = mc; else lo = mc + 1;
+        if (a <= mids[mc]) hi = mc; else lo = mc + 1;
     }
     c = lo;
-    if (c < 0x7E && a == mid_above(c) && (c & 1)) c = c + 1;
-    if (g_fault == 2 && c < 0x7E && a == mid_above(c) && !(c & 1)) c = c + 1; /* planted: ties away */
+    if (c < 0x7E && a == mids[c] && (c & 1)) c = c + 1;
+    if (g_fault == 2 && c < 0x7E && a == mids[c] && !(c & 1)) c = c + 1; /* planted: ties away */
     return (uint8_t)((neg << 7) | c);
 }
 
@@ -339,6 +347,13 @@ float orc_swiglu(double gate, double up)
     double silu = gate / (1.0 + exp(-gate));
     if (g_fault == 7) silu = gate / (1.0 + exp(gate));   /* planted: wrong sign */
     return (float)(silu * up);
+}
+
+/* Elementwise SwiGLU over arrays: h[i] = orc_swiglu(gate[i], up[i]). */
+void orc_swiglu_vec(const double* gate, const double* up, int n, float* h)
+{
+    int i;
+    for (i = 0; i < n; ++i) h[i] = orc_swiglu(gate[i], up[i]);
 }
 
 /* ------------------------------------------------------------------------ */
