@@ -76,4 +76,4 @@ def test_quant_weight_bit_exact(orc):
         q_ref, s_ref = ex.oracle(orc, e)
         assert np.array_equal(s[e].view(np.uint32), s_ref.view(np.uint32)), e
         assert np.array_equal(q[e], q_ref), e
-    assert s[0, 1, 2] == 0.0 and not q[0, 128:, 256:].any()
+    assert s[0, 1, 2] == 0.0 and set(np.unique(q[0, 128:, 256:]).tolist()) <= {0x00, 0x80}
