@@ -1,8 +1,6 @@
 // The C ABI of libmoeq (include/moeq.h): argument validation, workspace
-// layout, TMA tensor-map construction and the launch sequence.  Every check
+// layout and the launches.  Every check
 // runs on the host before anything is launched.
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -51,68 +49,54 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 moeq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
 
-// ------------------------------------------------------------------ tensor maps
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
-
-// 2-D map over the FP8 weights seen as [rows, K] bytes, 128 x 128 boxes,
-// no swizzle (each box lands as 128 rows of 128 contiguous bytes).
-bool weight_map(CUtensorMap* map, const uint8_t* w, uint64_t rows, uint64_t K) {
-    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K};
-    cuuint32_t box[2] = {128, 128};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 // ------------------------------------------------------------------ workspace
-// Standalone GEMM workspace: [status int (256 B)] [tickets] [partials].
-struct GemmWs {
-    size_t tickets, partials, end;
+// Header (256 B): status word, epoch, done ticket, route flag.
+constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffRouteFlag = 12, kHeader = 256;
+
+struct StreamWs {
+    size_t tickets[kMaxLists];
+    size_t partials;
+    size_t h_ready, comb, end;
 };
 
-GemmWs gemm_ws_layout(size_t base, int RB, int max_uniq, int nbox, int grid) {
-    GemmWs l;
-    l.tickets = align_up(base, 256);
-    l.partials = align_up(l.tickets + sizeof(int) * static_cast<size_t>(RB) * max_uniq, 256);
-    l.end = l.partials + sizeof(float) * gemm_partials_floats(nbox, grid);
+// Ticket and partial areas for the given lists, starting at `base`.
+StreamWs stream_ws_layout(size_t base, int n_lists, const int* tickets_per_list, int grid, int h_ready_n,
+                          int comb_n) {
+    StreamWs l;
+    size_t off = align_up(base, 256);
+    for (int i = 0; i < kMaxLists; ++i) {
+        l.tickets[i] = off;
+        if (i < n_lists) off = align_up(off + sizeof(int) * static_cast<size_t>(tickets_per_list[i]), 256);
+    }
+    l.partials = off;
+    off = align_up(off + sizeof(float) * stream_partials_floats(grid) * n_lists, 256);
+    l.h_ready = off;
+    off = align_up(off + sizeof(int) * static_cast<size_t>(h_ready_n), 256);
+    l.comb = off;
+    l.end = align_up(off + sizeof(int) * static_cast<size_t>(comb_n), 256);
     return l;
 }
 
 struct LayerWs {
-    size_t plan, h, y, end;
-    GemmWs gu, dn;
+    size_t plan, h, y;
+    StreamWs s;
 };
 
 LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     LayerWs l;
     const int mu = moeq_max_uniq(M, E, k), mp = moeq_max_pairs(M, k);
-    l.plan = 256;
+    l.plan = kHeader;
     l.h = align_up(l.plan + moeq_route_plan_bytes(M, E, k), 256);
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
     const size_t after = l.y + sizeof(float) * static_cast<size_t>(mp) * H;
-    l.gu = gemm_ws_layout(after, I / 128, mu, 2, grid);
-    l.dn = gemm_ws_layout(l.gu.end, H / 128, mu, 1, grid);
-    l.end = l.dn.end;
+    const int tk[4] = {I / 128, mu * (I / 128), H / 128, mu * (H / 128)};
+    l.s = stream_ws_layout(after, 4, tk, grid, mu * (I / 128), M * (H / 128));
     return l;
+}
+
+StreamWs gemm_ws_layout(int RB, int max_uniq, int grid) {
+    const int tk[1] = {RB * max_uniq};
+    return stream_ws_layout(kHeader, 1, tk, grid, 0, 0);
 }
 
 struct PlanLayout {
@@ -142,41 +126,16 @@ bool plan_ok(const moeq_route_plan* p) {
     return p && p->topk_id && p->topk_w && p->n_uniq && p->uniq && p->offs && p->pair_tok && p->pair_of;
 }
 
-// Shared body of the two GEMM calls, after their own argument checks.
-moeq_status run_gemm(const void* a, int a_f32, const int32_t* a_row, int K, int rows_per_expert, int up_offset,
-                     int RB, int nbox, const uint8_t* w, const float* sw, int n_experts, const int32_t* uniq,
-                     const int32_t* offs, const int32_t* n_uniq, int max_uniq, int max_pairs, int rows_a,
-                     float* out, int out_ld,
-                     uint8_t* qdump, float* sdump, void* ws, const GemmWs& wl, const DeviceInfo& dev,
-                     cudaStream_t stream) {
-    CUtensorMap map;
-    if (!weight_map(&map, w, static_cast<uint64_t>(n_experts) * rows_per_expert, static_cast<uint64_t>(K)))
-        return MOEQ_ERR_CUDA;
-    GemmArgs g;
-    g.a = a;
-    g.a_f32 = a_f32;
-    g.a_row = a_row;
-    g.K = K;
-    g.rows_per_expert = rows_per_expert;
-    g.up_offset = up_offset;
-    g.RB = RB;
-    g.sw = sw;
-    g.uniq = uniq;
-    g.offs = offs;
-    g.n_uniq = n_uniq;
-    g.out = out;
-    g.out_ld = out_ld;
-    g.qdump = qdump;
-    g.sdump = sdump;
+void fill_ws(StreamArgs& a, void* ws, const StreamWs& l) {
     char* base = static_cast<char*>(ws);
-    g.tickets = reinterpret_cast<int*>(base + wl.tickets);
-    g.partials = reinterpret_cast<float*>(base + wl.partials);
-    g.status = reinterpret_cast<int*>(base);
-    g.n_experts = n_experts;
-    g.max_uniq = max_uniq;
-    g.max_pairs = max_pairs;
-    g.rows_a = rows_a;
-    return cuda_status(launch_expert_gemm(map, g, nbox, dev.sms, stream));
+    a.status = reinterpret_cast<int*>(base + kOffStatus);
+    a.epoch = reinterpret_cast<int*>(base + kOffEpoch);
+    a.done = reinterpret_cast<int*>(base + kOffDone);
+    a.route_flag = reinterpret_cast<int*>(base + kOffRouteFlag);
+    for (int i = 0; i < kMaxLists; ++i) a.tickets[i] = reinterpret_cast<int*>(base + l.tickets[i]);
+    a.partials = reinterpret_cast<float*>(base + l.partials);
+    a.h_ready = reinterpret_cast<int*>(base + l.h_ready);
+    a.comb = reinterpret_cast<int*>(base + l.comb);
 }
 
 }  // namespace
@@ -236,23 +195,24 @@ size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int t
         return 0;
     const DeviceInfo dev = current_device();
     if (!dev.sms) return 0;
-    return layer_ws_layout(M, H, I, E, top_k, dev.sms).end;
+    return layer_ws_layout(M, H, I, E, top_k, dev.sms).s.end;
 }
 
 size_t moeq_gemm_workspace_size(int rows_out, int max_uniq, int is_gate_up) {
+    (void)is_gate_up;
     if (rows_out <= 0 || rows_out % 128 || max_uniq < 1) return 0;
     const DeviceInfo dev = current_device();
     if (!dev.sms) return 0;
-    return gemm_ws_layout(256, rows_out / 128, max_uniq, is_gate_up ? 2 : 1, dev.sms).end;
+    return gemm_ws_layout(rows_out / 128, max_uniq, dev.sms).end;
 }
 
 moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
-    if (!ws || ws_bytes < 256 || !aligned16(ws)) return MOEQ_ERR_WORKSPACE;
+    if (!ws || ws_bytes < kHeader || !aligned16(ws)) return MOEQ_ERR_WORKSPACE;
     return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)));
 }
 
 moeq_status moeq_read_device_status(const void* ws, size_t ws_bytes, int* device_status) {
-    if (!ws || ws_bytes < 256 || !device_status) return MOEQ_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < kHeader || !device_status) return MOEQ_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return MOEQ_ERR_CUDA;
     return cuda_status(cudaMemcpy(device_status, ws, sizeof(int), cudaMemcpyDeviceToHost));
 }
@@ -273,6 +233,15 @@ moeq_status moeq_quant_weight(const float* w, int E, int N, int K, uint8_t* q, f
         return MOEQ_ERR_UNSUPPORTED_SHAPE;
     if (!current_device().ok) return MOEQ_ERR_DEVICE;
     return cuda_status(launch_quant_weight(w, E, N, K, q, s, as_stream(stream)));
+}
+
+moeq_status moeq_pack_weight(const uint8_t* q_rows, int E, int N, int K, uint8_t* q_tiles, void* stream) {
+    if (!q_rows || !q_tiles || !aligned16(q_rows) || !aligned16(q_tiles)) return MOEQ_ERR_INVALID_ARG;
+    if (E < 1 || E > 65535) return MOEQ_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || N % 128 || K % 128 || N / 128 > 65535 || K / 128 > 65535)
+        return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    if (!current_device().ok) return MOEQ_ERR_DEVICE;
+    return cuda_status(launch_pack_weight(q_rows, E, N, K, q_tiles, as_stream(stream)));
 }
 
 moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k, const moeq_route_plan* plan,
@@ -296,34 +265,83 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     if (x_dtype != MOEQ_BF16 && x_dtype != MOEQ_F32) return MOEQ_ERR_INVALID_ARG;
     if (M < 1 || M > MOEQ_MAX_TOKENS || n_experts < 1 || max_uniq < 1 || max_pairs < 1) return MOEQ_ERR_INVALID_ARG;
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
-    if (static_cast<long long>(n_experts) * 2 * I >= (1LL << 31)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const GemmWs wl = gemm_ws_layout(256, I / 128, max_uniq, 2, dev.sms);
+    const StreamWs wl = gemm_ws_layout(I / 128, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
-    return run_gemm(x, x_dtype == MOEQ_F32, pair_tok, H, 2 * I, I, I / 128, 2, w_gu, s_gu, n_experts, uniq, offs,
-                    n_uniq_dev, max_uniq, max_pairs, M, h, I, q_x_opt, s_x_opt, ws, wl, dev, as_stream(stream));
+    StreamArgs a = {};
+    Operand& o = a.op[kKindGU];
+    o.w = w_gu;
+    o.sw = s_gu;
+    o.K = H;
+    o.KB = H / 128;
+    o.NB = 2 * I / 128;
+    o.RB = I / 128;
+    o.a = x;
+    o.a_f32 = x_dtype == MOEQ_F32;
+    o.a_row = pair_tok;
+    o.rows_a = M;
+    o.out = h;
+    o.out_ld = I;
+    o.qdump = q_x_opt;
+    o.sdump = s_x_opt;
+    a.n_lists = 1;
+    a.list_kind[0] = kKindGU;
+    a.list_src[0] = kSrcPlanAll;
+    a.n_uniq = n_uniq_dev;
+    a.uniq = uniq;
+    a.offs = offs;
+    a.pair_tok = pair_tok;
+    a.n_experts = n_experts;
+    a.max_uniq = max_uniq;
+    a.max_pairs = max_pairs;
+    a.M = M;
+    fill_ws(a, ws, wl);
+    return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
 }
 
-moeq_status moeq_expert_gemm_down(const void* a, moeq_dtype a_dtype, int K, int N, const uint8_t* w_d,
+moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, int N, const uint8_t* w_d,
                                   const float* s_d, int n_experts, const int32_t* uniq, const int32_t* offs,
                                   const int32_t* n_uniq_dev, int max_uniq, int max_pairs, float* y, uint8_t* q_a_opt,
                                   float* s_a_opt, void* ws, size_t ws_bytes, void* stream) {
-    if (!a || !w_d || !s_d || !uniq || !offs || !n_uniq_dev || !y) return MOEQ_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(w_d) || !aligned16(y) || !aligned4(s_d)) return MOEQ_ERR_INVALID_ARG;
+    if (!a_in || !w_d || !s_d || !uniq || !offs || !n_uniq_dev || !y) return MOEQ_ERR_INVALID_ARG;
+    if (!aligned16(a_in) || !aligned16(w_d) || !aligned16(y) || !aligned4(s_d)) return MOEQ_ERR_INVALID_ARG;
     if ((q_a_opt == nullptr) != (s_a_opt == nullptr)) return MOEQ_ERR_INVALID_ARG;
     if (q_a_opt && !aligned16(q_a_opt)) return MOEQ_ERR_INVALID_ARG;
     if (a_dtype != MOEQ_BF16 && a_dtype != MOEQ_F32) return MOEQ_ERR_INVALID_ARG;
     if (n_experts < 1 || max_uniq < 1 || max_pairs < 1) return MOEQ_ERR_INVALID_ARG;
     if (K <= 0 || N <= 0 || K % 128 || N % 128 || K > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
-    if (static_cast<long long>(n_experts) * N >= (1LL << 31)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const GemmWs wl = gemm_ws_layout(256, N / 128, max_uniq, 1, dev.sms);
+    const StreamWs wl = gemm_ws_layout(N / 128, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
-    return run_gemm(a, a_dtype == MOEQ_F32, nullptr, K, N, 0, N / 128, 1, w_d, s_d, n_experts, uniq, offs,
-                    n_uniq_dev, max_uniq, max_pairs, max_pairs, y, N, q_a_opt, s_a_opt, ws, wl, dev,
-                    as_stream(stream));
+    StreamArgs a = {};
+    Operand& o = a.op[kKindDN];
+    o.w = w_d;
+    o.sw = s_d;
+    o.K = K;
+    o.KB = K / 128;
+    o.NB = N / 128;
+    o.RB = N / 128;
+    o.a = a_in;
+    o.a_f32 = a_dtype == MOEQ_F32;
+    o.a_row = nullptr;
+    o.rows_a = max_pairs;
+    o.out = y;
+    o.out_ld = N;
+    o.qdump = q_a_opt;
+    o.sdump = s_a_opt;
+    a.n_lists = 1;
+    a.list_kind[0] = kKindDN;
+    a.list_src[0] = kSrcPlanAll;
+    a.n_uniq = n_uniq_dev;
+    a.uniq = uniq;
+    a.offs = offs;
+    a.n_experts = n_experts;
+    a.max_uniq = max_uniq;
+    a.max_pairs = max_pairs;
+    fill_ws(a, ws, wl);
+    return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
 }
 
 moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k, void* out_bf16,
@@ -346,42 +364,82 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     if (plan_opt && !plan_ok(plan_opt)) return MOEQ_ERR_INVALID_ARG;
     if (!route_args_ok(M, E_routed, top_k)) return MOEQ_ERR_INVALID_ARG;
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K || I > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
-    const long long n_exp = static_cast<long long>(E_routed) + 1;
-    if (n_exp * 2 * I >= (1LL << 31) || n_exp * H >= (1LL << 31)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
     const LayerWs l = layer_ws_layout(M, H, I, E_routed, top_k, dev.sms);
-    if (!ws || !aligned16(ws) || ws_bytes < l.end) return MOEQ_ERR_WORKSPACE;
+    if (!ws || !aligned16(ws) || ws_bytes < l.s.end) return MOEQ_ERR_WORKSPACE;
 
     char* base = static_cast<char*>(ws);
     moeq_route_plan plan;
-    if (plan_opt) {
+    if (plan_opt)
         plan = *plan_opt;
-    } else {
+    else
         moeq_route_plan_carve(base + l.plan, l.h - l.plan, M, E_routed, top_k, &plan);
-    }
     float* h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
     float* y = y_opt ? y_opt : reinterpret_cast<float*>(base + l.y);
-    const int mu = moeq_max_uniq(M, E_routed, top_k);
-    cudaStream_t st = as_stream(stream);
-    auto mark = [&](int i) -> cudaError_t {
-        return events_opt ? cudaEventRecord(static_cast<cudaEvent_t>(events_opt[i]), st) : cudaSuccess;
-    };
+    const int mu = moeq_max_uniq(M, E_routed, top_k), mp = moeq_max_pairs(M, top_k);
 
-    if (mark(0) != cudaSuccess) return MOEQ_ERR_CUDA;
-    if (launch_route(logits, M, E_routed, top_k, plan, st) != cudaSuccess) return MOEQ_ERR_CUDA;
-    if (mark(1) != cudaSuccess) return MOEQ_ERR_CUDA;
-    const int mp = moeq_max_pairs(M, top_k);
-    moeq_status s = run_gemm(x, 0, plan.pair_tok, H, 2 * I, I, I / 128, 2, w_gu, s_gu, E_routed + 1, plan.uniq,
-                             plan.offs, plan.n_uniq, mu, mp, M, h, I, nullptr, nullptr, ws, l.gu, dev, st);
-    if (s != MOEQ_OK) return s;
-    if (mark(2) != cudaSuccess) return MOEQ_ERR_CUDA;
-    s = run_gemm(h, 1, nullptr, I, H, 0, H / 128, 1, w_d, s_d, E_routed + 1, plan.uniq, plan.offs, plan.n_uniq, mu,
-                 mp, mp, y, H, nullptr, nullptr, ws, l.dn, dev, st);
-    if (s != MOEQ_OK) return s;
-    if (mark(3) != cudaSuccess) return MOEQ_ERR_CUDA;
-    if (launch_combine(y, H, plan, M, top_k, out, st) != cudaSuccess) return MOEQ_ERR_CUDA;
-    if (mark(4) != cudaSuccess) return MOEQ_ERR_CUDA;
+    StreamArgs a = {};
+    Operand& g = a.op[kKindGU];
+    g.w = w_gu;
+    g.sw = s_gu;
+    g.K = H;
+    g.KB = H / 128;
+    g.NB = 2 * I / 128;
+    g.RB = I / 128;
+    g.a = x;
+    g.a_f32 = 0;
+    g.a_row = plan.pair_tok;
+    g.rows_a = M;
+    g.out = h;
+    g.out_ld = I;
+    Operand& d = a.op[kKindDN];
+    d.w = w_d;
+    d.sw = s_d;
+    d.K = I;
+    d.KB = I / 128;
+    d.NB = H / 128;
+    d.RB = H / 128;
+    d.a = h;
+    d.a_f32 = 1;
+    d.a_row = nullptr;
+    d.rows_a = mp;
+    d.out = y;
+    d.out_ld = H;
+    a.n_lists = 4;
+    const int kinds[4] = {kKindGU, kKindGU, kKindDN, kKindDN};
+    const int srcs[4] = {kSrcShared, kSrcPlanRouted, kSrcShared, kSrcPlanRouted};
+    for (int i = 0; i < 4; ++i) {
+        a.list_kind[i] = kinds[i];
+        a.list_src[i] = srcs[i];
+    }
+    a.n_uniq = plan.n_uniq;
+    a.uniq = plan.uniq;
+    a.offs = plan.offs;
+    a.pair_tok = plan.pair_tok;
+    a.pair_of = plan.pair_of;
+    a.topk_w = plan.topk_w;
+    a.n_experts = E_routed + 1;
+    a.max_uniq = mu;
+    a.max_pairs = mp;
+    a.shared_id = E_routed;
+    a.shared_p0 = M * top_k;
+    a.M = M;
+    a.fused_route = 1;
+    a.logits = logits;
+    a.E_routed = E_routed;
+    a.top_k = top_k;
+    a.plan = plan;
+    a.fused_combine = 1;
+    a.out_bf16 = static_cast<__nv_bfloat16*>(out);
+    fill_ws(a, ws, l.s);
+
+    cudaStream_t st = as_stream(stream);
+    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
+    if (launch_stream(a, dev.sms, true, st) != cudaSuccess) return MOEQ_ERR_CUDA;
+    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
     return MOEQ_OK;
 }
 

@@ -89,6 +89,34 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 1-D bulk copy of `bytes` (multiple of 16, 16-byte aligned ends) into
+// shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// gpu-scope acquire load / release store of a flag in global memory.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -131,15 +159,16 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Load 4 consecutive activation elements (k .. k+3) of row `row` as fp32.
+// Load 4 consecutive activation elements (k .. k+3) of row `row` as fp32,
+// through L2 (coherent with writes by other CTAs of the same kernel).
 template <bool kF32>
 __device__ __forceinline__ float4 load_act4(const void* a, size_t ld, int row, int k) {
     if (kF32) {
         const float* p = static_cast<const float*>(a) + static_cast<size_t>(row) * ld + k;
-        return __ldg(reinterpret_cast<const float4*>(p));
+        return __ldcg(reinterpret_cast<const float4*>(p));
     } else {
         const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(a) + static_cast<size_t>(row) * ld + k;
-        uint2 raw = __ldg(reinterpret_cast<const uint2*>(p));
+        uint2 raw = __ldcg(reinterpret_cast<const uint2*>(p));
         float4 r;
         r.x = __uint_as_float(raw.x << 16);
         r.y = __uint_as_float(raw.x & 0xFFFF0000u);

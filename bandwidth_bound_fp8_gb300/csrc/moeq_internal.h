@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -11,44 +12,75 @@
 
 namespace moeq {
 
-// Geometry of one expert-GEMM launch (gate_up or down).
-struct GemmArgs {
-    const void* a;              // activations [rows_a, K] bf16 or fp32
-    int a_f32;                  // 1: fp32, 0: bf16
-    const int32_t* a_row;       // row of `a` used by pair p; nullptr = p itself
-    int K;                      // reduction length (multiple of 128)
-    int rows_per_expert;        // rows of one expert's weight matrix (2I or N)
-    int up_offset;              // gate_up: row offset of the up half (I); down: 0
-    int RB;                     // 128-row output blocks per expert (I/128 or N/128)
-    const float* sw;            // weight scales [E, rows_per_expert/128, K/128]
-    const int32_t* uniq;        // plan
-    const int32_t* offs;
-    const int32_t* n_uniq;
-    float* out;                 // [max_pairs, out_ld]
+constexpr int kMaxTokens = MOEQ_MAX_TOKENS;
+constexpr int kMaxLists = 4;
+constexpr int kKindGU = 0;  // gate_up: a stage holds the gate tile and the up tile of one K group
+constexpr int kKindDN = 1;  // down: a stage holds two consecutive K tiles of one row block
+constexpr int kSrcShared = 0;     // the layer's shared expert, known before routing
+constexpr int kSrcPlanAll = 1;    // every unique expert of the plan (standalone calls)
+constexpr int kSrcPlanRouted = 2; // the plan's routed experts (all but the last)
+
+// One GEMM operand set.  Weights are tile-major: tile (e, nb, kb) -- the
+// 128 x 128 block of rows nb*128.. and columns kb*128.. of expert e -- is 16
+// KiB at w + ((e * NB + nb) * KB + kb) * 16384, rows of 128 bytes, the 16-byte
+// chunk c of row r stored at chunk c ^ (r % 8).
+struct Operand {
+    const uint8_t* w;
+    const float* sw;      // [E, NB, KB]
+    int K, KB, NB, RB;    // RB = output row blocks per expert (I/128 for gate_up, N/128 for down)
+    const void* a;        // activations [rows_a, K], bf16 or fp32
+    int a_f32;
+    const int32_t* a_row; // gate_up: row of `a` used by pair p (pair_tok); nullptr = p
+    int rows_a;
+    float* out;           // [max_pairs, out_ld]
     int out_ld;
-    uint8_t* qdump;             // optional [rows_a, K]
-    float* sdump;               // optional [rows_a, K/128]
-    int* tickets;               // [max_uniq * RB], zero between launches
-    float* partials;            // [2 * grid, kMaxTok, rows per unit]
-    int* status;                // device status word
-    int n_experts;              // experts in the weight tensor (plan ids must be below)
-    int max_uniq;               // plan capacity: U read on the device is clamped to it
-    int max_pairs;              // rows of `out`
-    int rows_a;                 // rows of `a`
+    uint8_t* qdump;       // optional [rows_a, K]
+    float* sdump;         // optional [rows_a, K/128]
 };
 
-constexpr int kMaxTokens = MOEQ_MAX_TOKENS;
+struct StreamArgs {
+    Operand op[2];
+    int n_lists;
+    int list_kind[kMaxLists];
+    int list_src[kMaxLists];
+    // plan (device)
+    const int32_t* n_uniq;
+    const int32_t* uniq;
+    const int32_t* offs;
+    const int32_t* pair_tok;
+    const int32_t* pair_of;
+    const float* topk_w;
+    int n_experts, max_uniq, max_pairs;
+    // the layer's shared expert (id, first pair, token count)
+    int shared_id, shared_p0, M;
+    // layer fusion
+    int fused_route;          // CTA 0 computes the plan, the others wait for route_flag
+    const float* logits;
+    int E_routed, top_k;
+    moeq_route_plan plan;     // writable plan (fused route)
+    int fused_combine;        // the down epilogue also writes out_bf16
+    __nv_bfloat16* out_bf16;
+    // workspace
+    int* status;
+    int* epoch;
+    int* done;
+    int* route_flag;
+    int* tickets[kMaxLists];
+    float* partials;          // per list: 2 * grid slots of kMaxTokens * 256 floats
+    size_t partial_list_floats;
+    int* h_ready;             // [max_uniq, RB of gate_up]: epoch of the last write of h
+    int* comb;                // [M, RB of down]
+};
 
-// Expert GEMM with fused activation quantisation.  nbox = 2: gate_up with
-// SwiGLU epilogue; nbox = 1: plain output.
-cudaError_t launch_expert_gemm(const CUtensorMap& map, const GemmArgs& args, int nbox, int grid,
-                               cudaStream_t stream);
-size_t gemm_partials_floats(int nbox, int grid);
+size_t stream_partials_floats(int grid);
+cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);
 
 cudaError_t launch_quant_act(const void* x, int x_f32, int M, int K, uint8_t* q, float* s,
                              cudaStream_t stream);
 cudaError_t launch_quant_weight(const float* w, int E, int N, int K, uint8_t* q, float* s,
                                 cudaStream_t stream);
+cudaError_t launch_pack_weight(const uint8_t* q_rows, int E, int N, int K, uint8_t* q_tiles,
+                               cudaStream_t stream);
 cudaError_t launch_route(const float* logits, int M, int E, int k, const moeq_route_plan& plan,
                          cudaStream_t stream);
 cudaError_t launch_combine(const float* y, int N, const moeq_route_plan& plan, int M, int k,

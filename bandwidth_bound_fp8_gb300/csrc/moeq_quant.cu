@@ -36,9 +36,14 @@ cudaError_t launch_quant_act(const void* x, int x_f32, int M, int K, uint8_t* q,
     return cudaGetLastError();
 }
 
+// Byte offset of element (r, k) of a tile: rows of 128 bytes, the 16-byte
+// chunk k/16 of row r stored at chunk (k/16) ^ (r % 8).
+__device__ __forceinline__ int tile_chunk(int r, int chunk) { return r * 128 + ((chunk ^ (r & 7)) << 4); }
+
 // One block of 256 threads per 128 x 128 weight block.  Each thread owns
 // half a row (64 consecutive elements): thread t -> row t/2, columns
-// (t%2)*64 .. +63.  amax over the block, s = fl32(amax/448), then codes.
+// (t%2)*64 .. +63.  amax over the block, s = fl32(amax/448), then codes,
+// written tile-major (see the layout in moeq_internal.h).
 __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restrict__ w, int N, int K,
                                                            uint8_t* __restrict__ q, float* __restrict__ s) {
     __shared__ float red[8];
@@ -67,7 +72,8 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restri
     }
     __syncthreads();
     const float sc = __fdiv_rn(red[0], 448.0f);
-    if (t == 0) s[(static_cast<size_t>(e) * NB + nb) * KB + kb] = sc;
+    const size_t tile = (static_cast<size_t>(e) * NB + nb) * KB + kb;
+    if (t == 0) s[tile] = sc;
     uint32_t out[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -80,15 +86,36 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const float* __restri
             out[i] = static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
         }
     }
-    uint4* dst = reinterpret_cast<uint4*>(q + base);
+    uint8_t* dst = q + tile * (kGroup * kGroup);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4*>(dst + tile_chunk(r, (c0 >> 4) + i)) =
+            make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
 }
 
 cudaError_t launch_quant_weight(const float* w, int E, int N, int K, uint8_t* q, float* s,
                                 cudaStream_t stream) {
     dim3 grid(K / kGroup, N / kGroup, E);
     quant_weight_kernel<<<grid, 256, 0, stream>>>(w, N, K, q, s);
+    return cudaGetLastError();
+}
+
+// Row-major codes [E, N, K] -> the tile-major layout (a pure permutation).
+__global__ void __launch_bounds__(256) pack_weight_kernel(const uint8_t* __restrict__ src, int N, int K,
+                                                          uint8_t* __restrict__ dst) {
+    const int kb = blockIdx.x, nb = blockIdx.y, e = blockIdx.z;
+    const int KB = K / kGroup, NB = N / kGroup;
+    const int t = threadIdx.x, r = t >> 1, c0 = (t & 1) * 64;
+    const uint4* in = reinterpret_cast<const uint4*>(
+        src + (static_cast<size_t>(e) * N + static_cast<size_t>(nb) * kGroup + r) * K + static_cast<size_t>(kb) * kGroup + c0);
+    uint8_t* out = dst + ((static_cast<size_t>(e) * NB + nb) * KB + kb) * (kGroup * kGroup);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(out + tile_chunk(r, (c0 >> 4) + i)) = __ldg(in + i);
+}
+
+cudaError_t launch_pack_weight(const uint8_t* q_rows, int E, int N, int K, uint8_t* q_tiles, cudaStream_t stream) {
+    dim3 grid(K / kGroup, N / kGroup, E);
+    pack_weight_kernel<<<grid, 256, 0, stream>>>(q_rows, N, K, q_tiles);
     return cudaGetLastError();
 }
 

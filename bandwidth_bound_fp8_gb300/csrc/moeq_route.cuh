@@ -1,0 +1,151 @@
+// Routing plan computation shared by the standalone route kernel and the
+// fused layer kernel (where one CTA computes it while the others already
+// stream the shared expert).  GLM-5.2 x10, bandwidth model: every token
+// activates its top-8 experts; §5-§6: tokens verified in one pass share one
+// read of each expert, so the plan lists each expert once with its tokens.
+//
+// Definition (the page fixes none of it; this library's reading):
+//   topk_id[m, j]: the j-th largest logit of token m, ties to the lower id;
+//   topk_w[m, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k picks;
+//   uniq: routed experts in ascending id, then the shared expert (id E);
+//   offs/pair_tok: the pairs of each unique expert, tokens ascending;
+//   pair_of[m, j]: the pair of (token m, slot j), slot k = shared.
+#pragma once
+
+#include <float.h>
+
+#include "moeq_device.cuh"
+
+namespace moeq {
+
+constexpr int kRouteMaxE = MOEQ_MAX_EXPERTS;
+constexpr int kRouteMaxK = MOEQ_MAX_TOPK;
+
+struct RouteScratch {
+    int id[MOEQ_MAX_TOKENS][kRouteMaxK];
+    float lv[MOEQ_MAX_TOKENS][kRouteMaxK];
+    int cnt[kRouteMaxE];
+    int poff[kRouteMaxE];
+    int total[2];
+};
+
+// Computes the plan with NT threads (tid in [0, NT)); `sync` is a barrier
+// over exactly those threads.  Writes every plan member to global memory;
+// the caller makes the writes visible (fence + flag) as it needs.
+template <int NT, typename Sync>
+__device__ __forceinline__ void route_compute(const float* __restrict__ logits, int M, int E, int k,
+                                              const moeq_route_plan& plan, RouteScratch& s, int tid, Sync sync) {
+    constexpr int kWarps = NT / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += NT) s.cnt[e] = 0;
+
+    for (int m = warp; m < M; m += kWarps) {
+        const float* l = logits + static_cast<size_t>(m) * E;
+        constexpr int kPer = kRouteMaxE / 32;
+        float v[kPer];
+        uint32_t taken = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? __ldcg(l + e) : -FLT_MAX;
+        }
+        const int nper = (E + 31) / 32;
+        for (int j = 0; j < k; ++j) {
+            float bv = -FLT_MAX;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                if (i < nper) {
+                    const int e = lane + 32 * i;
+                    if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+                        bv = v[i];
+                        be = e;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            if (lane == 0) {
+                s.id[m][j] = be;
+                s.lv[m][j] = bv;
+            }
+            __syncwarp();
+        }
+        float ex = 0.0f;
+        if (lane < k) ex = expf(s.lv[m][lane] - s.lv[m][0]);
+        float den = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane < k) {
+            plan.topk_id[m * k + lane] = s.id[m][lane];
+            plan.topk_w[m * k + lane] = __fdiv_rn(ex, den);
+        }
+    }
+    sync();
+    for (int i = tid; i < M * k; i += NT) atomicAdd(&s.cnt[s.id[i / k][i % k]], 1);
+    sync();
+    if (warp == 0) {
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per;
+        int used = 0, pairs = 0;
+        for (int e = e0; e < min(E, e0 + per); ++e) {
+            used += s.cnt[e] > 0;
+            pairs += s.cnt[e];
+        }
+        int used_x = used, pairs_x = pairs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, used_x, o);
+            const int b = __shfl_up_sync(0xffffffffu, pairs_x, o);
+            if (lane >= o) {
+                used_x += a;
+                pairs_x += b;
+            }
+        }
+        int u = used_x - used, p = pairs_x - pairs;
+        for (int e = e0; e < min(E, e0 + per); ++e) {
+            s.poff[e] = p;
+            if (s.cnt[e] > 0) {
+                plan.uniq[u] = e;
+                plan.offs[u] = p;
+                ++u;
+            }
+            p += s.cnt[e];
+        }
+        if (lane == 31) {
+            s.total[0] = used_x;
+            s.total[1] = pairs_x;
+        }
+    }
+    sync();
+    for (int i = tid; i < M * k; i += NT) {
+        const int m = i / k, j = i % k, e = s.id[m][j];
+        int rank = 0;
+        for (int m2 = 0; m2 < m; ++m2)
+            for (int j2 = 0; j2 < k; ++j2) rank += s.id[m2][j2] == e;
+        const int p = s.poff[e] + rank;
+        plan.pair_tok[p] = m;
+        plan.pair_of[m * (k + 1) + j] = p;
+    }
+    const int U = s.total[0], P = s.total[1];
+    for (int m = tid; m < M; m += NT) {
+        plan.pair_tok[P + m] = m;
+        plan.pair_of[m * (k + 1) + k] = P + m;
+    }
+    if (tid == 0) {
+        plan.uniq[U] = E;
+        plan.offs[U] = P;
+        plan.offs[U + 1] = P + M;
+        *plan.n_uniq = U + 1;
+    }
+}
+
+}  // namespace moeq

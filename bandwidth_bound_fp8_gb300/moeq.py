@@ -33,7 +33,7 @@ EXPORTS = [
     "moeq_status_string", "moeq_abi_version", "moeq_max_uniq", "moeq_max_pairs",
     "moeq_route_plan_bytes", "moeq_route_plan_carve", "moeq_workspace_size",
     "moeq_gemm_workspace_size", "moeq_workspace_init", "moeq_read_device_status",
-    "moeq_quant_act", "moeq_quant_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
+    "moeq_quant_act", "moeq_quant_weight", "moeq_pack_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
     "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer",
 ]
 
@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
         "moeq_read_device_status": (_i, [_vp, _sz, ctypes.POINTER(_i)]),
         "moeq_quant_act": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
         "moeq_quant_weight": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+        "moeq_pack_weight": (_i, [_vp, _i, _i, _i, _vp, _vp]),
         "moeq_route": (_i, [_vp, _i, _i, _i, ctypes.POINTER(moeq_route_plan), _vp]),
         "moeq_expert_gemm_gateup_swiglu": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp,
                                                 _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -220,6 +221,11 @@ def moeq_quant_weight(w, q, s, stream=None) -> None:
     _check("moeq_quant_weight", load().moeq_quant_weight(_p(w), E, N, K, _p(q), _p(s), _stream(stream)))
 
 
+def moeq_pack_weight(q_rows, q_tiles, stream=None) -> None:
+    E, N, K = q_rows.shape
+    _check("moeq_pack_weight", load().moeq_pack_weight(_p(q_rows), E, N, K, _p(q_tiles), _stream(stream)))
+
+
 def moeq_route(logits, plan: RoutePlan, top_k: int, stream=None) -> None:
     M, E = logits.shape
     _check("moeq_route", load().moeq_route(_p(logits), M, E, top_k, ctypes.byref(plan.c), _stream(stream)))
@@ -254,7 +260,9 @@ def moeq_moe_layer(x, logits, H, I, E_routed, top_k, w_gu, s_gu, w_d, s_d, out, 
         handles = [e.cuda_event for e in events]
         if not all(handles):
             raise ValueError("moeq_moe_layer: events must be created (recorded once) before use")
-        ev = (ctypes.c_void_p * 5)(*handles)
+        if len(handles) != 2:
+            raise ValueError("moeq_moe_layer: events must be two created events (before, after)")
+        ev = (ctypes.c_void_p * 2)(*handles)
     _check("moeq_moe_layer", load().moeq_moe_layer(
         _p(x), _p(logits), M, H, I, E_routed, top_k, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(out),
         ctypes.byref(plan.c) if plan is not None else None, _p(h), _p(y), ev, ws.ptr, ws.nbytes,

@@ -12,8 +12,8 @@ seeded token batches, so every step reads its ~340 MB (M = 1) cold from HBM
 
 Headline metric: effective weight bandwidth = unique weight + scale bytes
 the step touches / step time, in GB/s, at M = 1; the sweep key adds
-M = 1, 2, 4, 8, 16.  `roofline` reports the dominant kernel (the gate_up
-GEMM) against the measured HBM copy bandwidth; `e2e` is the same metric
+M = 1, 2, 4, 8, 16.  `roofline` reports the one kernel of the step (the fused
+layer kernel) against the measured HBM copy bandwidth; `e2e` is the same metric
 with the per-step host->device copy of x and logits and the device->host
 copy of the output inside the timed region; `cpu_baseline` is the oracle
 (test infrastructure, single-threaded C) on one M = 1 layer.
@@ -44,8 +44,8 @@ import synth  # noqa: E402
 METRIC = "FP8 quant+MoE expert GEMM: weight GB/s and % of HBM peak at M=1/4/16"
 CFG = synth.MOE_LAYER
 H, I, E, TOPK = CFG["H"], CFG["I"], CFG["E"], CFG["top_k"]
-GU_BYTES = 2 * I * H + (2 * I // 128) * (H // 128) * 4      # 25,171,968
-DN_BYTES = H * I + (H // 128) * (I // 128) * 4              # 12,585,984
+GU_BYTES = 2 * I * H + (2 * I // 128) * (H // 128) * 4      # 25,171,968 per expert
+DN_BYTES = H * I + (H // 128) * (I // 128) * 4              # 12,585,984 per expert
 EXPERT_BYTES = GU_BYTES + DN_BYTES                          # 37,757,952
 
 
@@ -230,7 +230,7 @@ def make_events(steps, events_every):
     recs = []
     if events_every:
         for _ in range(0, steps, events_every):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
             for e in ev:
                 e.record()
             recs.append(ev)
@@ -275,15 +275,13 @@ def bench_M(stack, M, steps, warmup, ws_world, seed, events_every=8):
     if moeq.moeq_read_device_status(ws.t, ws.nbytes) != 0:
         raise RuntimeError("device status word set during the bench")
     byts = sum(U[(warmup + i) % pool] * EXPERT_BYTES for i in range(steps))
-    stage_ms = [[], [], [], []]
-    gu_bytes = []
+    k_ms, k_bytes = [], []
     for k, ev in enumerate(recs):
-        for si in range(4):
-            stage_ms[si].append(ev[si].elapsed_time(ev[si + 1]))
-        gu_bytes.append(U[(warmup + k * events_every) % pool] * GU_BYTES)
+        k_ms.append(ev[0].elapsed_time(ev[1]))
+        k_bytes.append(U[(warmup + k * events_every) % pool] * EXPERT_BYTES)
     return dict(ms=ms, bytes=byts, steps=steps, U_mean=float(np.mean([U[(warmup + i) % pool] for i in range(steps)])),
-                stage_ms=[float(np.mean(s)) if s else None for s in stage_ms],
-                gu_bytes_mean=float(np.mean(gu_bytes)) if gu_bytes else None, wall=(wall0, wall1),
+                kernel_ms=float(np.mean(k_ms)) if k_ms else None,
+                kernel_bytes=float(np.mean(k_bytes)) if k_bytes else None, wall=(wall0, wall1),
                 xs=xs, lg=lg, U=U, ws=ws)
 
 
@@ -441,12 +439,12 @@ def main():
     value = total_bytes / (ms * 1e-3) / 1e9
     clocks = clk.summary(*r["wall"])
 
-    gu_ms = r["stage_ms"][1]
-    achieved = r["gu_bytes_mean"] / (gu_ms * 1e-3) / 1e9 if gu_ms else None
-    roof = {"bound": "hbm", "kernel": "expert_gemm_kernel<2> (gate_up + SwiGLU)", "achieved": round(achieved, 1),
-            "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic("gateup", args.M),
-            "algorithmic_bytes_per_launch": r["gu_bytes_mean"], "ms_per_launch": round(gu_ms, 5)}
+    k_ms = r["kernel_ms"]
+    achieved = r["kernel_bytes"] / (k_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "stream_kernel (whole MoE layer: route, gate_up+SwiGLU, down, combine)",
+            "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy), of {peak_kind}",
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": ncu_traffic("layer", args.M),
+            "algorithmic_bytes_per_launch": r["kernel_bytes"], "ms_per_launch": round(k_ms, 5)}
 
     sweep = {}
     if not args.no_sweep and rank == 0:
@@ -457,7 +455,7 @@ def main():
             sweep[f"M{M}"] = {"us_per_layer": round(us, 2), "weight_GBps": round(gbs, 1),
                               "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8TBps": round(gbs / 8000, 4),
                               "U_mean": rr["U_mean"],
-                              "stage_us": [round(s * 1e3, 2) if s else None for s in rr["stage_ms"]]}
+                              "kernel_us": round(rr["kernel_ms"] * 1e3, 2)}
             del rr
     e2e = None
     if rank == 0:
@@ -481,12 +479,9 @@ def main():
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(ms * 1e3 / args.steps, 3),
             "frac_of_8TBps": round(value / world / 8000, 4),
-            "stage_us": {"route": r["stage_ms"][0] and round(r["stage_ms"][0] * 1e3, 2),
-                         "gate_up": r["stage_ms"][1] and round(r["stage_ms"][1] * 1e3, 2),
-                         "down": r["stage_ms"][2] and round(r["stage_ms"][2] * 1e3, 2),
-                         "combine": r["stage_ms"][3] and round(r["stage_ms"][3] * 1e3, 2)},
+            "kernel_us": round(r["kernel_ms"] * 1e3, 3),
             "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-            "gpu_launches": 4 * args.steps, "sweep": sweep,
+            "gpu_launches": args.steps, "sweep": sweep,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -21,6 +21,16 @@
  *     s = fl32(amax / 448), q = RNE_satfinite(fl32(x / s)); a group whose
  *     s is 0 gets signed-zero codes;
  *   - weights carry one fp32 scale per 128 x 128 block;
+ *   - weight codes are stored TILE-MAJOR (the HBM layout every GEMM call
+ *     streams): the 128 x 128 block (nb, kb) of expert e -- rows nb*128..,
+ *     columns kb*128.. of its [N, K] matrix -- is one contiguous 16 KiB tile
+ *     at byte offset ((e * N/128 + nb) * K/128 + kb) * 16384; inside a tile
+ *     row r occupies bytes r*128 .. r*128+127 and its 16-byte chunk c (columns
+ *     16c .. 16c+15) sits at chunk position c ^ (r % 8).  Each tile is then
+ *     one sequential 16 KiB read, and the chunk rotation keeps shared-memory
+ *     reads conflict-free.  moeq_quant_weight writes this layout and
+ *     moeq_pack_weight converts row-major codes to it; scales stay row-major
+ *     [E, N/128, K/128];
  *   - GEMMs accumulate in fp32: y = sum_g s_a * s_w * sum_{k in g} q_a * q_w.
  *
  * Conventions for every call:
@@ -136,10 +146,16 @@ moeq_status moeq_quant_act(const void* x, moeq_dtype x_dtype, int M, int K,
                            uint8_t* q, float* s, void* stream);
 
 /* moeq_quant_weight -- offline block quantisation of E expert matrices.    */
-/* w [E, N, K] fp32 -> q [E, N, K] codes, s [E, N/128, K/128] fp32, one     */
-/* scale per 128 x 128 block with the same codec as the activations.        */
+/* w [E, N, K] fp32 row-major -> q: E*N*K codes in the tile-major layout,   */
+/* s [E, N/128, K/128] fp32, one scale per 128 x 128 block with the same    */
+/* codec as the activations (s = fl32(amax/448), RNE, saturating).          */
 moeq_status moeq_quant_weight(const float* w, int E, int N, int K,
                               uint8_t* q, float* s, void* stream);
+
+/* moeq_pack_weight -- row-major E4M3 codes [E, N, K] -> the tile-major      */
+/* layout (a permutation of bytes; q_rows and q_tiles must not overlap).    */
+moeq_status moeq_pack_weight(const uint8_t* q_rows, int E, int N, int K,
+                             uint8_t* q_tiles, void* stream);
 
 /* moeq_route -- top-k routing plus expert deduplication for M tokens.     */
 /* logits [M, E_routed] fp32 -> *plan (see moeq_route_plan).                */
@@ -154,7 +170,8 @@ moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k,
 /* deterministic fp32 reduction, and the SwiGLU epilogue                    */
 /* (GLM-5.2 x10 §1: split-K; §4: quantisation fused into the GEMM).         */
 /*   x       [M, H] bf16 or fp32, M <= MOEQ_MAX_TOKENS                      */
-/*   w_gu    [n_experts, 2I, H] E4M3: gate rows [0, I), up rows [I, 2I)     */
+/*   w_gu    n_experts x [2I, H] E4M3 tile-major: gate rows [0, I), up rows */
+/*           [I, 2I)                                                        */
 /*   s_gu    [n_experts, 2I/128, H/128] fp32                                */
 /*   uniq/offs/pair_tok/n_uniq_dev: the plan (device), U read on the device */
 /*   h       [max_pairs, I] fp32: h[p] = silu(gate . x[tok(p)]) * (up . x)  */
@@ -176,7 +193,8 @@ moeq_status moeq_expert_gemm_gateup_swiglu(
 /* unique expert, split-K, deterministic fp32 reduction.                    */
 /*   a       [max_pairs, K] bf16 or fp32; row p is the input of pair p      */
 /*           (h from the gate_up call, or x for a dense projection)         */
-/*   w_d     [n_experts, N, K] E4M3;  s_d [n_experts, N/128, K/128] fp32    */
+/*   w_d     n_experts x [N, K] E4M3 tile-major; s_d [n_experts, N/128,     */
+/*           K/128] fp32                                                    */
 /*   y       [max_pairs, N] fp32, row p = W_d[expert(p)] applied to a[p]    */
 /*   q_a_opt [max_pairs, K], s_a_opt [max_pairs, K/128]: optional dump of   */
 /*           the fused prologue's codes and scales                          */
@@ -198,17 +216,23 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
                          void* out_bf16, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* moeq_moe_layer -- one MoE FFN layer for M tokens:                        */
+/* moeq_moe_layer -- one MoE FFN layer for M tokens, in ONE kernel:         */
 /*   route -> [quant x + gate_up + SwiGLU] -> [quant h + down] -> combine   */
+/*   One persistent CTA per SM (cooperative launch): CTA 0 routes while     */
+/*   the others stream the shared expert, gate_up and down stream back to   */
+/*   back, down waits per expert for its h, and the combine runs in the     */
+/*   down epilogue.                                                         */
 /*   x      [M, H] bf16; logits [M, E_routed] fp32                          */
-/*   w_gu/s_gu, w_d/s_d: E_routed + 1 experts, the shared expert last       */
+/*   w_gu/s_gu, w_d/s_d: E_routed + 1 experts (tile-major codes), the       */
+/*           shared expert last                                             */
 /*   out    [M, H] bf16                                                     */
 /*   plan_opt, h_opt [max_pairs, I], y_opt [max_pairs, H]: optional         */
 /*           caller buffers that receive the plan and the intermediates     */
 /*           (NULL: kept in the workspace)                                  */
-/*   events_opt: NULL, or 5 cudaEvent_t recorded on `stream` before the     */
-/*           first kernel and after each of the four stages, for per-stage  */
-/*           timing by the caller                                           */
+/*   events_opt: NULL, or 2 cudaEvent_t recorded on `stream` right before   */
+/*           and right after the layer's kernel, for the caller's timing    */
+/* A workspace serves one layer call at a time: consecutive calls on one    */
+/* stream may share it, concurrent calls may not.                           */
 /* ------------------------------------------------------------------------ */
 moeq_status moeq_moe_layer(const void* x, const float* logits,
                            int M, int H, int I, int E_routed, int top_k,

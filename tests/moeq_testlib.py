@@ -31,14 +31,36 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().numpy()
 
 
+def tiles_to_rows(q_tiles: np.ndarray, E: int, N: int, K: int) -> np.ndarray:
+    """Undo the tile-major weight layout (a byte permutation, no arithmetic):
+    tile (e, nb, kb) holds rows of 128 bytes whose 16-byte chunk c sits at
+    chunk position c ^ (r % 8)."""
+    t = np.asarray(q_tiles, np.uint8).reshape(E, N // 128, K // 128, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    t = t[:, :, :, r, c ^ (r & 7), :]                      # logical chunk order
+    return t.transpose(0, 1, 3, 2, 4, 5).reshape(E, N, K)
+
+
+def rows_to_tiles(q_rows: np.ndarray) -> np.ndarray:
+    """Inverse of tiles_to_rows."""
+    E, N, K = q_rows.shape
+    t = np.asarray(q_rows, np.uint8).reshape(E, N // 128, 128, K // 128, 8, 16).transpose(0, 1, 3, 2, 4, 5)
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    out = np.empty_like(t)
+    out[:, :, :, r, c ^ (r & 7), :] = t
+    return out.reshape(E, N, K)
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return to_np(t.contiguous().view(torch.uint16))
 
 
 class Experts:
     """E expert matrices [N, K] drawn per expert from its own seed, quantised
-    on the GPU by libmoeq; the oracle view re-draws the same fp32 weights and
-    quantises them on the CPU."""
+    on the GPU by libmoeq (codes tile-major in self.q, E*N*K bytes); the
+    oracle view re-draws the same fp32 weights and quantises them on the CPU."""
 
     def __init__(self, E: int, N: int, K: int, base_seed: int, which: int, layer: int = 0,
                  scale_blocks: dict | None = None):

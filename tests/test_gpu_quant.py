@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import synth
-from moeq_testlib import Experts, bf16_bits, to_np
+from moeq_testlib import Experts, bf16_bits, rows_to_tiles, tiles_to_rows, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -71,9 +71,22 @@ def test_quant_act_edge_cases(orc):
 def test_quant_weight_bit_exact(orc):
     ex = Experts(3, 256, 384, base_seed=5, which=0,
                  scale_blocks={(0, 1, 2): 0.0, (1, 0, 0): 1e4, (2, 1, 1): 1e-30})
-    q, s = to_np(ex.q), to_np(ex.s)
+    q, s = tiles_to_rows(to_np(ex.q), 3, 256, 384), to_np(ex.s)
     for e in range(3):
         q_ref, s_ref = ex.oracle(orc, e)
         assert np.array_equal(s[e].view(np.uint32), s_ref.view(np.uint32)), e
         assert np.array_equal(q[e], q_ref), e
     assert s[0, 1, 2] == 0.0 and set(np.unique(q[0, 128:, 256:]).tolist()) <= {0x00, 0x80}
+
+
+def test_pack_weight_is_the_tile_permutation():
+    """moeq_pack_weight moves row-major codes to the tile-major layout; the
+    test's own permutation (tests/moeq_testlib.rows_to_tiles) must agree."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    g = torch.Generator().manual_seed(3)
+    rows = torch.randint(0, 256, (2, 384, 256), generator=g, dtype=torch.uint8)
+    tiles = torch.empty_like(rows).cuda()
+    moeq.moeq_pack_weight(rows.cuda(), tiles)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(tiles), rows_to_tiles(rows.numpy()))
+    assert np.array_equal(tiles_to_rows(to_np(tiles), 2, 384, 256), rows.numpy())
