@@ -126,8 +126,9 @@ bool plan_ok(const moeq_route_plan* p) {
     return p && p->topk_id && p->topk_w && p->n_uniq && p->uniq && p->offs && p->pair_tok && p->pair_of;
 }
 
-void fill_ws(StreamArgs& a, void* ws, const StreamWs& l) {
+void fill_ws(StreamArgs& a, void* ws, const StreamWs& l, int grid) {
     char* base = static_cast<char*>(ws);
+    a.partial_list_floats = stream_partials_floats(grid);
     a.status = reinterpret_cast<int*>(base + kOffStatus);
     a.epoch = reinterpret_cast<int*>(base + kOffEpoch);
     a.done = reinterpret_cast<int*>(base + kOffDone);
@@ -296,7 +297,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.M = M;
-    fill_ws(a, ws, wl);
+    fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
 }
 
@@ -340,7 +341,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.n_experts = n_experts;
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
-    fill_ws(a, ws, wl);
+    fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
 }
 
@@ -432,7 +433,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.plan = plan;
     a.fused_combine = 1;
     a.out_bf16 = static_cast<__nv_bfloat16*>(out);
-    fill_ws(a, ws, l.s);
+    fill_ws(a, ws, l.s, dev.sms);
 
     cudaStream_t st = as_stream(stream);
     if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)

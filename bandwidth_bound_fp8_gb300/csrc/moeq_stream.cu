@@ -17,53 +17,80 @@
 // splits into segments (runs of one row block); only its first and last can
 // be partial in K, so each CTA leaves at most two fp32 partials per list; the
 // last CTA to finish a row block (atomic ticket) sums them in CTA order and
-// runs the epilogue, so results do not depend on timing.
+// runs the epilogue, so results do not depend on timing.  A segment splits
+// into chunks whose quantised activations fit one shared-memory slot.
 //
-// Inside a CTA warp 16 is the producer (one lane issues the bulk copies) and
-// warps 0-15 consume: they quantise the segment's activation groups (per
-// token, 1 x 128, s = amax/448, RNE to E4M3) into shared memory, then each
-// lane takes 16 bytes of a weight row per pass, widens them exactly to fp32
-// and accumulates products with the decoded activation codes in paired fp32
-// FMAs, scaling per K group by s_a * s_w.
+// Warp roles (576 threads):
+//   warps 0-15  consumers: per stage, each lane widens 16 weight bytes of a
+//               row exactly to fp32 and accumulates paired fp32 FMAs with the
+//               decoded activation codes, scaling per K group by s_a * s_w;
+//               at a segment's end they leave one sum per (row, token);
+//   warp 16     producer: one lane issues the bulk copies of every unit;
+//   warp 17     helper: prepares the next chunk (plan lookup, weight scales,
+//               live quantisation of its activation groups: per token, 1 x 128,
+//               s = amax/448, RNE to E4M3) while the consumers stream the
+//               current one, and finishes segments (split-K partials and the
+//               ticketed reduction, SwiGLU or plain store, readiness flags,
+//               the combine) off the streaming path.
+// The roles meet only through mbarriers: the stage ring (full/empty), two
+// activation slots (prep_full/act_empty) and two result slots
+// (res_full/res_empty).
 //
-// Layer fusion (cooperative launch, all CTAs resident): CTA 0 computes the
-// routing plan while the other CTAs stream the shared expert, which needs no
-// routing; gate_up epilogues publish per-(expert, row block) readiness of h;
-// down segments wait (bounded) for their expert's h while their weights are
-// already in flight; the down epilogue that completes the last expert of a
-// (token, row block) also writes the combined bf16 output.
+// Layer fusion (cooperative launch, all CTAs resident): CTA 0's consumers
+// compute the routing plan while the other CTAs stream the shared expert,
+// which needs no routing; gate_up finishes publish per-(expert, row block)
+// readiness of h; the helper waits (bounded) for an expert's h before
+// quantising it for down, while the producer already streams down weights;
+// the down finish that completes the last expert of a (token, row block)
+// also writes the combined bf16 output.  A helper never waits on another CTA
+// while it still owes a segment finish.
 #include "moeq_device.cuh"
 #include "moeq_internal.h"
 #include "moeq_route.cuh"
 
 namespace moeq {
 
-constexpr int kCW = 16;                // consumer warps
+constexpr int kCW = 16;                  // consumer warps
 constexpr int kConsumers = kCW * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarp = kCW;
+constexpr int kHelperWarp = kCW + 1;
+constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kTile = 16384;
 constexpr int kStageBytes = 2 * kTile;
-constexpr int kStages = 5;
-constexpr int kActCap = 6144;          // decoded activation floats in shared memory
-constexpr int kActScaleCap = kActCap / kGroup;
-constexpr int kMaxKG = MOEQ_MAX_K / kGroup;
+constexpr int kStages = 4;
+constexpr int kActSlot = 6144;           // decoded activation floats per slot
+constexpr int kChunkGroups = kActSlot / kGroup;
 constexpr int kAccLd = kMaxTok + 1;
-constexpr int kUnitRows = 256;         // rows of a gate_up unit (gate + up); down units use 128
+constexpr int kUnitRows = 256;           // rows of a gate_up unit (gate + up); down units use 128
+
+struct ChunkDesc {
+    int kind;          // kKindGU / kKindDN; -1: no more work
+    int ku0, ku1;      // units [ku0, ku1) of the segment's row block
+    int g0, ng;        // K groups of this chunk's activations
+    int ntok;
+    int seg_end;       // the segment's last chunk
+};
+
+struct SegMeta {       // what the helper needs to finish a segment
+    int kind, li, e_local, rb, ku0, ku1;
+    int expert, p0, ntok, slot, shared_static, valid;
+    long long T, G, c, lo;
+    int KU, RB;
+};
 
 struct SmemTail {
     union {
-        float act[kActCap];            // decoded activations [tok][group][permuted k]
-        RouteScratch route;            // plan computation (CTA 0, before any activation)
+        float act[2][kActSlot];          // decoded activations [tok][group][permuted k]
+        RouteScratch route;              // plan computation (CTA 0, before any activation)
     };
-    float act_s[kActScaleCap];         // activation scales [tok][group]
-    float sw[2][kMaxKG];               // weight scales of the segment
-    float acc[kUnitRows * kAccLd];     // one sum per (row, token)
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    float act_s[2][kChunkGroups];        // activation scales [tok][group]
+    float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
+    float res[2][kUnitRows * kAccLd];    // one sum per (row, token)
+    ChunkDesc chunk[2];
+    SegMeta seg[2];
+    uint64_t full[kStages], empty[kStages];
+    uint64_t prep_full[2], act_empty[2], res_full[2], res_empty[2];
     int abort_flag;
-    int last_flag;
-    int n_comb;
-    int comb_tok[kMaxTok];
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemTail);
@@ -116,31 +143,6 @@ __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U
     return L;
 }
 
-struct ExpertRef {
-    int expert, p0, ntok, slot;
-    bool shared_static, valid;
-};
-
-__device__ __forceinline__ ExpertRef expert_ref(const StreamArgs& a, int src, int e_local) {
-    ExpertRef r;
-    if (src == kSrcShared) {
-        r.expert = a.shared_id;
-        r.p0 = a.shared_p0;
-        r.ntok = a.M;
-        r.slot = a.max_uniq - 1;
-        r.shared_static = true;
-    } else {
-        r.expert = __ldcg(a.uniq + e_local);
-        r.p0 = __ldcg(a.offs + e_local);
-        r.ntok = __ldcg(a.offs + e_local + 1) - r.p0;
-        r.slot = e_local;
-        r.shared_static = false;
-    }
-    r.valid = r.expert >= 0 && r.expert < a.n_experts && r.p0 >= 0 && r.ntok >= 1 && r.ntok <= kMaxTok &&
-              r.p0 + r.ntok <= a.max_pairs;
-    return r;
-}
-
 __device__ __forceinline__ const uint8_t* tile_ptr(const Operand& op, int e, int nb, int kb) {
     return op.w + ((static_cast<size_t>(e) * op.NB + nb) * op.KB + kb) * kTile;
 }
@@ -163,91 +165,89 @@ __device__ __forceinline__ bool wait_flag(const int* flag, int want, int* status
     }
 }
 
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, SmemTail& sm, int* status) {
+    if (mbar_wait_bounded(bar, parity, &sm.abort_flag)) return true;
+    record_error(status, MOEQ_ERR_TIMEOUT);
+    sm.abort_flag = 1;
+    return false;
+}
+
 // ------------------------------------------------------------------ producer
 __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint8_t* stages, int epoch) {
     const uint64_t pol = l2_evict_first_policy();
     long long issued = 0;
     int U = 0;
     bool have_plan = !a.fused_route;
-    for (int li = 0; li < a.n_lists; ++li) {
+    for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
         if (list_needs_plan(a, li)) {
             if (!have_plan) {
                 wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
                 have_plan = true;
             }
             U = __ldcg(a.n_uniq);
-            if (U < 0 || U > a.max_uniq) U = 0;  // reported by the consumers
+            if (U < 0 || U > a.max_uniq) U = 0;  // reported by the helper
         }
         const ListInfo L = list_info(a, li, U);
         const Operand& op = a.op[L.kind];
+        const int upe = L.RB * L.KU;
         int cur = -1, expert = 0;
-        for (long long u = L.lo; u < L.hi; ++u) {
-            const int e_local = static_cast<int>(u / (static_cast<long long>(L.RB) * L.KU));
-            const int rem = static_cast<int>(u % (static_cast<long long>(L.RB) * L.KU));
-            const int rb = rem / L.KU, ku = rem % L.KU;
+        for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi); ++u) {
+            const int e_local = u / upe;
+            const int rem = u - e_local * upe;
+            const int rb = rem / L.KU, ku = rem - rb * L.KU;
             if (e_local != cur) {
                 cur = e_local;
                 expert = L.src == kSrcShared ? a.shared_id : __ldcg(a.uniq + e_local);
                 if (expert < 0 || expert >= a.n_experts) expert = 0;
             }
             const int s = static_cast<int>(issued % kStages);
-            if (issued >= kStages) {
-                if (!mbar_wait_bounded(&sm.empty[s], static_cast<uint32_t>((issued / kStages - 1) & 1),
-                                       &sm.abort_flag)) {
-                    record_error(a.status, MOEQ_ERR_TIMEOUT);
-                    sm.abort_flag = 1;
-                }
-            }
-            if (sm.abort_flag) goto drain;
-            {
-                uint8_t* dst = stages + static_cast<size_t>(s) * kStageBytes;
-                if (L.kind == kKindGU) {
-                    mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
-                    bulk_load(dst, tile_ptr(op, expert, rb, ku), kTile, &sm.full[s], pol);
-                    bulk_load(dst + kTile, tile_ptr(op, expert, L.RB + rb, ku), kTile, &sm.full[s], pol);
-                } else {
-                    const int nt = min(2, op.KB - 2 * ku);
-                    mbar_arrive_expect_tx(&sm.full[s], nt * kTile);
-                    bulk_load(dst, tile_ptr(op, expert, rb, 2 * ku), nt * kTile, &sm.full[s], pol);
-                }
+            if (issued >= kStages)
+                mbar_wait_or_abort(&sm.empty[s], static_cast<uint32_t>((issued / kStages - 1) & 1), sm, a.status);
+            if (sm.abort_flag) break;
+            uint8_t* dst = stages + static_cast<size_t>(s) * kStageBytes;
+            if (L.kind == kKindGU) {
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                bulk_load(dst, tile_ptr(op, expert, rb, ku), kTile, &sm.full[s], pol);
+                bulk_load(dst + kTile, tile_ptr(op, expert, L.RB + rb, ku), kTile, &sm.full[s], pol);
+            } else {
+                const int nt = min(2, op.KB - 2 * ku);
+                mbar_arrive_expect_tx(&sm.full[s], nt * kTile);
+                bulk_load(dst, tile_ptr(op, expert, rb, 2 * ku), nt * kTile, &sm.full[s], pol);
             }
             ++issued;
         }
     }
-    return;
-drain:
-    // Let the copies already issued land before the CTA may exit (bounded).
-    for (long long j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
-        const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(&sm.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1)) &&
-               global_timer_ns() - t0 < 100ull * 1000ull * 1000ull) {
+    if (sm.abort_flag) {
+        // Let the copies already issued land before the CTA may exit (bounded).
+        for (long long j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+            const unsigned long long t0 = global_timer_ns();
+            while (!mbar_try_wait(&sm.full[j % kStages], static_cast<uint32_t>((j / kStages) & 1)) &&
+                   global_timer_ns() - t0 < 100ull * 1000ull * 1000ull) {
+            }
         }
     }
 }
 
-// ------------------------------------------------------------------ consumers
-// Quantise activation groups [g0, g1) of the segment's tokens into shared
-// memory (decoded values and scales).  Loads are issued four items at a time.
-// Out of line: it runs once per chunk and its division sequences would
-// otherwise crowd the registers of the streaming loop.
+// ------------------------------------------------------------------ helper
+// Quantise activation groups [g0, g0+ng) of a segment's tokens into a slot
+// (decoded values and scales), one warp, eight items' loads in flight.
 template <bool kF32>
-__device__ __noinline__ void quantise(const StreamArgs& a, const Operand& op, SmemTail& sm, const ExpertRef& r,
-                                      int g0, int g1, bool dump, int cw, int lane) {
-    const int ng = g1 - g0;
-    const int items = r.ntok * ng;
-    for (int base = cw; base < items; base += 4 * kCW) {
-        float4 v[4];
-        int row[4];
+__device__ __noinline__ void helper_quantise(const StreamArgs& a, const Operand& op, float* act, float* act_s,
+                                             const SegMeta& m, int g0, int ng, bool dump, int lane) {
+    const int items = m.ntok * ng;
+    for (int base = 0; base < items; base += 8) {
+        float4 v[8];
+        int row[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int item = base + b * kCW;
-            row[b] = -1;
+        for (int b = 0; b < 8; ++b) {
+            const int item = base + b;
+            row[b] = 0;
             if (item < items) {
                 const int t = item / ng, gg = g0 + item % ng;
-                const int p = r.p0 + t;
+                const int p = m.p0 + t;
                 // gate_up reads token rows (the shared expert's pairs are tokens
                 // 0..M-1 before any plan exists); down reads pair rows.
-                int rr = op.a_row ? (r.shared_static ? t : __ldcg(op.a_row + p)) : p;
+                int rr = op.a_row ? (m.shared_static ? t : __ldcg(op.a_row + p)) : p;
                 if (rr < 0 || rr >= op.rows_a) {
                     if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
                     rr = 0;
@@ -257,15 +257,15 @@ __device__ __noinline__ void quantise(const StreamArgs& a, const Operand& op, Sm
             }
         }
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int item = base + b * kCW;
+        for (int b = 0; b < 8; ++b) {
+            const int item = base + b;
             if (item >= items) break;
             const int t = item / ng, gl = item % ng, gg = g0 + gl;
             float s;
             float4 dec;
             const uint32_t codes = quant_group_warp(v[b], &s, &dec);
-            *reinterpret_cast<float4*>(sm.act + (t * ng + gl) * kGroup + act_pos(lane * 4)) = dec;
-            if (lane == 0) sm.act_s[t * ng + gl] = s;
+            *reinterpret_cast<float4*>(act + (t * ng + gl) * kGroup + act_pos(lane * 4)) = dec;
+            if (lane == 0) act_s[t * ng + gl] = s;
             if (dump) {
                 *reinterpret_cast<uint32_t*>(op.qdump + static_cast<size_t>(row[b]) * op.K + gg * kGroup +
                                              lane * 4) = codes;
@@ -275,6 +275,255 @@ __device__ __noinline__ void quantise(const StreamArgs& a, const Operand& op, Sm
     }
 }
 
+// Finish one segment from its result slot: gate_up -> h = silu(gate) * up
+// and (layer) the readiness flag of (expert, row block); down -> y and
+// (layer) the combine of every token whose last expert this was.
+__device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta& m, const float* res, int lane,
+                                             int epoch) {
+    const Operand& op = a.op[m.kind];
+    if (m.valid) {
+        for (int idx = lane; idx < 128 * m.ntok; idx += 32) {
+            const int i = idx & 127, t = idx >> 7;
+            float* o = op.out + static_cast<size_t>(m.p0 + t) * op.out_ld + m.rb * 128 + i;
+            if (m.kind == kKindGU) {
+                const float g = res[i * kAccLd + t];
+                const float u = res[(128 + i) * kAccLd + t];
+                *o = __fdiv_rn(g, 1.0f + expf(-g)) * u;
+            } else {
+                *o = res[i * kAccLd + t];
+            }
+        }
+    }
+    if (m.kind == kKindGU && a.fused_route) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release(a.h_ready + static_cast<size_t>(m.slot) * op.RB + m.rb, epoch);
+    }
+    if (m.kind == kKindDN && a.fused_combine) {
+        __threadfence();
+        __syncwarp();
+        int tok = -1, last = 0;
+        if (lane < m.ntok && m.valid) {
+            tok = m.shared_static ? lane : __ldcg(a.pair_tok + m.p0 + lane);
+            if (tok >= 0 && tok < a.M) last = atomicAdd(a.comb + tok * op.RB + m.rb, 1) == a.top_k;
+        }
+        uint32_t todo = __ballot_sync(0xffffffffu, last);
+        if (todo) __threadfence();
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int tk = __shfl_sync(0xffffffffu, tok, src);
+            const int* po = a.pair_of + tk * (a.top_k + 1);
+            for (int i = lane; i < 128; i += 32) {
+                const int n = m.rb * 128 + i;
+                float accv = __ldcg(op.out + static_cast<size_t>(__ldcg(po + a.top_k)) * op.out_ld + n);
+                for (int j = 0; j < a.top_k; ++j)
+                    accv = fmaf(__ldcg(a.topk_w + tk * a.top_k + j),
+                                __ldcg(op.out + static_cast<size_t>(__ldcg(po + j)) * op.out_ld + n), accv);
+                a.out_bf16[static_cast<size_t>(tk) * op.out_ld + n] = __float2bfloat16_rn(accv);
+            }
+            if (lane == 0) a.comb[tk * op.RB + m.rb] = 0;
+        }
+    }
+}
+
+// Finish segment number `sidx` (its result slot is sidx & 1).
+__device__ __noinline__ void helper_finish(const StreamArgs& a, SmemTail& sm, long long sidx, int lane, int epoch) {
+    const int rs = static_cast<int>(sidx & 1);
+    mbar_wait_or_abort(&sm.res_full[rs], static_cast<uint32_t>((sidx >> 1) & 1), sm, a.status);
+    const SegMeta m = sm.seg[rs];
+    float* res = sm.res[rs];
+    const int rows = m.kind == kKindGU ? 256 : 128;
+    if (!(m.ku0 == 0 && m.ku1 == m.KU)) {
+        // split K: publish this CTA's partial, take a ticket, and if this is
+        // the last contribution sum all of them in CTA order.
+        const long long rblk = static_cast<long long>(m.e_local) * m.RB + m.rb;
+        const long long c_lo = cta_of_unit(rblk * m.KU, m.T, m.G);
+        const long long c_hi = cta_of_unit(rblk * m.KU + m.KU - 1, m.T, m.G);
+        float* part_base = a.partials + static_cast<size_t>(m.li) * a.partial_list_floats;
+        const int my_slot = static_cast<int>(2 * m.c + ((m.lo / m.KU) == rblk ? 0 : 1));
+        float* mine = part_base + static_cast<size_t>(my_slot) * kMaxTok * rows;
+        for (int idx = lane; idx < rows * m.ntok; idx += 32) {
+            const int row = idx % rows, t = idx / rows;
+            mine[t * rows + row] = res[row * kAccLd + t];
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            int n = 0;
+            for (long long cc = c_lo; cc <= c_hi; ++cc) n += unit_lo(cc, m.T, m.G) < unit_lo(cc + 1, m.T, m.G);
+            last = atomicAdd(a.tickets[m.li] + rblk, 1) == n - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence();
+            for (int idx = lane; idx < rows * m.ntok; idx += 32) {
+                const int row = idx % rows, t = idx / rows;
+                float v = 0.0f;
+                for (long long cc = c_lo; cc <= c_hi; ++cc) {
+                    const long long lo = unit_lo(cc, m.T, m.G);
+                    if (lo >= unit_lo(cc + 1, m.T, m.G)) continue;
+                    const int slot = static_cast<int>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1));
+                    v += __ldcg(part_base + (static_cast<size_t>(slot) * kMaxTok + t) * rows + row);
+                }
+                res[row * kAccLd + t] = v;
+            }
+            __syncwarp();
+            if (lane == 0) a.tickets[m.li][rblk] = 0;
+            helper_epilogue(a, m, res, lane, epoch);
+        }
+    } else {
+        helper_epilogue(a, m, res, lane, epoch);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.res_empty[rs]);
+}
+
+// The helper walks the same lists / segments as the producer, cut into
+// chunks: prepare chunk c (scales, quantised activations, descriptor), then
+// finish the segment whose last chunk is c-1.
+template <bool kGuF32, bool kDnF32>
+__device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
+    long long c = 0;         // chunks prepared
+    long long sidx = 0;      // segments started
+    long long owed = -1;     // a fully prepared segment not yet finished
+    int U = 0;
+    bool have_plan = !a.fused_route;
+    for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
+        if (list_needs_plan(a, li)) {
+            if (!have_plan) {
+                if (owed >= 0) {  // never wait on another CTA while owing a finish
+                    helper_finish(a, sm, owed, lane, epoch);
+                    owed = -1;
+                }
+                if (lane == 0) wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
+                __syncwarp();
+                have_plan = true;
+            }
+            U = __ldcg(a.n_uniq);
+            if (U < 0 || U > a.max_uniq) {
+                if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
+                U = 0;
+            }
+        }
+        const ListInfo L = list_info(a, li, U);
+        const Operand& op = a.op[L.kind];
+        const int GPU = L.kind == kKindGU ? 1 : 2;
+        const int upe = L.RB * L.KU;
+        for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi) && !sm.abort_flag;) {
+            SegMeta m;
+            m.kind = L.kind;
+            m.li = li;
+            m.e_local = u / upe;
+            const int rem = u - m.e_local * upe;
+            m.rb = rem / L.KU;
+            m.ku0 = rem - m.rb * L.KU;
+            const int seg_end_u = min(static_cast<int>(L.hi), u - m.ku0 + L.KU);
+            m.ku1 = m.ku0 + (seg_end_u - u);
+            if (L.src == kSrcShared) {
+                m.expert = a.shared_id;
+                m.p0 = a.shared_p0;
+                m.ntok = a.M;
+                m.slot = a.max_uniq - 1;
+                m.shared_static = 1;
+            } else {
+                m.expert = __ldcg(a.uniq + m.e_local);
+                m.p0 = __ldcg(a.offs + m.e_local);
+                m.ntok = __ldcg(a.offs + m.e_local + 1) - m.p0;
+                m.slot = m.e_local;
+                m.shared_static = 0;
+            }
+            m.valid = m.expert >= 0 && m.expert < a.n_experts && m.p0 >= 0 && m.ntok >= 1 && m.ntok <= kMaxTok &&
+                      m.p0 + m.ntok <= a.max_pairs;
+            if (!m.valid) {
+                if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
+                m.expert = 0;
+                m.p0 = 0;
+                m.ntok = 1;
+            }
+            m.T = L.T;
+            m.G = L.G;
+            m.c = L.c;
+            m.lo = L.lo;
+            m.KU = L.KU;
+            m.RB = L.RB;
+            // down in the layer needs this expert's complete h: finish what is
+            // owed, then wait (lanes check the row-block flags in parallel)
+            if (m.kind == kKindDN && a.fused_route) {
+                if (owed >= 0) {
+                    helper_finish(a, sm, owed, lane, epoch);
+                    owed = -1;
+                }
+                const int nrb = a.op[kKindGU].RB;
+                for (int j = lane; j < nrb; j += 32)
+                    wait_flag(a.h_ready + static_cast<size_t>(m.slot) * nrb + j, epoch, a.status, &sm.abort_flag);
+                __syncwarp();
+            }
+            const bool dump = m.valid && op.qdump != nullptr && m.rb == 0 &&
+                              (m.kind == kKindDN || m.shared_static || m.e_local == L.n_exp - 1);
+            const int cu = max(1, (kActSlot / (kGroup * m.ntok)) / GPU);  // units per chunk
+            for (int ua = m.ku0; ua < m.ku1; ua += cu) {
+                const int ub = min(m.ku1, ua + cu);
+                const int cs = static_cast<int>(c & 1);
+                if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
+                if (ua == m.ku0) {
+                    // a new segment: its result slot must have been finished
+                    if (owed >= 0 && owed == sidx - 2) {
+                        helper_finish(a, sm, owed, lane, epoch);
+                        owed = -1;
+                    }
+                    if (lane == 0) sm.seg[sidx & 1] = m;
+                }
+                const int g0 = ua * GPU, g1 = min(op.KB, ub * GPU), ng = g1 - g0;
+                for (int i = lane; i < ng * 2; i += 32) {
+                    const int b = i / ng, gl = i % ng;
+                    if (b == 1 && m.kind != kKindGU) continue;
+                    const int nb = m.rb + (b ? L.RB : 0);
+                    sm.sw[cs][b][gl] = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
+                }
+                if (m.kind == kKindGU)
+                    helper_quantise<kGuF32>(a, op, sm.act[cs], sm.act_s[cs], m, g0, ng, dump, lane);
+                else
+                    helper_quantise<kDnF32>(a, op, sm.act[cs], sm.act_s[cs], m, g0, ng, dump, lane);
+                if (lane == 0) {
+                    ChunkDesc d;
+                    d.kind = m.kind;
+                    d.ku0 = ua;
+                    d.ku1 = ub;
+                    d.g0 = g0;
+                    d.ng = ng;
+                    d.ntok = m.ntok;
+                    d.seg_end = ub == m.ku1;
+                    sm.chunk[cs] = d;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+                ++c;
+                // the previous segment is fully prepared and the consumers
+                // have its successor's first chunk: finish it now
+                if (owed >= 0 && ua == m.ku0) {
+                    helper_finish(a, sm, owed, lane, epoch);
+                    owed = -1;
+                }
+            }
+            owed = sidx;
+            ++sidx;
+            u = seg_end_u;
+        }
+    }
+    // end marker, then the last finish
+    {
+        const int cs = static_cast<int>(c & 1);
+        if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
+        if (lane == 0) sm.chunk[cs].kind = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+    }
+    if (owed >= 0 && !sm.abort_flag) helper_finish(a, sm, owed, lane, epoch);
+}
+
+// ------------------------------------------------------------------ consumers
 // Per lane and pass: dot product of its 16 weight bytes (row `rows_base +
 // 4p + lane/8`, logical chunk lane%8) with the matching decoded activations
 // of tokens t0 .. t0+MT-1 (loads clamped to the last token).
@@ -312,7 +561,7 @@ __device__ __forceinline__ void tile_dot(const uint8_t* tile, int rows_base, con
     }
 }
 
-// As tile_dot for tokens T0 .. T0+MT-1, but folds each pass straight into
+// As tile_dot for tokens T0 .. T0+MT-1, folding each pass straight into
 // running sums: acc[p][T0 + t] += dot * scl[T0 + t].
 template <int MT, int PASSES, int T0, int MTOT>
 __device__ __forceinline__ void tile_dot_acc(const uint8_t* tile, int rows_base, const float* act_g, int tok_ld,
@@ -356,76 +605,68 @@ __device__ __forceinline__ float reduce8(float v) {
     return v;
 }
 
-// One segment: units [ku0, ku1) of row block rb of expert r.  Leaves one sum
-// per (unit row, token) in sm.acc.  MODE 1/2/4: up to that many tokens with
-// running sums in registers; MODE 0: any count, two tokens at a time, each
-// K group reduced across lanes into sm.acc.
-template <int KIND, bool kF32, int MODE>
-__device__ __forceinline__ void run_segment(const StreamArgs& a, SmemTail& sm, const uint8_t* stages,
-                                            const ExpertRef& r, int rb, int ku0, int ku1, bool dump, int cw,
-                                            int lane, int ctid, long long& it) {
-    const Operand& op = a.op[KIND];
+// One segment, chunk after chunk, for one consumer warp.  Leaves one sum per
+// (row of this warp, token) in result slot rs.  MODE 1/2/4: up to that many
+// tokens with running sums in registers; MODE 0: any count, two tokens at a
+// time, each K group reduced across lanes into the result slot.
+template <int KIND, int MODE>
+__device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
+                                                int cw, int lane, long long& c, long long& it) {
     constexpr int MT = MODE == 0 ? 2 : MODE;
     constexpr int PASSES = KIND == kKindGU ? 4 : 2;   // 4-row passes per warp and tile
-    constexpr int GPU = KIND == kKindGU ? 1 : 2;      // K groups per unit
     // gate_up: warp w covers rows (w%8)*16.. of tile w/8; down: rows w*8.. of both tiles
     const int tile_w = KIND == kKindGU ? (cw >> 3) : 0;
     const int rows_base = KIND == kKindGU ? (cw & 7) * 16 : cw * 8;
     const int acc_row0 = KIND == kKindGU ? tile_w * 128 + rows_base : rows_base;
+    float* res = sm.res[rs];
+    const int ntok = sm.chunk[c & 1].ntok;
     if (MODE == 0)
-        for (int i = ctid; i < kUnitRows * kMaxTok; i += kConsumers) sm.acc[(i / kMaxTok) * kAccLd + i % kMaxTok] = 0.f;
+        for (int i = lane; i < PASSES * 4 * ntok; i += 32) res[(acc_row0 + i / ntok) * kAccLd + i % ntok] = 0.f;
     float acc[PASSES][MT];
 #pragma unroll
     for (int p = 0; p < PASSES; ++p)
 #pragma unroll
         for (int t = 0; t < MT; ++t) acc[p][t] = 0.0f;
 
-    const int upc = max(1, (kActCap / (kGroup * r.ntok)) / GPU);  // units per activation chunk
-    for (int ua = ku0; ua < ku1; ua += upc) {
-        const int ub = min(ku1, ua + upc);
-        const int g0 = ua * GPU, g1 = min(op.KB, ub * GPU);
-        consumer_sync();   // activation buffer free
-        quantise<kF32>(a, op, sm, r, g0, g1, dump, cw, lane);
-        consumer_sync();   // activation buffer full
-        const int ng = g1 - g0;
-        const int tok_ld = ng * kGroup;
-        for (int ku = ua; ku < ub; ++ku, ++it) {
+    for (bool first = true;; first = false) {
+        const int cs = static_cast<int>(c & 1);
+        if (!first) mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
+        const ChunkDesc d = sm.chunk[cs];
+        const float* act = sm.act[cs];
+        const float* act_s = sm.act_s[cs];
+        const int tok_ld = d.ng * kGroup;
+        for (int ku = d.ku0; ku < d.ku1; ++ku, ++it) {
             const int s = static_cast<int>(it % kStages);
-            if (!mbar_wait_bounded(&sm.full[s], static_cast<uint32_t>((it / kStages) & 1), &sm.abort_flag)) {
-                // Keep the control flow (and so every named barrier) identical
-                // across the consumer warps; the results are void.
-                record_error(a.status, MOEQ_ERR_TIMEOUT);
-                sm.abort_flag = 1;
-            }
+            mbar_wait_or_abort(&sm.full[s], static_cast<uint32_t>((it / kStages) & 1), sm, a.status);
             const uint8_t* st = stages + static_cast<size_t>(s) * kStageBytes;
-            const int ntile = KIND == kKindGU ? 1 : min(2, op.KB - 2 * ku);
+            const int ntile = KIND == kKindGU ? 1 : min(2, a.op[KIND].KB - 2 * ku);
             for (int tt = 0; tt < ntile; ++tt) {
-                const int g = KIND == kKindGU ? ku : 2 * ku + tt;
+                const int gl = (KIND == kKindGU ? ku : 2 * ku + tt) - d.g0;
                 const uint8_t* tile = st + (KIND == kKindGU ? tile_w : tt) * kTile;
-                const float* act_g = sm.act + (g - g0) * kGroup;
-                const float swg = sm.sw[tile_w][g - ku0 * GPU];
+                const float* act_g = act + gl * kGroup;
+                const float swg = sm.sw[cs][tile_w][gl];
                 if (MODE != 0) {
                     float scl[MT];
 #pragma unroll
-                    for (int t = 0; t < MT; ++t) scl[t] = sm.act_s[min(t, r.ntok - 1) * ng + (g - g0)] * swg;
+                    for (int t = 0; t < MT; ++t) scl[t] = act_s[min(t, ntok - 1) * d.ng + gl] * swg;
                     if (MT <= 2) {
-                        tile_dot_acc<MT, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, r.ntok, lane, scl, acc);
+                        tile_dot_acc<MT, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
                     } else {  // four tokens as two pairs: fewer live registers
-                        tile_dot_acc<2, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, r.ntok, lane, scl, acc);
-                        tile_dot_acc<2, PASSES, 2, MT>(tile, rows_base, act_g, tok_ld, r.ntok, lane, scl, acc);
+                        tile_dot_acc<2, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
+                        tile_dot_acc<2, PASSES, 2, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
                     }
                 } else {
-                    for (int t0 = 0; t0 < r.ntok; t0 += 2) {
+                    for (int t0 = 0; t0 < ntok; t0 += 2) {
                         float part[PASSES][2];
-                        tile_dot<2, PASSES>(tile, rows_base, act_g, tok_ld, t0, r.ntok, lane, part);
+                        tile_dot<2, PASSES>(tile, rows_base, act_g, tok_ld, t0, ntok, lane, part);
 #pragma unroll
                         for (int p = 0; p < PASSES; ++p) {
                             const int row = acc_row0 + p * 4 + (lane >> 3);
 #pragma unroll
                             for (int t = 0; t < 2; ++t) {
                                 const float v = reduce8(part[p][t]);
-                                if ((lane & 7) == 0 && t0 + t < r.ntok)
-                                    sm.acc[row * kAccLd + t0 + t] += v * (sm.act_s[(t0 + t) * ng + (g - g0)] * swg);
+                                if ((lane & 7) == 0 && t0 + t < ntok)
+                                    res[row * kAccLd + t0 + t] += v * (act_s[(t0 + t) * d.ng + gl] * swg);
                             }
                         }
                     }
@@ -434,6 +675,10 @@ __device__ __forceinline__ void run_segment(const StreamArgs& a, SmemTail& sm, c
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.act_empty[cs]);
+        ++c;
+        if (d.seg_end || sm.abort_flag) break;
     }
     if (MODE != 0) {
 #pragma unroll
@@ -442,166 +687,29 @@ __device__ __forceinline__ void run_segment(const StreamArgs& a, SmemTail& sm, c
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const float v = reduce8(acc[p][t]);
-                if ((lane & 7) == 0 && t < r.ntok) sm.acc[row * kAccLd + t] = v;
+                if ((lane & 7) == 0 && t < ntok) res[row * kAccLd + t] = v;
             }
         }
     }
 }
 
-// The wide-token modes run out of line so that their register needs do not
-// constrain the one- and two-token loops (the common case at M <= 16).
-template <int KIND, bool kF32, int MODE>
-__device__ __noinline__ void run_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages,
-                                              const ExpertRef& r, int rb, int ku0, int ku1, bool dump, int cw,
-                                              int lane, int ctid, long long& it) {
-    run_segment<KIND, kF32, MODE>(a, sm, stages, r, rb, ku0, ku1, dump, cw, lane, ctid, it);
+template <int KIND, int MODE>
+__device__ __noinline__ void consume_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
+                                                  int cw, int lane, long long& c, long long& it) {
+    consume_segment<KIND, MODE>(a, sm, stages, rs, cw, lane, c, it);
 }
 
-// Epilogue of a finished row block: gate_up -> h = silu(gate) * up and, in
-// the layer, the readiness flag of (expert, row block); down -> y and, in the
-// layer, the combine of every token whose last expert this was.
 template <int KIND>
-__device__ __forceinline__ void epilogue(const StreamArgs& a, SmemTail& sm, const ExpertRef& r, int rb, int ctid,
-                                         int epoch) {
-    const Operand& op = a.op[KIND];
-    if (r.valid) {
-        for (int idx = ctid; idx < 128 * r.ntok; idx += kConsumers) {
-            const int i = idx & 127, t = idx >> 7;
-            float* o = op.out + static_cast<size_t>(r.p0 + t) * op.out_ld + rb * 128 + i;
-            if (KIND == kKindGU) {
-                const float g = sm.acc[i * kAccLd + t];
-                const float u = sm.acc[(128 + i) * kAccLd + t];
-                *o = __fdiv_rn(g, 1.0f + expf(-g)) * u;
-            } else {
-                *o = sm.acc[i * kAccLd + t];
-            }
-        }
-    }
-    if (KIND == kKindGU && a.fused_route) {
-        __threadfence();
-        consumer_sync();
-        if (ctid == 0) st_release(a.h_ready + static_cast<size_t>(r.slot) * op.RB + rb, epoch);
-    }
-    if (KIND == kKindDN && a.fused_combine) {
-        __threadfence();
-        if (ctid == 0) sm.n_comb = 0;
-        consumer_sync();
-        if (ctid < r.ntok && r.valid) {
-            const int tok = r.shared_static ? ctid : __ldcg(a.pair_tok + r.p0 + ctid);
-            if (tok >= 0 && tok < a.M) {
-                const int old = atomicAdd(a.comb + tok * op.RB + rb, 1);
-                if (old == a.top_k) sm.comb_tok[atomicAdd(&sm.n_comb, 1)] = tok;
-            }
-        }
-        consumer_sync();
-        const int nc = sm.n_comb;
-        if (nc) __threadfence();
-        for (int j = 0; j < nc; ++j) {
-            const int tok = sm.comb_tok[j];
-            if (ctid < 128) {
-                const int n = rb * 128 + ctid;
-                const int* po = a.pair_of + tok * (a.top_k + 1);
-                float accv = __ldcg(op.out + static_cast<size_t>(__ldcg(po + a.top_k)) * op.out_ld + n);
-                for (int jj = 0; jj < a.top_k; ++jj)
-                    accv = fmaf(__ldcg(a.topk_w + tok * a.top_k + jj),
-                                __ldcg(op.out + static_cast<size_t>(__ldcg(po + jj)) * op.out_ld + n), accv);
-                a.out_bf16[static_cast<size_t>(tok) * op.out_ld + n] = __float2bfloat16_rn(accv);
-            }
-            if (ctid == 0) a.comb[tok * op.RB + rb] = 0;
-        }
-    }
-}
-
-template <int KIND, bool kF32>
-__device__ __forceinline__ void run_list(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int li, int U, int cw, int lane,
-                         int ctid, long long& it, int epoch) {
-    const ListInfo L = list_info(a, li, U);
-    const Operand& op = a.op[KIND];
-    constexpr int kRows = KIND == kKindGU ? 256 : 128;
-    const long long upe = static_cast<long long>(L.RB) * L.KU;
-    long long u = L.lo;
-    while (u < L.hi) {
-        const int e_local = static_cast<int>(u / upe);
-        const int rem = static_cast<int>(u % upe);
-        const int rb = rem / L.KU, ku0 = rem % L.KU;
-        const long long seg_end = min(L.hi, u - ku0 + L.KU);
-        const int ku1 = ku0 + static_cast<int>(seg_end - u);
-        ExpertRef r = expert_ref(a, L.src, e_local);
-        if (!r.valid) {
-            if (ctid == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
-            r.expert = 0;
-            r.p0 = 0;
-            r.ntok = 1;
-        }
-        // down in the layer: this expert's h must be complete (bounded wait)
-        if (KIND == kKindDN && a.fused_route && ctid == 0) {
-            const int nrb = a.op[kKindGU].RB;
-            for (int j = 0; j < nrb; ++j)
-                if (!wait_flag(a.h_ready + static_cast<size_t>(r.slot) * nrb + j, epoch, a.status, &sm.abort_flag))
-                    break;
-        }
-        consumer_sync();   // previous segment's readers of sw / acc are done; h is ready
-        const int nsw = KIND == kKindGU ? (ku1 - ku0) : (min(op.KB, 2 * ku1) - 2 * ku0);
-        for (int i = ctid; i < nsw * (KIND == kKindGU ? 2 : 1); i += kConsumers) {
-            const int b = i / nsw, gl = i % nsw;
-            const int g = (KIND == kKindGU ? ku0 : 2 * ku0) + gl;
-            const int nb = rb + (b ? L.RB : 0);
-            sm.sw[b][gl] = __ldg(op.sw + (static_cast<size_t>(r.expert) * op.NB + nb) * op.KB + g);
-        }
-        const bool dump = r.valid && op.qdump != nullptr && rb == 0 &&
-                          (KIND == kKindDN || r.shared_static || e_local == L.n_exp - 1);
-        if (r.ntok <= 1)
-            run_segment<KIND, kF32, 1>(a, sm, stages, r, rb, ku0, ku1, dump, cw, lane, ctid, it);
-        else if (r.ntok <= 2)
-            run_segment<KIND, kF32, 2>(a, sm, stages, r, rb, ku0, ku1, dump, cw, lane, ctid, it);
-        else if (r.ntok <= 4)
-            run_segment_cold<KIND, kF32, 4>(a, sm, stages, r, rb, ku0, ku1, dump, cw, lane, ctid, it);
-        else
-            run_segment_cold<KIND, kF32, 0>(a, sm, stages, r, rb, ku0, ku1, dump, cw, lane, ctid, it);
-        consumer_sync();
-
-        if (ku0 == 0 && ku1 == L.KU) {
-            epilogue<KIND>(a, sm, r, rb, ctid, epoch);
-        } else {
-            const long long rblk = static_cast<long long>(e_local) * L.RB + rb;
-            const long long c_lo = cta_of_unit(rblk * L.KU, L.T, L.G);
-            const long long c_hi = cta_of_unit(rblk * L.KU + L.KU - 1, L.T, L.G);
-            float* part_base = a.partials + static_cast<size_t>(li) * a.partial_list_floats;
-            const int my_slot = static_cast<int>(2 * L.c + ((L.lo / L.KU) == rblk ? 0 : 1));
-            float* mine = part_base + static_cast<size_t>(my_slot) * kMaxTok * kRows;
-            for (int idx = ctid; idx < kRows * r.ntok; idx += kConsumers) {
-                const int row = idx % kRows, t = idx / kRows;
-                mine[t * kRows + row] = sm.acc[row * kAccLd + t];
-            }
-            __threadfence();
-            consumer_sync();
-            if (ctid == 0) {
-                int n = 0;
-                for (long long cc = c_lo; cc <= c_hi; ++cc) n += unit_lo(cc, L.T, L.G) < unit_lo(cc + 1, L.T, L.G);
-                const int old = atomicAdd(a.tickets[li] + rblk, 1);
-                sm.last_flag = (old == n - 1);
-            }
-            consumer_sync();
-            if (sm.last_flag) {
-                __threadfence();
-                for (int idx = ctid; idx < kRows * r.ntok; idx += kConsumers) {
-                    const int row = idx % kRows, t = idx / kRows;
-                    float v = 0.0f;
-                    for (long long cc = c_lo; cc <= c_hi; ++cc) {
-                        const long long lo = unit_lo(cc, L.T, L.G);
-                        if (lo >= unit_lo(cc + 1, L.T, L.G)) continue;
-                        const int slot = static_cast<int>(2 * cc + ((lo / L.KU) == rblk ? 0 : 1));
-                        v += __ldcg(part_base + (static_cast<size_t>(slot) * kMaxTok + t) * kRows + row);
-                    }
-                    sm.acc[row * kAccLd + t] = v;
-                }
-                consumer_sync();
-                if (ctid == 0) a.tickets[li][rblk] = 0;
-                epilogue<KIND>(a, sm, r, rb, ctid, epoch);
-            }
-        }
-        u = seg_end;
-    }
+__device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
+                                                 int ntok, int cw, int lane, long long& c, long long& it) {
+    if (ntok <= 1)
+        consume_segment<KIND, 1>(a, sm, stages, rs, cw, lane, c, it);
+    else if (ntok <= 2)
+        consume_segment<KIND, 2>(a, sm, stages, rs, cw, lane, c, it);
+    else if (ntok <= 4)
+        consume_segment_cold<KIND, 4>(a, sm, stages, rs, cw, lane, c, it);
+    else
+        consume_segment_cold<KIND, 0>(a, sm, stages, rs, cw, lane, c, it);
 }
 
 struct ConsumerSync {
@@ -620,58 +728,62 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kCW);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.prep_full[s], 1);
+            mbar_init(&sm.act_empty[s], kCW);
+            mbar_init(&sm.res_full[s], kCW);
+            mbar_init(&sm.res_empty[s], 1);
+        }
         sm.abort_flag = 0;
         fence_mbar_init();
     }
     const int epoch = a.fused_route ? ld_relaxed(a.epoch) + 1 : 0;
     __syncthreads();
 
-    if (warp == kCW) {
+    if (warp == kProducerWarp) {
         if (lane == 0) producer(a, sm, stages, epoch);
         return;
     }
-
-    const int cw = warp, ctid = tid;
-    if (a.fused_route && blockIdx.x == 0) {
-        route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, a.plan, sm.route, ctid, ConsumerSync{});
-        __threadfence();
-        consumer_sync();
-        if (ctid == 0) st_release(a.route_flag, epoch);
-    }
-    long long it = 0;
-    int U = 0;
-    bool have_plan = !a.fused_route;
-    for (int li = 0; li < a.n_lists; ++li) {
-        if (list_needs_plan(a, li)) {
-            if (!have_plan) {
-                if (ctid == 0) wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
-                consumer_sync();
-                have_plan = true;
-            }
-            U = __ldcg(a.n_uniq);
-            if (U < 0 || U > a.max_uniq) {
-                if (ctid == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
-                U = 0;
-            }
-        }
-        if (a.list_kind[li] == kKindGU)
-            run_list<kKindGU, kGuF32>(a, sm, stages, li, U, cw, lane, ctid, it, epoch);
-        else
-            run_list<kKindDN, kDnF32>(a, sm, stages, li, U, cw, lane, ctid, it, epoch);
-    }
-
-    if (a.fused_route) {
-        // The last CTA to finish publishes the epoch for the next launch.
-        consumer_sync();
-        if (ctid == 0) {
+    if (warp == kHelperWarp) {
+        // CTA 0's consumers write the routing plan into the activation slots'
+        // memory first; the helper waits for the plan before touching them.
+        helper<kGuF32, kDnF32>(a, sm, lane, epoch);
+        if (a.fused_route && lane == 0) {
+            // The last CTA to finish publishes the epoch for the next launch.
             __threadfence();
-            const int old = atomicAdd(a.done, 1);
-            if (old == static_cast<int>(gridDim.x) - 1) {
+            if (atomicAdd(a.done, 1) == static_cast<int>(gridDim.x) - 1) {
                 *a.done = 0;
                 __threadfence();
                 st_release(a.epoch, epoch);
             }
         }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp;
+    if (a.fused_route && blockIdx.x == 0) {
+        route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, a.plan, sm.route, tid, ConsumerSync{});
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) st_release(a.route_flag, epoch);
+    }
+    long long c = 0, it = 0, sidx = 0;
+    for (;;) {
+        const int cs = static_cast<int>(c & 1);
+        mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
+        const int kind = sm.chunk[cs].kind;
+        if (kind < 0 || sm.abort_flag) break;
+        const int rs = static_cast<int>(sidx & 1);
+        if (sidx >= 2) mbar_wait_or_abort(&sm.res_empty[rs], static_cast<uint32_t>(((sidx >> 1) - 1) & 1), sm, a.status);
+        const int ntok = sm.chunk[cs].ntok;
+        if (kind == kKindGU)
+            consume_dispatch<kKindGU>(a, sm, stages, rs, ntok, cw, lane, c, it);
+        else
+            consume_dispatch<kKindDN>(a, sm, stages, rs, ntok, cw, lane, c, it);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+        ++sidx;
     }
 }
 
