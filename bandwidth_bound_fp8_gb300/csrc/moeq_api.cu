@@ -51,19 +51,27 @@ moeq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOE
 
 // ------------------------------------------------------------------ workspace
 // Header (256 B): status word, epoch, done ticket, route flag.
-constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffRouteFlag = 12, kHeader = 256;
+constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffRouteFlag = 12, kOffACnt = 16, kHeader = 256;
 
 struct StreamWs {
+    size_t aq[2], as[2];
     size_t tickets[kMaxLists];
     size_t partials;
     size_t h_ready, comb, end;
 };
 
-// Ticket and partial areas for the given lists, starting at `base`.
-StreamWs stream_ws_layout(size_t base, int n_lists, const int* tickets_per_list, int grid, int h_ready_n,
-                          int comb_n) {
+// Quantised-activation buffers (rows x K floats + rows x K/128 scales per
+// operand), ticket and partial areas for the given lists, from `base`.
+StreamWs stream_ws_layout(size_t base, const int* aq_rows, const int* aq_k, int n_lists, const int* tickets_per_list,
+                          int grid, int h_ready_n, int comb_n) {
     StreamWs l;
     size_t off = align_up(base, 256);
+    for (int k = 0; k < 2; ++k) {
+        l.aq[k] = off;
+        off = align_up(off + sizeof(float) * static_cast<size_t>(aq_rows[k]) * aq_k[k], 256);
+        l.as[k] = off;
+        off = align_up(off + sizeof(float) * static_cast<size_t>(aq_rows[k]) * (aq_k[k] / 128), 256);
+    }
     for (int i = 0; i < kMaxLists; ++i) {
         l.tickets[i] = off;
         if (i < n_lists) off = align_up(off + sizeof(int) * static_cast<size_t>(tickets_per_list[i]), 256);
@@ -90,13 +98,18 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
     const size_t after = l.y + sizeof(float) * static_cast<size_t>(mp) * H;
     const int tk[4] = {I / 128, mu * (I / 128), H / 128, mu * (H / 128)};
-    l.s = stream_ws_layout(after, 4, tk, grid, mu * (I / 128), M * (H / 128));
+    const int rows[2] = {M, mp}, ks[2] = {H, I};
+    l.s = stream_ws_layout(after, rows, ks, 4, tk, grid, mu * (I / 128), M * (H / 128));
     return l;
 }
 
-StreamWs gemm_ws_layout(int RB, int max_uniq, int grid) {
+// kind 0: gate_up (input rows = tokens), kind 1: down (input rows = pairs)
+StreamWs gemm_ws_layout(int kind, int RB, int K, int rows_a, int max_uniq, int grid) {
     const int tk[1] = {RB * max_uniq};
-    return stream_ws_layout(kHeader, 1, tk, grid, 0, 0);
+    int rows[2] = {0, 0}, ks[2] = {128, 128};
+    rows[kind] = rows_a;
+    ks[kind] = K;
+    return stream_ws_layout(kHeader, rows, ks, 1, tk, grid, 0, 0);
 }
 
 struct PlanLayout {
@@ -133,6 +146,11 @@ void fill_ws(StreamArgs& a, void* ws, const StreamWs& l, int grid) {
     a.epoch = reinterpret_cast<int*>(base + kOffEpoch);
     a.done = reinterpret_cast<int*>(base + kOffDone);
     a.route_flag = reinterpret_cast<int*>(base + kOffRouteFlag);
+    a.a_cnt = reinterpret_cast<int*>(base + kOffACnt);
+    for (int k = 0; k < 2; ++k) {
+        a.op[k].aq = reinterpret_cast<float*>(base + l.aq[k]);
+        a.op[k].as = reinterpret_cast<float*>(base + l.as[k]);
+    }
     for (int i = 0; i < kMaxLists; ++i) a.tickets[i] = reinterpret_cast<int*>(base + l.tickets[i]);
     a.partials = reinterpret_cast<float*>(base + l.partials);
     a.h_ready = reinterpret_cast<int*>(base + l.h_ready);
@@ -199,12 +217,12 @@ size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int t
     return layer_ws_layout(M, H, I, E, top_k, dev.sms).s.end;
 }
 
-size_t moeq_gemm_workspace_size(int rows_out, int max_uniq, int is_gate_up) {
-    (void)is_gate_up;
-    if (rows_out <= 0 || rows_out % 128 || max_uniq < 1) return 0;
+size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up) {
+    if (rows_out <= 0 || rows_out % 128 || max_uniq < 1 || K <= 0 || K % 128 || K > MOEQ_MAX_K || rows_in < 1)
+        return 0;
     const DeviceInfo dev = current_device();
     if (!dev.sms) return 0;
-    return gemm_ws_layout(rows_out / 128, max_uniq, dev.sms).end;
+    return gemm_ws_layout(is_gate_up ? 0 : 1, rows_out / 128, K, rows_in, max_uniq, dev.sms).end;
 }
 
 moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -268,10 +286,11 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const StreamWs wl = gemm_ws_layout(I / 128, max_uniq, dev.sms);
+    const StreamWs wl = gemm_ws_layout(0, I / 128, H, M, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
     StreamArgs a = {};
     Operand& o = a.op[kKindGU];
+    o.quant_input = 1;
     o.w = w_gu;
     o.sw = s_gu;
     o.K = H;
@@ -298,7 +317,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.max_pairs = max_pairs;
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
-    return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
+    return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
 
 moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, int N, const uint8_t* w_d,
@@ -314,10 +333,11 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     if (K <= 0 || N <= 0 || K % 128 || N % 128 || K > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const StreamWs wl = gemm_ws_layout(N / 128, max_uniq, dev.sms);
+    const StreamWs wl = gemm_ws_layout(1, N / 128, K, max_pairs, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
     StreamArgs a = {};
     Operand& o = a.op[kKindDN];
+    o.quant_input = 1;
     o.w = w_d;
     o.sw = s_d;
     o.K = K;
@@ -342,7 +362,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     fill_ws(a, ws, wl, dev.sms);
-    return cuda_status(launch_stream(a, dev.sms, false, as_stream(stream)));
+    return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
 
 moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k, void* out_bf16,
@@ -394,6 +414,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     g.rows_a = M;
     g.out = h;
     g.out_ld = I;
+    g.quant_input = 1;
     Operand& d = a.op[kKindDN];
     d.w = w_d;
     d.sw = s_d;
@@ -433,6 +454,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.plan = plan;
     a.fused_combine = 1;
     a.out_bf16 = static_cast<__nv_bfloat16*>(out);
+    a.h_to_dn = 1;
     fill_ws(a, ws, l.s, dev.sms);
 
     cudaStream_t st = as_stream(stream);

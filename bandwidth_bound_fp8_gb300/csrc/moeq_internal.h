@@ -36,6 +36,9 @@ struct Operand {
     int out_ld;
     uint8_t* qdump;       // optional [rows_a, K]
     float* sdump;         // optional [rows_a, K/128]
+    float* aq;            // workspace: decoded activation codes [rows_a, K] in the consumer layout
+    float* as;            // workspace: activation scales [rows_a, K/128]
+    int quant_input;      // 1: the kernel's first phase quantises `a` into aq/as
 };
 
 struct StreamArgs {
@@ -65,6 +68,8 @@ struct StreamArgs {
     int* epoch;
     int* done;
     int* route_flag;
+    int* a_cnt;               // CTAs done with the input quantisation phase (epoch * grid when all are)
+    int h_to_dn;              // layer: the gate_up finish also quantises h into op[down].aq/as
     int* tickets[kMaxLists];
     float* partials;          // per list: 2 * grid slots of kMaxTokens * 256 floats
     size_t partial_list_floats;

@@ -27,11 +27,15 @@
 //               at a segment's end they leave one sum per (row, token);
 //   warp 16     producer: one lane issues the bulk copies of every unit;
 //   warp 17     helper: prepares the next chunk (plan lookup, weight scales,
-//               live quantisation of its activation groups: per token, 1 x 128,
-//               s = amax/448, RNE to E4M3) while the consumers stream the
-//               current one, and finishes segments (split-K partials and the
-//               ticketed reduction, SwiGLU or plain store, readiness flags,
-//               the combine) off the streaming path.
+//               bulk copies of its quantised activation groups) while the
+//               consumers stream the current one, and finishes segments
+//               (split-K partials and the ticketed reduction, SwiGLU or plain
+//               store, readiness flags, the combine) off the streaming path.
+// Live quantisation (per token, 1 x 128, s = amax/448, RNE to E4M3) happens
+// once per (row, group) inside the kernel: the given inputs in a first phase
+// spread over all CTAs, h in the gate_up finish that produces it.  The
+// decoded codes stay in an L2-resident workspace buffer in the consumers'
+// layout, so preparing a chunk is a few bulk copies.
 // The roles meet only through mbarriers: the stage ring (full/empty), two
 // activation slots (prep_full/act_empty) and two result slots
 // (res_full/res_empty).
@@ -39,8 +43,9 @@
 // Layer fusion (cooperative launch, all CTAs resident): CTA 0's consumers
 // compute the routing plan while the other CTAs stream the shared expert,
 // which needs no routing; gate_up finishes publish per-(expert, row block)
-// readiness of h; the helper waits (bounded) for an expert's h before
-// quantising it for down, while the producer already streams down weights;
+// readiness of h (already quantised); the helper waits (bounded) for an
+// expert's h before loading it for down, while the producer already streams
+// down weights;
 // the down finish that completes the last expert of a (token, row block)
 // also writes the combined bf16 output.  A helper never waits on another CTA
 // while it still owes a segment finish.
@@ -229,50 +234,51 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
 }
 
 // ------------------------------------------------------------------ helper
-// Quantise activation groups [g0, g0+ng) of a segment's tokens into a slot
-// (decoded values and scales), one warp, eight items' loads in flight.
-template <bool kF32>
-__device__ __noinline__ void helper_quantise(const StreamArgs& a, const Operand& op, float* act, float* act_s,
-                                             const SegMeta& m, int g0, int ng, bool dump, int lane) {
-    const int items = m.ntok * ng;
-    for (int base = 0; base < items; base += 8) {
-        float4 v[8];
-        int row[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int item = base + b;
-            row[b] = 0;
-            if (item < items) {
-                const int t = item / ng, gg = g0 + item % ng;
-                const int p = m.p0 + t;
-                // gate_up reads token rows (the shared expert's pairs are tokens
-                // 0..M-1 before any plan exists); down reads pair rows.
-                int rr = op.a_row ? (m.shared_static ? t : __ldcg(op.a_row + p)) : p;
-                if (rr < 0 || rr >= op.rows_a) {
-                    if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
-                    rr = 0;
-                }
-                row[b] = rr;
-                v[b] = load_act4<kF32>(op.a, static_cast<size_t>(op.K), rr, gg * kGroup + lane * 4);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const int item = base + b;
-            if (item >= items) break;
-            const int t = item / ng, gl = item % ng, gg = g0 + gl;
-            float s;
-            float4 dec;
-            const uint32_t codes = quant_group_warp(v[b], &s, &dec);
-            *reinterpret_cast<float4*>(act + (t * ng + gl) * kGroup + act_pos(lane * 4)) = dec;
-            if (lane == 0) act_s[t * ng + gl] = s;
-            if (dump) {
-                *reinterpret_cast<uint32_t*>(op.qdump + static_cast<size_t>(row[b]) * op.K + gg * kGroup +
-                                             lane * 4) = codes;
-                if (lane == 0) op.sdump[static_cast<size_t>(row[b]) * op.KB + gg] = s;
+// Bounded spin until *cnt >= want (acquire).
+__device__ __forceinline__ bool wait_count(const int* cnt, int want, int* status, volatile int* abort) {
+    if (ld_acquire(cnt) - want >= 0) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ld_acquire(cnt) - want >= 0) return true;
+        if ((i & 31u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                record_error(status, MOEQ_ERR_TIMEOUT);
+                *abort = 1;
+                return false;
             }
         }
     }
+}
+
+// Stage chunk activations into slot cs: bulk copies of the already
+// quantised (decoded, consumer-layout) rows of groups [g0, g0+ng) and their
+// scales; prep_full[cs] completes when the bytes land.
+__device__ __forceinline__ void helper_load_act(const StreamArgs& a, const Operand& op, SmemTail& sm, int cs,
+                                                const SegMeta& m, int g0, int ng, int lane) {
+    int row = 0;
+    if (lane < m.ntok) {
+        const int p = m.p0 + lane;
+        // gate_up reads token rows (the shared expert's pairs are tokens 0..M-1
+        // before any plan exists); down reads pair rows.
+        row = op.a_row ? (m.shared_static ? lane : __ldcg(op.a_row + p)) : p;
+        if (row < 0 || row >= op.rows_a) {
+            record_error(a.status, MOEQ_ERR_INVALID_ARG);
+            row = 0;
+        }
+    }
+    for (int t = 0; t < m.ntok; ++t) {
+        const int rt = __shfl_sync(0xffffffffu, row, t);
+        for (int gl = lane; gl < ng; gl += 32) sm.act_s[cs][t * ng + gl] = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + gl);
+    }
+    __syncwarp();
+    const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
+    if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
+    __syncwarp();
+    fence_proxy_async();
+    if (lane < m.ntok)
+        bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
+                  &sm.prep_full[cs], l2_evict_first_policy());
 }
 
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
@@ -281,20 +287,39 @@ __device__ __noinline__ void helper_quantise(const StreamArgs& a, const Operand&
 __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta& m, const float* res, int lane,
                                              int epoch) {
     const Operand& op = a.op[m.kind];
-    if (m.valid) {
-        for (int idx = lane; idx < 128 * m.ntok; idx += 32) {
-            const int i = idx & 127, t = idx >> 7;
-            float* o = op.out + static_cast<size_t>(m.p0 + t) * op.out_ld + m.rb * 128 + i;
-            if (m.kind == kKindGU) {
+    if (m.valid && m.kind == kKindGU) {
+        // lane owns h columns 4*lane .. 4*lane+3 of this row block; in the
+        // layer the 128 columns are one K group of down: quantise it here,
+        // once, for every down CTA that will read it.
+        const Operand& dn = a.op[kKindDN];
+        for (int t = 0; t < m.ntok; ++t) {
+            float hv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = 4 * lane + j;
                 const float g = res[i * kAccLd + t];
                 const float u = res[(128 + i) * kAccLd + t];
-                *o = __fdiv_rn(g, 1.0f + expf(-g)) * u;
-            } else {
-                *o = res[i * kAccLd + t];
+                hv[j] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
             }
+            const float4 h4 = make_float4(hv[0], hv[1], hv[2], hv[3]);
+            const size_t p = static_cast<size_t>(m.p0 + t);
+            *reinterpret_cast<float4*>(op.out + p * op.out_ld + m.rb * 128 + 4 * lane) = h4;
+            if (a.h_to_dn) {
+                float sc;
+                float4 dec;
+                quant_group_warp(h4, &sc, &dec);
+                *reinterpret_cast<float4*>(dn.aq + (p * dn.KB + m.rb) * kGroup + act_pos(4 * lane)) = dec;
+                if (lane == 0) dn.as[p * dn.KB + m.rb] = sc;
+            }
+        }
+    } else if (m.valid) {
+        for (int idx = lane; idx < 128 * m.ntok; idx += 32) {
+            const int i = idx & 127, t = idx >> 7;
+            op.out[static_cast<size_t>(m.p0 + t) * op.out_ld + m.rb * 128 + i] = res[i * kAccLd + t];
         }
     }
     if (m.kind == kKindGU && a.fused_route) {
+        fence_proxy_async();
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release(a.h_ready + static_cast<size_t>(m.slot) * op.RB + m.rb, epoch);
@@ -383,11 +408,11 @@ __device__ __noinline__ void helper_finish(const StreamArgs& a, SmemTail& sm, lo
 // The helper walks the same lists / segments as the producer, cut into
 // chunks: prepare chunk c (scales, quantised activations, descriptor), then
 // finish the segment whose last chunk is c-1.
-template <bool kGuF32, bool kDnF32>
 __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
     long long c = 0;         // chunks prepared
     long long sidx = 0;      // segments started
     long long owed = -1;     // a fully prepared segment not yet finished
+    bool have_input = false;
     int U = 0;
     bool have_plan = !a.fused_route;
     for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
@@ -448,6 +473,17 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
             m.lo = L.lo;
             m.KU = L.KU;
             m.RB = L.RB;
+            // activations quantised by the kernel's first phase: all CTAs' shares
+            if (op.quant_input && !have_input) {
+                if (owed >= 0) {
+                    helper_finish(a, sm, owed, lane, epoch);
+                    owed = -1;
+                }
+                if (lane == 0)
+                    wait_count(a.a_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
+                __syncwarp();
+                have_input = true;
+            }
             // down in the layer needs this expert's complete h: finish what is
             // owed, then wait (lanes check the row-block flags in parallel)
             if (m.kind == kKindDN && a.fused_route) {
@@ -459,9 +495,8 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
                 for (int j = lane; j < nrb; j += 32)
                     wait_flag(a.h_ready + static_cast<size_t>(m.slot) * nrb + j, epoch, a.status, &sm.abort_flag);
                 __syncwarp();
+                fence_proxy_async();
             }
-            const bool dump = m.valid && op.qdump != nullptr && m.rb == 0 &&
-                              (m.kind == kKindDN || m.shared_static || m.e_local == L.n_exp - 1);
             const int cu = max(1, (kActSlot / (kGroup * m.ntok)) / GPU);  // units per chunk
             for (int ua = m.ku0; ua < m.ku1; ua += cu) {
                 const int ub = min(m.ku1, ua + cu);
@@ -482,10 +517,6 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
                     const int nb = m.rb + (b ? L.RB : 0);
                     sm.sw[cs][b][gl] = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
                 }
-                if (m.kind == kKindGU)
-                    helper_quantise<kGuF32>(a, op, sm.act[cs], sm.act_s[cs], m, g0, ng, dump, lane);
-                else
-                    helper_quantise<kDnF32>(a, op, sm.act[cs], sm.act_s[cs], m, g0, ng, dump, lane);
                 if (lane == 0) {
                     ChunkDesc d;
                     d.kind = m.kind;
@@ -497,8 +528,7 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
                     d.seg_end = ub == m.ku1;
                     sm.chunk[cs] = d;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+                helper_load_act(a, op, sm, cs, m, g0, ng, lane);   // ends with the prep_full arrival
                 ++c;
                 // the previous segment is fully prepared and the consumers
                 // have its successor's first chunk: finish it now
@@ -716,6 +746,41 @@ struct ConsumerSync {
     __device__ __forceinline__ void operator()() const { consumer_sync(); }
 };
 
+// The kernel's first phase: the inputs given as activations (x for gate_up;
+// for a standalone down call, its input) are live-quantised once, each
+// (row, 128-group) by one consumer warp of one CTA, into the decoded
+// consumer layout that chunk loads copy from.  CTA 0 routes instead when the
+// layer is fused.
+template <bool kGuF32, bool kDnF32>
+__device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int lane) {
+    const bool skip0 = a.fused_route && gridDim.x > 1;
+    const long long G = gridDim.x - (skip0 ? 1 : 0);
+    const long long c = static_cast<long long>(blockIdx.x) - (skip0 ? 1 : 0);
+    if (c < 0) return;
+    const long long n0 = a.op[0].quant_input ? static_cast<long long>(a.op[0].rows_a) * a.op[0].KB : 0;
+    const long long n1 = a.op[1].quant_input ? static_cast<long long>(a.op[1].rows_a) * a.op[1].KB : 0;
+    const long long n = n0 + n1;
+    const long long lo = c * n / G, hi = (c + 1) * n / G;
+    for (long long i = lo + warp; i < hi; i += kCW) {
+        const int k = i < n0 ? 0 : 1;
+        const Operand& op = a.op[k];
+        const long long j = i < n0 ? i : i - n0;
+        const int row = static_cast<int>(j / op.KB), g = static_cast<int>(j % op.KB);
+        const float4 v = (k == 0 ? kGuF32 : kDnF32)
+                             ? load_act4<true>(op.a, static_cast<size_t>(op.K), row, g * kGroup + lane * 4)
+                             : load_act4<false>(op.a, static_cast<size_t>(op.K), row, g * kGroup + lane * 4);
+        float sc;
+        float4 dec;
+        const uint32_t codes = quant_group_warp(v, &sc, &dec);
+        *reinterpret_cast<float4*>(op.aq + (static_cast<size_t>(row) * op.KB + g) * kGroup + act_pos(lane * 4)) = dec;
+        if (lane == 0) op.as[static_cast<size_t>(row) * op.KB + g] = sc;
+        if (op.qdump) {
+            *reinterpret_cast<uint32_t*>(op.qdump + static_cast<size_t>(row) * op.K + g * kGroup + lane * 4) = codes;
+            if (lane == 0) op.sdump[static_cast<size_t>(row) * op.KB + g] = sc;
+        }
+    }
+}
+
 template <bool kGuF32, bool kDnF32>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -737,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    const int epoch = a.fused_route ? ld_relaxed(a.epoch) + 1 : 0;
+    const int epoch = ld_relaxed(a.epoch) + 1;
     __syncthreads();
 
     if (warp == kProducerWarp) {
@@ -747,8 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     if (warp == kHelperWarp) {
         // CTA 0's consumers write the routing plan into the activation slots'
         // memory first; the helper waits for the plan before touching them.
-        helper<kGuF32, kDnF32>(a, sm, lane, epoch);
-        if (a.fused_route && lane == 0) {
+        helper(a, sm, lane, epoch);
+        if (lane == 0) {
             // The last CTA to finish publishes the epoch for the next launch.
             __threadfence();
             if (atomicAdd(a.done, 1) == static_cast<int>(gridDim.x) - 1) {
@@ -768,6 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         consumer_sync();
         if (tid == 0) st_release(a.route_flag, epoch);
     }
+    quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
+    fence_proxy_async();
+    __threadfence();
+    consumer_sync();
+    if (tid == 0) atomicAdd(a.a_cnt, 1);
     long long c = 0, it = 0, sidx = 0;
     for (;;) {
         const int cs = static_cast<int>(c & 1);

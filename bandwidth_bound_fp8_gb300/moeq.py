@@ -71,7 +71,7 @@ def load(path: str = LIB_PATH):
         "moeq_route_plan_bytes": (_sz, [_i, _i, _i]),
         "moeq_route_plan_carve": (_i, [_vp, _sz, _i, _i, _i, ctypes.POINTER(moeq_route_plan)]),
         "moeq_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-        "moeq_gemm_workspace_size": (_sz, [_i, _i, _i]),
+        "moeq_gemm_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
         "moeq_workspace_init": (_i, [_vp, _sz, _vp]),
         "moeq_read_device_status": (_i, [_vp, _sz, ctypes.POINTER(_i)]),
         "moeq_quant_act": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
@@ -149,8 +149,8 @@ def moeq_workspace_size(M, H, I, n_experts_incl_shared, top_k) -> int:
     return load().moeq_workspace_size(M, H, I, n_experts_incl_shared, top_k)
 
 
-def moeq_gemm_workspace_size(rows_out, max_uniq, is_gate_up) -> int:
-    return load().moeq_gemm_workspace_size(rows_out, max_uniq, int(bool(is_gate_up)))
+def moeq_gemm_workspace_size(rows_out, K, rows_in, max_uniq, is_gate_up) -> int:
+    return load().moeq_gemm_workspace_size(rows_out, K, rows_in, max_uniq, int(bool(is_gate_up)))
 
 
 class RoutePlan:

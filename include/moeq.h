@@ -124,10 +124,11 @@ moeq_status moeq_route_plan_carve(void* base, size_t bytes, int M, int E_routed,
  * the current device's SM count; returns 0 on invalid arguments or when no
  * device is present. */
 size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int top_k);
-/* Bytes needed by one standalone GEMM call.  rows_out = I for
- * moeq_expert_gemm_gateup_swiglu (is_gate_up = 1), N for moeq_expert_gemm_down
- * (is_gate_up = 0); max_uniq as for the plan the call is given. */
-size_t moeq_gemm_workspace_size(int rows_out, int max_uniq, int is_gate_up);
+/* Bytes needed by one standalone GEMM call.  gate_up (is_gate_up = 1):
+ * rows_out = I, K = H, rows_in = M; down (is_gate_up = 0): rows_out = N,
+ * K = K, rows_in = max_pairs.  max_uniq as for the plan the call is given.
+ * Depends on the current device's SM count; 0 on invalid arguments. */
+size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up);
 /* Zero the workspace (split-K tickets and the device status word) on
  * `stream`.  Needed once after allocation; kernels leave it zeroed. */
 moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream);

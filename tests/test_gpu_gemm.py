@@ -31,7 +31,7 @@ def run_down(a, ex, uniq, offs, want_dump=True):
     y = torch.full((P, N), float("nan"), device="cuda")
     qd = torch.zeros((P, K), dtype=torch.uint8, device="cuda") if want_dump else None
     sd = torch.zeros((P, K // 128), dtype=torch.float32, device="cuda") if want_dump else None
-    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, len(uniq), 0))
+    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, P, len(uniq), 0))
     moeq.moeq_expert_gemm_down(a, K, N, ex.q, ex.s, ex.E, du, do, dn, len(uniq), P, y, ws, qd, sd)
     torch.cuda.synchronize()
     assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
@@ -94,7 +94,7 @@ def run_gateup(x, ex, uniq, offs, pair_tok, I):
     h = torch.full((P, I), float("nan"), device="cuda")
     qx = torch.zeros((M, H), dtype=torch.uint8, device="cuda")
     sx = torch.zeros((M, H // 128), dtype=torch.float32, device="cuda")
-    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(I, len(uniq), 1))
+    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(I, H, M, len(uniq), 1))
     moeq.moeq_expert_gemm_gateup_swiglu(x, H, I, ex.q, ex.s, ex.E, du, do, dp, dn, len(uniq), P, h, ws, qx, sx)
     torch.cuda.synchronize()
     assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
