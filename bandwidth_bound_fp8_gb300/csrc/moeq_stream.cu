@@ -20,17 +20,18 @@
 // runs the epilogue, so results do not depend on timing.  A segment splits
 // into chunks whose quantised activations fit one shared-memory slot.
 //
-// Warp roles (576 threads):
+// Warp roles (608 threads):
 //   warps 0-15  consumers: per stage, each lane widens 16 weight bytes of a
 //               row exactly to fp32 and accumulates paired fp32 FMAs with the
 //               decoded activation codes, scaling per K group by s_a * s_w;
 //               at a segment's end they leave one sum per (row, token);
 //   warp 16     producer: one lane issues the bulk copies of every unit;
-//   warp 17     helper: prepares the next chunk (plan lookup, weight scales,
+//   warp 17     prep: prepares the next chunk (plan lookup, weight scales,
 //               bulk copies of its quantised activation groups) while the
-//               consumers stream the current one, and finishes segments
-//               (split-K partials and the ticketed reduction, SwiGLU or plain
-//               store, readiness flags, the combine) off the streaming path.
+//               consumers stream the current one;
+//   warp 18     finish: finishes segments (split-K partials and the ticketed
+//               reduction, SwiGLU or plain store, readiness flags, the
+//               combine) off the streaming path.
 // Live quantisation (per token, 1 x 128, s = amax/448, RNE to E4M3) happens
 // once per (row, group) inside the kernel: the given inputs in a first phase
 // spread over all CTAs, h in the gate_up finish that produces it.  The
@@ -38,7 +39,8 @@
 // layout, so preparing a chunk is a few bulk copies.
 // The roles meet only through mbarriers: the stage ring (full/empty), two
 // activation slots (prep_full/act_empty) and two result slots
-// (res_full/res_empty).
+// (res_full/res_empty); no role waits on another CTA while the others owe
+// it progress, so the cross-CTA dependencies (plan, h) cannot deadlock.
 //
 // Layer fusion (cooperative launch, all CTAs resident): CTA 0's consumers
 // compute the routing plan while the other CTAs stream the shared expert,
@@ -47,8 +49,7 @@
 // expert's h before loading it for down, while the producer already streams
 // down weights;
 // the down finish that completes the last expert of a (token, row block)
-// also writes the combined bf16 output.  A helper never waits on another CTA
-// while it still owes a segment finish.
+// also writes the combined bf16 output.
 #include "moeq_device.cuh"
 #include "moeq_internal.h"
 #include "moeq_route.cuh"
@@ -58,8 +59,9 @@ namespace moeq {
 constexpr int kCW = 16;                  // consumer warps
 constexpr int kConsumers = kCW * 32;
 constexpr int kProducerWarp = kCW;
-constexpr int kHelperWarp = kCW + 1;
-constexpr int kThreads = (kCW + 2) * 32;
+constexpr int kPrepWarp = kCW + 1;
+constexpr int kFinishWarp = kCW + 2;
+constexpr int kThreads = (kCW + 3) * 32;
 constexpr int kTile = 16384;
 constexpr int kStageBytes = 2 * kTile;
 constexpr int kStages = 4;
@@ -92,7 +94,8 @@ struct SmemTail {
     float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
     float res[2][kUnitRows * kAccLd];    // one sum per (row, token)
     ChunkDesc chunk[2];
-    SegMeta seg[2];
+    SegMeta seg[4];                      // by segment index & 3 (see prep_warp)
+    int n_segments;                      // total, written by the prep warp before its end marker
     uint64_t full[kStages], empty[kStages];
     uint64_t prep_full[2], act_empty[2], res_full[2], res_empty[2];
     int abort_flag;
@@ -339,24 +342,46 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
             todo &= todo - 1;
             const int tk = __shfl_sync(0xffffffffu, tok, src);
             const int* po = a.pair_of + tk * (a.top_k + 1);
-            for (int i = lane; i < 128; i += 32) {
-                const int n = m.rb * 128 + i;
-                float accv = __ldcg(op.out + static_cast<size_t>(__ldcg(po + a.top_k)) * op.out_ld + n);
-                for (int j = 0; j < a.top_k; ++j)
-                    accv = fmaf(__ldcg(a.topk_w + tk * a.top_k + j),
-                                __ldcg(op.out + static_cast<size_t>(__ldcg(po + j)) * op.out_ld + n), accv);
-                a.out_bf16[static_cast<size_t>(tk) * op.out_ld + n] = __float2bfloat16_rn(accv);
+            // lane owns columns 4*lane .. 4*lane+3; all slots' rows in flight
+            const int n = m.rb * 128 + 4 * lane;
+            const int ps = __ldcg(po + a.top_k);
+            float4 accv = __ldcg(reinterpret_cast<const float4*>(op.out + static_cast<size_t>(ps) * op.out_ld + n));
+            for (int j0 = 0; j0 < a.top_k; j0 += 8) {
+                float4 yv[8];
+                float wv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j0 + j < a.top_k) {
+                        const int pj = __ldcg(po + j0 + j);
+                        wv[j] = __ldcg(a.topk_w + tk * a.top_k + j0 + j);
+                        yv[j] = __ldcg(reinterpret_cast<const float4*>(op.out + static_cast<size_t>(pj) * op.out_ld + n));
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j0 + j < a.top_k) {
+                        accv.x = fmaf(wv[j], yv[j].x, accv.x);
+                        accv.y = fmaf(wv[j], yv[j].y, accv.y);
+                        accv.z = fmaf(wv[j], yv[j].z, accv.z);
+                        accv.w = fmaf(wv[j], yv[j].w, accv.w);
+                    }
+                }
             }
+            __nv_bfloat162 lo2 = __floats2bfloat162_rn(accv.x, accv.y), hi2 = __floats2bfloat162_rn(accv.z, accv.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+            *reinterpret_cast<uint2*>(a.out_bf16 + static_cast<size_t>(tk) * op.out_ld + n) = packed;
             if (lane == 0) a.comb[tk * op.RB + m.rb] = 0;
         }
     }
 }
 
-// Finish segment number `sidx` (its result slot is sidx & 1).
-__device__ __noinline__ void helper_finish(const StreamArgs& a, SmemTail& sm, long long sidx, int lane, int epoch) {
+// Finish segment number `sidx` (its result slot is sidx & 1), whose
+// result the consumers have published.
+__device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, long long sidx, int lane, int epoch) {
     const int rs = static_cast<int>(sidx & 1);
-    mbar_wait_or_abort(&sm.res_full[rs], static_cast<uint32_t>((sidx >> 1) & 1), sm, a.status);
-    const SegMeta m = sm.seg[rs];
+    const SegMeta m = sm.seg[sidx & 3];
     float* res = sm.res[rs];
     const int rows = m.kind == kKindGU ? 256 : 128;
     if (!(m.ku0 == 0 && m.ku1 == m.KU)) {
@@ -383,16 +408,32 @@ __device__ __noinline__ void helper_finish(const StreamArgs& a, SmemTail& sm, lo
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
             __threadfence();
-            for (int idx = lane; idx < rows * m.ntok; idx += 32) {
-                const int row = idx % rows, t = idx / rows;
-                float v = 0.0f;
+            // eight items per lane at a time, every contributor's load of a
+            // batch in flight together; contributors summed in CTA order
+            const int nitems = rows * m.ntok;
+            for (int base = 0; base < nitems; base += 8 * 32) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = 0.0f;
                 for (long long cc = c_lo; cc <= c_hi; ++cc) {
                     const long long lo = unit_lo(cc, m.T, m.G);
                     if (lo >= unit_lo(cc + 1, m.T, m.G)) continue;
                     const int slot = static_cast<int>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1));
-                    v += __ldcg(part_base + (static_cast<size_t>(slot) * kMaxTok + t) * rows + row);
+                    const float* src = part_base + static_cast<size_t>(slot) * kMaxTok * rows;
+                    float w[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int idx = base + j * 32 + lane;
+                        w[j] = idx < nitems ? __ldcg(src + (idx / rows) * rows + idx % rows) : 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] += w[j];
                 }
-                res[row * kAccLd + t] = v;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int idx = base + j * 32 + lane;
+                    if (idx < nitems) res[(idx % rows) * kAccLd + idx / rows] = v[j];
+                }
             }
             __syncwarp();
             if (lane == 0) a.tickets[m.li][rblk] = 0;
@@ -401,27 +442,22 @@ __device__ __noinline__ void helper_finish(const StreamArgs& a, SmemTail& sm, lo
     } else {
         helper_epilogue(a, m, res, lane, epoch);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.res_empty[rs]);
 }
 
-// The helper walks the same lists / segments as the producer, cut into
-// chunks: prepare chunk c (scales, quantised activations, descriptor), then
-// finish the segment whose last chunk is c-1.
-__device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
+// The prep warp walks the same lists / segments as the producer, cut into
+// chunks, and prepares each chunk (scales, activation rows, descriptor) at
+// most two chunks ahead of the consumers.  Segment metadata goes to
+// seg[segment & 3]: when segment S+4 is written the consumers have started
+// S+3, hence the finish of S+1 ... and of S is done.
+__device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
     long long c = 0;         // chunks prepared
     long long sidx = 0;      // segments started
-    long long owed = -1;     // a fully prepared segment not yet finished
     bool have_input = false;
     int U = 0;
     bool have_plan = !a.fused_route;
     for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
         if (list_needs_plan(a, li)) {
             if (!have_plan) {
-                if (owed >= 0) {  // never wait on another CTA while owing a finish
-                    helper_finish(a, sm, owed, lane, epoch);
-                    owed = -1;
-                }
                 if (lane == 0) wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
                 __syncwarp();
                 have_plan = true;
@@ -475,22 +511,13 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
             m.RB = L.RB;
             // activations quantised by the kernel's first phase: all CTAs' shares
             if (op.quant_input && !have_input) {
-                if (owed >= 0) {
-                    helper_finish(a, sm, owed, lane, epoch);
-                    owed = -1;
-                }
-                if (lane == 0)
-                    wait_count(a.a_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
+                if (lane == 0) wait_count(a.a_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
                 __syncwarp();
                 have_input = true;
             }
-            // down in the layer needs this expert's complete h: finish what is
-            // owed, then wait (lanes check the row-block flags in parallel)
+            // down in the layer needs this expert's complete h (lanes check the
+            // row-block flags in parallel); the finish warp keeps finishing
             if (m.kind == kKindDN && a.fused_route) {
-                if (owed >= 0) {
-                    helper_finish(a, sm, owed, lane, epoch);
-                    owed = -1;
-                }
                 const int nrb = a.op[kKindGU].RB;
                 for (int j = lane; j < nrb; j += 32)
                     wait_flag(a.h_ready + static_cast<size_t>(m.slot) * nrb + j, epoch, a.status, &sm.abort_flag);
@@ -502,14 +529,7 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
                 const int ub = min(m.ku1, ua + cu);
                 const int cs = static_cast<int>(c & 1);
                 if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
-                if (ua == m.ku0) {
-                    // a new segment: its result slot must have been finished
-                    if (owed >= 0 && owed == sidx - 2) {
-                        helper_finish(a, sm, owed, lane, epoch);
-                        owed = -1;
-                    }
-                    if (lane == 0) sm.seg[sidx & 1] = m;
-                }
+                if (ua == m.ku0 && lane == 0) sm.seg[sidx & 3] = m;
                 const int g0 = ua * GPU, g1 = min(op.KB, ub * GPU), ng = g1 - g0;
                 for (int i = lane; i < ng * 2; i += 32) {
                     const int b = i / ng, gl = i % ng;
@@ -530,27 +550,33 @@ __device__ __forceinline__ void helper(const StreamArgs& a, SmemTail& sm, int la
                 }
                 helper_load_act(a, op, sm, cs, m, g0, ng, lane);   // ends with the prep_full arrival
                 ++c;
-                // the previous segment is fully prepared and the consumers
-                // have its successor's first chunk: finish it now
-                if (owed >= 0 && ua == m.ku0) {
-                    helper_finish(a, sm, owed, lane, epoch);
-                    owed = -1;
-                }
             }
-            owed = sidx;
             ++sidx;
             u = seg_end_u;
         }
     }
-    // end marker, then the last finish
-    {
-        const int cs = static_cast<int>(c & 1);
-        if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
-        if (lane == 0) sm.chunk[cs].kind = -1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+    // end marker (the consumers pass it on to the finish warp)
+    const int cs = static_cast<int>(c & 1);
+    if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
+    if (lane == 0) {
+        sm.n_segments = static_cast<int>(sidx);
+        sm.chunk[cs].kind = -1;
     }
-    if (owed >= 0 && !sm.abort_flag) helper_finish(a, sm, owed, lane, epoch);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+}
+
+// The finish warp finishes segments in order as the consumers publish them,
+// until the consumers pass on the prep warp's end marker.
+__device__ __forceinline__ void finish_warp(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
+    for (long long sidx = 0;; ++sidx) {
+        const int rs = static_cast<int>(sidx & 1);
+        mbar_wait_or_abort(&sm.res_full[rs], static_cast<uint32_t>((sidx >> 1) & 1), sm, a.status);
+        if (sm.abort_flag || sidx >= static_cast<volatile int&>(sm.n_segments)) break;
+        finish_segment(a, sm, sidx, lane, epoch);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.res_empty[rs]);
+    }
 }
 
 // ------------------------------------------------------------------ consumers
@@ -800,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(&sm.res_empty[s], 1);
         }
         sm.abort_flag = 0;
+        sm.n_segments = 0x7fffffff;
         fence_mbar_init();
     }
     const int epoch = ld_relaxed(a.epoch) + 1;
@@ -809,10 +836,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         if (lane == 0) producer(a, sm, stages, epoch);
         return;
     }
-    if (warp == kHelperWarp) {
+    if (warp == kPrepWarp) {
         // CTA 0's consumers write the routing plan into the activation slots'
-        // memory first; the helper waits for the plan before touching them.
-        helper(a, sm, lane, epoch);
+        // memory first; the prep warp waits for the plan before touching them.
+        prep_warp(a, sm, lane, epoch);
+        return;
+    }
+    if (warp == kFinishWarp) {
+        finish_warp(a, sm, lane, epoch);
         if (lane == 0) {
             // The last CTA to finish publishes the epoch for the next launch.
             __threadfence();
@@ -828,24 +859,32 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     // ---------------------------------------------------------------- consumers
     const int cw = warp;
     if (a.fused_route && blockIdx.x == 0) {
+        // CTA 0 has no share of the input quantisation while it routes
+        if (tid == 0) atomicAdd(a.a_cnt, 1);
         route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, a.plan, sm.route, tid, ConsumerSync{});
         __threadfence();
         consumer_sync();
         if (tid == 0) st_release(a.route_flag, epoch);
+    } else {
+        quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
+        fence_proxy_async();
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) atomicAdd(a.a_cnt, 1);
     }
-    quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
-    fence_proxy_async();
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) atomicAdd(a.a_cnt, 1);
     long long c = 0, it = 0, sidx = 0;
     for (;;) {
+        const int rs = static_cast<int>(sidx & 1);
+        if (sidx >= 2) mbar_wait_or_abort(&sm.res_empty[rs], static_cast<uint32_t>(((sidx >> 1) - 1) & 1), sm, a.status);
         const int cs = static_cast<int>(c & 1);
         mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
         const int kind = sm.chunk[cs].kind;
-        if (kind < 0 || sm.abort_flag) break;
-        const int rs = static_cast<int>(sidx & 1);
-        if (sidx >= 2) mbar_wait_or_abort(&sm.res_empty[rs], static_cast<uint32_t>(((sidx >> 1) - 1) & 1), sm, a.status);
+        if (kind < 0 || sm.abort_flag) {
+            // pass the end on to the finish warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+            break;
+        }
         const int ntok = sm.chunk[cs].ntok;
         if (kind == kKindGU)
             consume_dispatch<kKindGU>(a, sm, stages, rs, ntok, cw, lane, c, it);
