@@ -97,9 +97,9 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.h = align_up(l.plan + moeq_route_plan_bytes(M, E, k), 256);
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
     const size_t after = l.y + sizeof(float) * static_cast<size_t>(mp) * H;
-    const int tk[4] = {I / 128, mu * (I / 128), H / 128, mu * (H / 128)};
+    const int tk[6] = {I / 128, mu * (I / 128), mu * (I / 128), H / 128, mu * (H / 128), mu * (H / 128)};
     const int rows[2] = {M, mp}, ks[2] = {H, I};
-    l.s = stream_ws_layout(after, rows, ks, 4, tk, grid, mu * (I / 128), M * (H / 128));
+    l.s = stream_ws_layout(after, rows, ks, 6, tk, grid, mu * (I / 128), M * (H / 128));
     return l;
 }
 
@@ -428,10 +428,10 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     d.rows_a = mp;
     d.out = y;
     d.out_ld = H;
-    a.n_lists = 4;
-    const int kinds[4] = {kKindGU, kKindGU, kKindDN, kKindDN};
-    const int srcs[4] = {kSrcShared, kSrcPlanRouted, kSrcShared, kSrcPlanRouted};
-    for (int i = 0; i < 4; ++i) {
+    a.n_lists = 6;
+    const int kinds[6] = {kKindGU, kKindGU, kKindGU, kKindDN, kKindDN, kKindDN};
+    const int srcs[6] = {kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB, kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB};
+    for (int i = 0; i < 6; ++i) {
         a.list_kind[i] = kinds[i];
         a.list_src[i] = srcs[i];
     }

@@ -13,12 +13,13 @@
 namespace moeq {
 
 constexpr int kMaxTokens = MOEQ_MAX_TOKENS;
-constexpr int kMaxLists = 4;
+constexpr int kMaxLists = 6;
 constexpr int kKindGU = 0;  // gate_up: a stage holds the gate tile and the up tile of one K group
 constexpr int kKindDN = 1;  // down: a stage holds two consecutive K tiles of one row block
 constexpr int kSrcShared = 0;     // the layer's shared expert, known before routing
 constexpr int kSrcPlanAll = 1;    // every unique expert of the plan (standalone calls)
-constexpr int kSrcPlanRouted = 2; // the plan's routed experts (all but the last)
+constexpr int kSrcPlanRoutedA = 2; // the first half of the plan's routed experts
+constexpr int kSrcPlanRoutedB = 3; // the second half (down of half A hides the finish of half B's h)
 
 // One GEMM operand set.  Weights are tile-major: tile (e, nb, kb) -- the
 // 128 x 128 block of rows nb*128.. and columns kb*128.. of expert e -- is 16

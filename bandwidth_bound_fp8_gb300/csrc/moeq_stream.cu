@@ -114,7 +114,7 @@ __device__ __forceinline__ int act_pos(int k) { return (((k & 15) >> 2) * 8 + (k
 
 // ------------------------------------------------------------------ work lists
 struct ListInfo {
-    int kind, src, n_exp, RB, KU;
+    int kind, src, n_exp, e0, RB, KU;  // experts e0 .. e0+n_exp-1 of the plan (or the static shared one)
     long long T, G, c;   // units, participating CTAs, this CTA's index among them
     long long lo, hi;    // this CTA's share [lo, hi)
 };
@@ -132,8 +132,11 @@ __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U
     ListInfo L;
     L.kind = a.list_kind[li];
     L.src = a.list_src[li];
-    L.n_exp = L.src == kSrcShared ? 1 : (L.src == kSrcPlanAll ? U : U - 1);
-    if (L.n_exp < 0) L.n_exp = 0;
+    const int routed = U > 1 ? U - 1 : 0, half = (routed + 1) / 2;
+    L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
+    L.n_exp = L.src == kSrcShared ? 1
+            : L.src == kSrcPlanAll ? U
+            : L.src == kSrcPlanRoutedA ? half : routed - half;
     const Operand& op = a.op[L.kind];
     L.RB = op.RB;
     L.KU = L.kind == kKindGU ? op.KB : (op.KB + 1) / 2;
@@ -205,7 +208,7 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
             const int rb = rem / L.KU, ku = rem - rb * L.KU;
             if (e_local != cur) {
                 cur = e_local;
-                expert = L.src == kSrcShared ? a.shared_id : __ldcg(a.uniq + e_local);
+                expert = L.src == kSrcShared ? a.shared_id : __ldcg(a.uniq + L.e0 + e_local);
                 if (expert < 0 || expert >= a.n_experts) expert = 0;
             }
             const int s = static_cast<int>(issued % kStages);
@@ -489,10 +492,11 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 m.slot = a.max_uniq - 1;
                 m.shared_static = 1;
             } else {
-                m.expert = __ldcg(a.uniq + m.e_local);
-                m.p0 = __ldcg(a.offs + m.e_local);
-                m.ntok = __ldcg(a.offs + m.e_local + 1) - m.p0;
-                m.slot = m.e_local;
+                const int ue = L.e0 + m.e_local;
+                m.expert = __ldcg(a.uniq + ue);
+                m.p0 = __ldcg(a.offs + ue);
+                m.ntok = __ldcg(a.offs + ue + 1) - m.p0;
+                m.slot = ue;
                 m.shared_static = 0;
             }
             m.valid = m.expert >= 0 && m.expert < a.n_experts && m.p0 >= 0 && m.ntok >= 1 && m.ntok <= kMaxTok &&
