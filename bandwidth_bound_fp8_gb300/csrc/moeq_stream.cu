@@ -20,7 +20,7 @@
 // runs the epilogue, so results do not depend on timing.  A segment splits
 // into chunks whose quantised activations fit one shared-memory slot.
 //
-// Warp roles (608 threads):
+// Warp roles (640 threads):
 //   warps 0-15  consumers: per stage, each lane widens 16 weight bytes of a
 //               row exactly to fp32 and accumulates paired fp32 FMAs with the
 //               decoded activation codes, scaling per K group by s_a * s_w;
@@ -29,9 +29,9 @@
 //   warp 17     prep: prepares the next chunk (plan lookup, weight scales,
 //               bulk copies of its quantised activation groups) while the
 //               consumers stream the current one;
-//   warp 18     finish: finishes segments (split-K partials and the ticketed
+//   warps 18-19 finish: finish segments (split-K partials and the ticketed
 //               reduction, SwiGLU or plain store, readiness flags, the
-//               combine) off the streaming path.
+//               combine) off the streaming path, even and odd segments.
 // Live quantisation (per token, 1 x 128, s = amax/448, RNE to E4M3) happens
 // once per (row, group) inside the kernel: the given inputs in a first phase
 // spread over all CTAs, h in the gate_up finish that produces it.  The
@@ -60,8 +60,9 @@ constexpr int kCW = 16;                  // consumer warps
 constexpr int kConsumers = kCW * 32;
 constexpr int kProducerWarp = kCW;
 constexpr int kPrepWarp = kCW + 1;
-constexpr int kFinishWarp = kCW + 2;
-constexpr int kThreads = (kCW + 3) * 32;
+constexpr int kFinishWarp0 = kCW + 2;    // finishes even segments (result slot 0)
+constexpr int kFinishWarp1 = kCW + 3;    // finishes odd segments (result slot 1)
+constexpr int kThreads = (kCW + 4) * 32;
 constexpr int kTile = 16384;
 constexpr int kStageBytes = 2 * kTile;
 constexpr int kStages = 4;
@@ -96,6 +97,7 @@ struct SmemTail {
     ChunkDesc chunk[2];
     SegMeta seg[4];                      // by segment index & 3 (see prep_warp)
     int n_segments;                      // total, written by the prep warp before its end marker
+    int finish_done;                     // finish warps that have ended
     uint64_t full[kStages], empty[kStages];
     uint64_t prep_full[2], act_empty[2], res_full[2], res_empty[2];
     int abort_flag;
@@ -570,11 +572,10 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
     if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
 }
 
-// The finish warp finishes segments in order as the consumers publish them,
-// until the consumers pass on the prep warp's end marker.
-__device__ __forceinline__ void finish_warp(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
-    for (long long sidx = 0;; ++sidx) {
-        const int rs = static_cast<int>(sidx & 1);
+// Finish warp rs finishes segments rs, rs+2, rs+4, ... (result slot rs) as
+// the consumers publish them, until the consumers pass on the end marker.
+__device__ __forceinline__ void finish_warp(const StreamArgs& a, SmemTail& sm, int rs, int lane, int epoch) {
+    for (long long sidx = rs;; sidx += 2) {
         mbar_wait_or_abort(&sm.res_full[rs], static_cast<uint32_t>((sidx >> 1) & 1), sm, a.status);
         if (sm.abort_flag || sidx >= static_cast<volatile int&>(sm.n_segments)) break;
         finish_segment(a, sm, sidx, lane, epoch);
@@ -831,6 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         }
         sm.abort_flag = 0;
         sm.n_segments = 0x7fffffff;
+        sm.finish_done = 0;
         fence_mbar_init();
     }
     const int epoch = ld_relaxed(a.epoch) + 1;
@@ -846,9 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         prep_warp(a, sm, lane, epoch);
         return;
     }
-    if (warp == kFinishWarp) {
-        finish_warp(a, sm, lane, epoch);
-        if (lane == 0) {
+    if (warp == kFinishWarp0 || warp == kFinishWarp1) {
+        finish_warp(a, sm, warp - kFinishWarp0, lane, epoch);
+        // the second finish warp to end closes the CTA's work
+        if (lane == 0 && atomicAdd(&sm.finish_done, 1) == 1) {
             // The last CTA to finish publishes the epoch for the next launch.
             __threadfence();
             if (atomicAdd(a.done, 1) == static_cast<int>(gridDim.x) - 1) {
@@ -884,9 +887,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
         const int kind = sm.chunk[cs].kind;
         if (kind < 0 || sm.abort_flag) {
-            // pass the end on to the finish warp
+            // pass the end on to both finish warps (slot rs now, the other
+            // slot once its last segment is finished)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+            const long long s2 = sidx + 1;
+            if (s2 >= 2) mbar_wait_or_abort(&sm.res_empty[s2 & 1], static_cast<uint32_t>(((s2 >> 1) - 1) & 1), sm, a.status);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.res_full[s2 & 1]);
             break;
         }
         const int ntok = sm.chunk[cs].ntok;
