@@ -667,7 +667,7 @@ __device__ __forceinline__ float reduce8(float v) {
 }
 
 // One segment, chunk after chunk, for one consumer warp.  Leaves one sum per
-// (row of this warp, token) in result slot rs.  MODE 1/2/4: up to that many
+// (row of this warp, token) in result slot rs.  MODE 1/2: up to that many
 // tokens with running sums in registers; MODE 0: any count, two tokens at a
 // time, each K group reduced across lanes into the result slot.
 template <int KIND, int MODE>
@@ -710,12 +710,7 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
                     float scl[MT];
 #pragma unroll
                     for (int t = 0; t < MT; ++t) scl[t] = act_s[min(t, ntok - 1) * d.ng + gl] * swg;
-                    if (MT <= 2) {
-                        tile_dot_acc<MT, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
-                    } else {  // four tokens as two pairs: fewer live registers
-                        tile_dot_acc<2, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
-                        tile_dot_acc<2, PASSES, 2, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
-                    }
+                    tile_dot_acc<MT, PASSES, 0, MT>(tile, rows_base, act_g, tok_ld, ntok, lane, scl, acc);
                 } else {
                     for (int t0 = 0; t0 < ntok; t0 += 2) {
                         float part[PASSES][2];
@@ -754,6 +749,8 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
     }
 }
 
+// Every mode runs out of line: each gets the whole register budget for its
+// streaming loop, and the consumer's outer state is saved once per segment.
 template <int KIND, int MODE>
 __device__ __noinline__ void consume_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
                                                   int cw, int lane, long long& c, long long& it) {
@@ -764,11 +761,9 @@ template <int KIND>
 __device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
                                                  int ntok, int cw, int lane, long long& c, long long& it) {
     if (ntok <= 1)
-        consume_segment<KIND, 1>(a, sm, stages, rs, cw, lane, c, it);
+        consume_segment_cold<KIND, 1>(a, sm, stages, rs, cw, lane, c, it);
     else if (ntok <= 2)
-        consume_segment<KIND, 2>(a, sm, stages, rs, cw, lane, c, it);
-    else if (ntok <= 4)
-        consume_segment_cold<KIND, 4>(a, sm, stages, rs, cw, lane, c, it);
+        consume_segment_cold<KIND, 2>(a, sm, stages, rs, cw, lane, c, it);
     else
         consume_segment_cold<KIND, 0>(a, sm, stages, rs, cw, lane, c, it);
 }
