@@ -29,6 +29,53 @@ struct RouteScratch {
     int total[2];
 };
 
+// Order-preserving map of a float to an unsigned key (-0 folded onto +0, so
+// that equal values tie exactly as they compare).
+__device__ __forceinline__ uint32_t route_key(float f) {
+    const uint32_t u = __float_as_uint(f + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float route_key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Top-k of one token's logits by one warp: lane l holds experts l, l+32, ...;
+// each round takes the warp maximum of the key, then the smallest expert id
+// holding it (ties to the lower id), with two warp reductions.
+template <int NPER>
+__device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int E, int k, int lane, int* ids,
+                                                float* vals) {
+    uint32_t key[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? route_key(__ldcg(l + e)) : 0u;
+    }
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const bool ok = (lane + 32 * i < E) && !((taken >> i) & 1u);
+            if (ok && (bi < 0 || key[i] > bk)) {
+                bk = key[i];
+                bi = i;
+            }
+        }
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const int cand = (bi >= 0 && bk == wk) ? lane + 32 * bi : 0x7fffffff;
+        const int we = __reduce_min_sync(0xffffffffu, cand);
+        if ((we & 31) == lane) taken |= 1u << (we >> 5);
+        if (lane == 0) {
+            ids[j] = we;
+            vals[j] = route_key_value(wk);
+        }
+    }
+    __syncwarp();
+}
+
 // Computes the plan with NT threads (tid in [0, NT)); `sync` is a barrier
 // over exactly those threads.  Writes every plan member to global memory;
 // the caller makes the writes visible (fence + flag) as it needs.
@@ -41,44 +88,10 @@ __device__ __forceinline__ void route_compute(const float* __restrict__ logits, 
 
     for (int m = warp; m < M; m += kWarps) {
         const float* l = logits + static_cast<size_t>(m) * E;
-        constexpr int kPer = kRouteMaxE / 32;
-        float v[kPer];
-        uint32_t taken = 0;
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = e < E ? __ldcg(l + e) : -FLT_MAX;
-        }
-        const int nper = (E + 31) / 32;
-        for (int j = 0; j < k; ++j) {
-            float bv = -FLT_MAX;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                if (i < nper) {
-                    const int e = lane + 32 * i;
-                    if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-                        bv = v[i];
-                        be = e;
-                    }
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == 0) {
-                s.id[m][j] = be;
-                s.lv[m][j] = bv;
-            }
-            __syncwarp();
-        }
+        if (E <= 256)
+            route_topk_warp<8>(l, E, k, lane, s.id[m], s.lv[m]);
+        else
+            route_topk_warp<kRouteMaxE / 32>(l, E, k, lane, s.id[m], s.lv[m]);
         float ex = 0.0f;
         if (lane < k) ex = expf(s.lv[m][lane] - s.lv[m][0]);
         float den = ex;

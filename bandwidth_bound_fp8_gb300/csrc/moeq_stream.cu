@@ -259,11 +259,13 @@ __device__ __forceinline__ bool wait_count(const int* cnt, int want, int* status
     }
 }
 
-// Stage chunk activations into slot cs: bulk copies of the already
-// quantised (decoded, consumer-layout) rows of groups [g0, g0+ng) and their
-// scales; prep_full[cs] completes when the bytes land.
-__device__ __forceinline__ void helper_load_act(const StreamArgs& a, const Operand& op, SmemTail& sm, int cs,
-                                                const SegMeta& m, int g0, int ng, int lane) {
+// Stage a chunk into slot cs: bulk copies of the already quantised
+// (decoded, consumer-layout) activation rows of groups [g0, g0+ng), their
+// scales, the weight scales and the descriptor.  Every load is issued before
+// any is waited for; prep_full[cs] completes when the copied bytes land.
+__device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& op, SmemTail& sm, int cs,
+                                           const SegMeta& m, const ListInfo& L, const ChunkDesc& d, int lane) {
+    const int g0 = d.g0, ng = d.ng;
     int row = 0;
     if (lane < m.ntok) {
         const int p = m.p0 + lane;
@@ -275,18 +277,45 @@ __device__ __forceinline__ void helper_load_act(const StreamArgs& a, const Opera
             row = 0;
         }
     }
-    for (int t = 0; t < m.ntok; ++t) {
-        const int rt = __shfl_sync(0xffffffffu, row, t);
-        for (int gl = lane; gl < ng; gl += 32) sm.act_s[cs][t * ng + gl] = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + gl);
-    }
-    __syncwarp();
     const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
-    if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
-    __syncwarp();
     fence_proxy_async();
     if (lane < m.ntok)
         bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
                   &sm.prep_full[cs], l2_evict_first_policy());
+    // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all loads first
+    const int n_as = m.ntok * ng, n_sw = ng * (m.kind == kKindGU ? 2 : 1);
+    constexpr int kPer = (kChunkGroups * 3 + 31) / 32;   // <= 48 + 96 values over 32 lanes
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = lane + 32 * j;
+        float x = 0.0f;
+        if (i < n_as) {
+            const int t = i / ng, gl = i % ng;
+            const int rt = __shfl_sync(0xffffffffu, row, t);   // uniform: t < ntok <= 16 < 32
+            x = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + gl);
+        } else if (i < n_as + n_sw) {
+            const int q = i - n_as, b = q / ng, gl = q % ng;
+            const int nb = m.rb + (b ? L.RB : 0);
+            x = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
+        } else {
+            __shfl_sync(0xffffffffu, row, 0);                   // keep the shuffle uniform
+        }
+        v[j] = x;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = lane + 32 * j;
+        if (i < n_as) {
+            sm.act_s[cs][i] = v[j];
+        } else if (i < n_as + n_sw) {
+            const int q = i - n_as;
+            sm.sw[cs][q / ng][q % ng] = v[j];
+        }
+    }
+    if (lane == 0) sm.chunk[cs] = d;
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
 }
 
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
@@ -327,21 +356,19 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
         }
     }
     if (m.kind == kKindGU && a.fused_route) {
-        fence_proxy_async();
-        __threadfence();
+        fence_proxy_async();   // h codes are read back by bulk copies
         __syncwarp();
         if (lane == 0) st_release(a.h_ready + static_cast<size_t>(m.slot) * op.RB + m.rb, epoch);
     }
     if (m.kind == kKindDN && a.fused_combine) {
-        __threadfence();
-        __syncwarp();
+        __syncwarp();   // y rows of every lane before the (acq_rel) combine tickets
         int tok = -1, last = 0;
         if (lane < m.ntok && m.valid) {
             tok = m.shared_static ? lane : __ldcg(a.pair_tok + m.p0 + lane);
-            if (tok >= 0 && tok < a.M) last = atomicAdd(a.comb + tok * op.RB + m.rb, 1) == a.top_k;
+            if (tok >= 0 && tok < a.M) last = atom_add_acq_rel(a.comb + tok * op.RB + m.rb, 1) == a.top_k;
         }
         uint32_t todo = __ballot_sync(0xffffffffu, last);
-        if (todo) __threadfence();
+        __syncwarp();   // the ticket lanes' acquires before every lane's loads
         while (todo) {
             const int src = __ffs(todo) - 1;
             todo &= todo - 1;
@@ -351,11 +378,11 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
             const int n = m.rb * 128 + 4 * lane;
             const int ps = __ldcg(po + a.top_k);
             float4 accv = __ldcg(reinterpret_cast<const float4*>(op.out + static_cast<size_t>(ps) * op.out_ld + n));
-            for (int j0 = 0; j0 < a.top_k; j0 += 8) {
-                float4 yv[8];
-                float wv[8];
+            for (int j0 = 0; j0 < a.top_k; j0 += 4) {
+                float4 yv[4];
+                float wv[4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     if (j0 + j < a.top_k) {
                         const int pj = __ldcg(po + j0 + j);
                         wv[j] = __ldcg(a.topk_w + tk * a.top_k + j0 + j);
@@ -363,7 +390,7 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
                     }
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     if (j0 + j < a.top_k) {
                         accv.x = fmaf(wv[j], yv[j].x, accv.x);
                         accv.y = fmaf(wv[j], yv[j].y, accv.y);
@@ -402,42 +429,62 @@ __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, l
             const int row = idx % rows, t = idx / rows;
             mine[t * rows + row] = res[row * kAccLd + t];
         }
-        __threadfence();
+        // The warp barrier orders every lane's partial before lane 0's ticket;
+        // the acq_rel ticket publishes them and, for the last contributor,
+        // acquires everyone else's.
         __syncwarp();
         int last = 0;
         if (lane == 0) {
             int n = 0;
             for (long long cc = c_lo; cc <= c_hi; ++cc) n += unit_lo(cc, m.T, m.G) < unit_lo(cc + 1, m.T, m.G);
-            last = atomicAdd(a.tickets[m.li] + rblk, 1) == n - 1;
+            last = atom_add_acq_rel(a.tickets[m.li] + rblk, 1) == n - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();   // lane 0's acquire before every lane's loads
         if (last) {
-            __threadfence();
-            // eight items per lane at a time, every contributor's load of a
-            // batch in flight together; contributors summed in CTA order
-            const int nitems = rows * m.ntok;
-            for (int base = 0; base < nitems; base += 8 * 32) {
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-                for (long long cc = c_lo; cc <= c_hi; ++cc) {
+            // Lane q < kWin resolves the slot of CTA c_lo + q (null when that
+            // CTA holds no unit); the window's partials are loaded together and
+            // summed in CTA order, CTAs past the window (rare) after them.
+            constexpr int kWin = 8, kPer = 2;
+            const float* src = nullptr;
+            {
+                const long long cc = c_lo + lane;
+                if (lane < kWin && cc <= c_hi) {
                     const long long lo = unit_lo(cc, m.T, m.G);
-                    if (lo >= unit_lo(cc + 1, m.T, m.G)) continue;
-                    const int slot = static_cast<int>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1));
-                    const float* src = part_base + static_cast<size_t>(slot) * kMaxTok * rows;
-                    float w[8];
+                    if (lo < unit_lo(cc + 1, m.T, m.G))
+                        src = part_base + static_cast<size_t>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1)) * kMaxTok * rows;
+                }
+            }
+            const float* srcs[kWin];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+            for (int q = 0; q < kWin; ++q)
+                srcs[q] = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), q));
+            const bool many = c_hi - c_lo + 1 > kWin;
+            const int nitems = rows * m.ntok;
+            for (int base = 0; base < nitems; base += kPer * 32) {
+                float w[kWin][kPer];
+#pragma unroll
+                for (int q = 0; q < kWin; ++q)
+#pragma unroll
+                    for (int j = 0; j < kPer; ++j) {
                         const int idx = base + j * 32 + lane;
-                        w[j] = idx < nitems ? __ldcg(src + (idx / rows) * rows + idx % rows) : 0.0f;
+                        w[q][j] = (srcs[q] != nullptr && idx < nitems) ? __ldcg(srcs[q] + idx) : 0.0f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] += w[j];
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < kPer; ++j) {
                     const int idx = base + j * 32 + lane;
-                    if (idx < nitems) res[(idx % rows) * kAccLd + idx / rows] = v[j];
+                    float v = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < kWin; ++q) v += w[q][j];   // CTA order (absent CTAs add +0)
+                    if (many) {
+                        for (long long cc = c_lo + kWin; cc <= c_hi; ++cc) {
+                            const long long lo = unit_lo(cc, m.T, m.G);
+                            if (lo >= unit_lo(cc + 1, m.T, m.G)) continue;
+                            const int slot = static_cast<int>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1));
+                            if (idx < nitems) v += __ldcg(part_base + static_cast<size_t>(slot) * kMaxTok * rows + idx);
+                        }
+                    }
+                    if (idx < nitems) res[(idx % rows) * kAccLd + idx / rows] = v;
                 }
             }
             __syncwarp();
@@ -536,25 +583,15 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 const int cs = static_cast<int>(c & 1);
                 if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
                 if (ua == m.ku0 && lane == 0) sm.seg[sidx & 3] = m;
-                const int g0 = ua * GPU, g1 = min(op.KB, ub * GPU), ng = g1 - g0;
-                for (int i = lane; i < ng * 2; i += 32) {
-                    const int b = i / ng, gl = i % ng;
-                    if (b == 1 && m.kind != kKindGU) continue;
-                    const int nb = m.rb + (b ? L.RB : 0);
-                    sm.sw[cs][b][gl] = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
-                }
-                if (lane == 0) {
-                    ChunkDesc d;
-                    d.kind = m.kind;
-                    d.ku0 = ua;
-                    d.ku1 = ub;
-                    d.g0 = g0;
-                    d.ng = ng;
-                    d.ntok = m.ntok;
-                    d.seg_end = ub == m.ku1;
-                    sm.chunk[cs] = d;
-                }
-                helper_load_act(a, op, sm, cs, m, g0, ng, lane);   // ends with the prep_full arrival
+                ChunkDesc d;
+                d.kind = m.kind;
+                d.ku0 = ua;
+                d.ku1 = ub;
+                d.g0 = ua * GPU;
+                d.ng = min(op.KB, ub * GPU) - d.g0;
+                d.ntok = m.ntok;
+                d.seg_end = ub == m.ku1;
+                prep_chunk(a, op, sm, cs, m, L, d, lane);   // ends with the prep_full arrival
                 ++c;
             }
             ++sidx;
