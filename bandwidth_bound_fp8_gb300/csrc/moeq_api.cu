@@ -315,6 +315,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.n_experts = n_experts;
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
+    a.max_ntok = M;   // the pairs of one expert are distinct tokens
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
@@ -361,6 +362,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.n_experts = n_experts;
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
+    a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
@@ -444,6 +446,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.n_experts = E_routed + 1;
     a.max_uniq = mu;
     a.max_pairs = mp;
+    a.max_ntok = M;
     a.shared_id = E_routed;
     a.shared_p0 = M * top_k;
     a.M = M;

@@ -57,6 +57,7 @@ struct StreamArgs {
     int n_experts, max_uniq, max_pairs;
     // the layer's shared expert (id, first pair, token count)
     int shared_id, shared_p0, M;
+    int max_ntok;             // largest token (pair) count of one expert: 1 .. kMaxTokens
     // layer fusion
     int fused_route;          // CTA 0 computes the plan, the others wait for route_flag
     const float* logits;

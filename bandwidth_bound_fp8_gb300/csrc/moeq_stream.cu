@@ -60,16 +60,18 @@ constexpr int kCW = 16;                  // consumer warps
 constexpr int kConsumers = kCW * 32;
 constexpr int kProducerWarp = kCW;
 constexpr int kPrepWarp = kCW + 1;
-constexpr int kFinishWarp0 = kCW + 2;    // finishes even segments (result slot 0)
-constexpr int kFinishWarp1 = kCW + 3;    // finishes odd segments (result slot 1)
+constexpr int kFinishWarp0 = kCW + 2;    // finishes even segments
+constexpr int kFinishWarp1 = kCW + 3;    // finishes odd segments
 constexpr int kThreads = (kCW + 4) * 32;
 constexpr int kTile = 16384;
 constexpr int kStageBytes = 2 * kTile;
 constexpr int kStages = 4;
 constexpr int kActSlot = 6144;           // decoded activation floats per slot
 constexpr int kChunkGroups = kActSlot / kGroup;
-constexpr int kAccLd = kMaxTok + 1;
 constexpr int kUnitRows = 256;           // rows of a gate_up unit (gate + up); down units use 128
+constexpr int kResPool = 2 * kUnitRows * (kMaxTok + 1);   // result slot floats (two at 16 tokens)
+constexpr int kMaxRes = 8;               // result slots at most
+constexpr int kSegRing = 16;             // segment metadata entries (>= kMaxRes + 8, see prep_warp)
 
 struct ChunkDesc {
     int kind;          // kKindGU / kKindDN; -1: no more work
@@ -93,13 +95,13 @@ struct SmemTail {
     };
     float act_s[2][kChunkGroups];        // activation scales [tok][group]
     float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
-    float res[2][kUnitRows * kAccLd];    // one sum per (row, token)
+    float res[kResPool];                 // result slots: one sum per (row, token), see ResRing
     ChunkDesc chunk[2];
-    SegMeta seg[4];                      // by segment index & 3 (see prep_warp)
+    SegMeta seg[kSegRing];               // by segment index % kSegRing (see prep_warp)
     int n_segments;                      // total, written by the prep warp before its end marker
     int finish_done;                     // finish warps that have ended
     uint64_t full[kStages], empty[kStages];
-    uint64_t prep_full[2], act_empty[2], res_full[2], res_empty[2];
+    uint64_t prep_full[2], act_empty[2], res_full[kMaxRes], res_empty[kMaxRes];
     int abort_flag;
 };
 
@@ -107,6 +109,21 @@ constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumers); }
+
+// Result slots: segment s publishes its sums in slot s % ns, element (row, t)
+// at row * ld + t.  ld is the odd number >= the launch's largest token count
+// per expert, so short launches get more slots (8 at one token, 2 at 16) and
+// the consumers run further ahead of the finish warps.
+struct ResRing {
+    int ns, ld;
+    __device__ __forceinline__ explicit ResRing(const StreamArgs& a)
+        : ns(min(kMaxRes, kResPool / (kUnitRows * (a.max_ntok | 1)))), ld(a.max_ntok | 1) {}
+    __device__ __forceinline__ int slot(long long sidx) const { return static_cast<int>(sidx % ns); }
+    __device__ __forceinline__ uint32_t parity(long long sidx) const { return static_cast<uint32_t>((sidx / ns) & 1); }
+    __device__ __forceinline__ float* at(SmemTail& sm, long long sidx) const {
+        return sm.res + static_cast<size_t>(slot(sidx)) * kUnitRows * ld;
+    }
+};
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
 
 // Position of element k (0..127) of a group in the shared activation layout:
@@ -289,17 +306,16 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int i = lane + 32 * j;
+        // every lane shuffles (the token index is clamped for lanes past the
+        // activation scales), then each loads its own value
+        const int rt = __shfl_sync(0xffffffffu, row, min(i / ng, m.ntok - 1));
         float x = 0.0f;
         if (i < n_as) {
-            const int t = i / ng, gl = i % ng;
-            const int rt = __shfl_sync(0xffffffffu, row, t);   // uniform: t < ntok <= 16 < 32
-            x = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + gl);
+            x = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + i % ng);
         } else if (i < n_as + n_sw) {
             const int q = i - n_as, b = q / ng, gl = q % ng;
             const int nb = m.rb + (b ? L.RB : 0);
             x = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
-        } else {
-            __shfl_sync(0xffffffffu, row, 0);                   // keep the shuffle uniform
         }
         v[j] = x;
     }
@@ -321,8 +337,8 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
 // and (layer) the readiness flag of (expert, row block); down -> y and
 // (layer) the combine of every token whose last expert this was.
-__device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta& m, const float* res, int lane,
-                                             int epoch) {
+__device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta& m, const float* res, int ld,
+                                             int lane, int epoch) {
     const Operand& op = a.op[m.kind];
     if (m.valid && m.kind == kKindGU) {
         // lane owns h columns 4*lane .. 4*lane+3 of this row block; in the
@@ -334,8 +350,8 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int i = 4 * lane + j;
-                const float g = res[i * kAccLd + t];
-                const float u = res[(128 + i) * kAccLd + t];
+                const float g = res[i * ld + t];
+                const float u = res[(128 + i) * ld + t];
                 hv[j] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
             }
             const float4 h4 = make_float4(hv[0], hv[1], hv[2], hv[3]);
@@ -352,7 +368,7 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
     } else if (m.valid) {
         for (int idx = lane; idx < 128 * m.ntok; idx += 32) {
             const int i = idx & 127, t = idx >> 7;
-            op.out[static_cast<size_t>(m.p0 + t) * op.out_ld + m.rb * 128 + i] = res[i * kAccLd + t];
+            op.out[static_cast<size_t>(m.p0 + t) * op.out_ld + m.rb * 128 + i] = res[i * ld + t];
         }
     }
     if (m.kind == kKindGU && a.fused_route) {
@@ -409,12 +425,12 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
     }
 }
 
-// Finish segment number `sidx` (its result slot is sidx & 1), whose
-// result the consumers have published.
+// Finish segment number `sidx`, whose result the consumers have published.
 __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, long long sidx, int lane, int epoch) {
-    const int rs = static_cast<int>(sidx & 1);
-    const SegMeta m = sm.seg[sidx & 3];
-    float* res = sm.res[rs];
+    const ResRing ring(a);
+    const int ld = ring.ld;
+    const SegMeta m = sm.seg[sidx % kSegRing];
+    float* res = ring.at(sm, sidx);
     const int rows = m.kind == kKindGU ? 256 : 128;
     if (!(m.ku0 == 0 && m.ku1 == m.KU)) {
         // split K: publish this CTA's partial, take a ticket, and if this is
@@ -422,85 +438,84 @@ __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, l
         const long long rblk = static_cast<long long>(m.e_local) * m.RB + m.rb;
         const long long c_lo = cta_of_unit(rblk * m.KU, m.T, m.G);
         const long long c_hi = cta_of_unit(rblk * m.KU + m.KU - 1, m.T, m.G);
+        const int n_c = static_cast<int>(c_hi - c_lo + 1);   // CTAs the row block spans
+        const int lg = m.kind == kKindGU ? 8 : 7;             // log2(rows)
         float* part_base = a.partials + static_cast<size_t>(m.li) * a.partial_list_floats;
         const int my_slot = static_cast<int>(2 * m.c + ((m.lo / m.KU) == rblk ? 0 : 1));
         float* mine = part_base + static_cast<size_t>(my_slot) * kMaxTok * rows;
-        for (int idx = lane; idx < rows * m.ntok; idx += 32) {
-            const int row = idx % rows, t = idx / rows;
-            mine[t * rows + row] = res[row * kAccLd + t];
-        }
+        const int nitems = rows * m.ntok;
+        for (int idx = lane; idx < nitems; idx += 32) mine[idx] = res[(idx & (rows - 1)) * ld + (idx >> lg)];
+        // Lane j resolves CTA c_lo + b + j: the slot of its partial of this
+        // row block, null when that CTA holds no unit (all lanes in parallel).
+        auto resolve = [&](int b) -> const float* {
+            const long long cc = c_lo + b + lane;
+            if (cc > c_hi) return nullptr;
+            const long long lo = unit_lo(cc, m.T, m.G);
+            if (lo >= unit_lo(cc + 1, m.T, m.G)) return nullptr;
+            return part_base + static_cast<size_t>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1)) * kMaxTok * rows;
+        };
+        const float* src0 = resolve(0);
+        int n = __popc(__ballot_sync(0xffffffffu, src0 != nullptr));
+        for (int b = 32; b < n_c; b += 32) n += __popc(__ballot_sync(0xffffffffu, resolve(b) != nullptr));
         // The warp barrier orders every lane's partial before lane 0's ticket;
-        // the acq_rel ticket publishes them and, for the last contributor,
+        // the acq_rel ticket publishes them and, for the last contribution,
         // acquires everyone else's.
         __syncwarp();
         int last = 0;
-        if (lane == 0) {
-            int n = 0;
-            for (long long cc = c_lo; cc <= c_hi; ++cc) n += unit_lo(cc, m.T, m.G) < unit_lo(cc + 1, m.T, m.G);
-            last = atom_add_acq_rel(a.tickets[m.li] + rblk, 1) == n - 1;
-        }
+        if (lane == 0) last = atom_add_acq_rel(a.tickets[m.li] + rblk, 1) == n - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
         __syncwarp();   // lane 0's acquire before every lane's loads
         if (last) {
-            // Lane q < kWin resolves the slot of CTA c_lo + q (null when that
-            // CTA holds no unit); the window's partials are loaded together and
-            // summed in CTA order, CTAs past the window (rare) after them.
-            constexpr int kWin = 8, kPer = 2;
-            const float* src = nullptr;
-            {
-                const long long cc = c_lo + lane;
-                if (lane < kWin && cc <= c_hi) {
-                    const long long lo = unit_lo(cc, m.T, m.G);
-                    if (lo < unit_lo(cc + 1, m.T, m.G))
-                        src = part_base + static_cast<size_t>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1)) * kMaxTok * rows;
-                }
-            }
-            const float* srcs[kWin];
-#pragma unroll
-            for (int q = 0; q < kWin; ++q)
-                srcs[q] = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(src), q));
-            const bool many = c_hi - c_lo + 1 > kWin;
-            const int nitems = rows * m.ntok;
+            // kWin contributors' partials are loaded together, then added in
+            // CTA order (absent CTAs add +0).
+            constexpr int kWin = 8, kPer = 4;
             for (int base = 0; base < nitems; base += kPer * 32) {
-                float w[kWin][kPer];
+                float v[kPer];
 #pragma unroll
-                for (int q = 0; q < kWin; ++q)
+                for (int j = 0; j < kPer; ++j) v[j] = 0.0f;
+                for (int b = 0; b < n_c; b += 32) {
+                    const float* sb = b == 0 ? src0 : resolve(b);
+                    const int nw = min(32, n_c - b);
+                    for (int w0 = 0; w0 < nw; w0 += kWin) {
+                        float w[kWin][kPer];
 #pragma unroll
-                    for (int j = 0; j < kPer; ++j) {
-                        const int idx = base + j * 32 + lane;
-                        w[q][j] = (srcs[q] != nullptr && idx < nitems) ? __ldcg(srcs[q] + idx) : 0.0f;
+                        for (int q = 0; q < kWin; ++q) {
+                            const float* sq = reinterpret_cast<const float*>(
+                                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(sb), w0 + q));
+#pragma unroll
+                            for (int j = 0; j < kPer; ++j) {
+                                const int idx = base + j * 32 + lane;
+                                w[q][j] = (sq != nullptr && idx < nitems) ? __ldcg(sq + idx) : 0.0f;
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < kWin; ++q)
+#pragma unroll
+                            for (int j = 0; j < kPer; ++j) v[j] += w[q][j];
                     }
+                }
 #pragma unroll
                 for (int j = 0; j < kPer; ++j) {
                     const int idx = base + j * 32 + lane;
-                    float v = 0.0f;
-#pragma unroll
-                    for (int q = 0; q < kWin; ++q) v += w[q][j];   // CTA order (absent CTAs add +0)
-                    if (many) {
-                        for (long long cc = c_lo + kWin; cc <= c_hi; ++cc) {
-                            const long long lo = unit_lo(cc, m.T, m.G);
-                            if (lo >= unit_lo(cc + 1, m.T, m.G)) continue;
-                            const int slot = static_cast<int>(2 * cc + ((lo / m.KU) == rblk ? 0 : 1));
-                            if (idx < nitems) v += __ldcg(part_base + static_cast<size_t>(slot) * kMaxTok * rows + idx);
-                        }
-                    }
-                    if (idx < nitems) res[(idx % rows) * kAccLd + idx / rows] = v;
+                    if (idx < nitems) res[(idx & (rows - 1)) * ld + (idx >> lg)] = v[j];
                 }
             }
             __syncwarp();
             if (lane == 0) a.tickets[m.li][rblk] = 0;
-            helper_epilogue(a, m, res, lane, epoch);
+            helper_epilogue(a, m, res, ld, lane, epoch);
         }
     } else {
-        helper_epilogue(a, m, res, lane, epoch);
+        helper_epilogue(a, m, res, ld, lane, epoch);
     }
 }
 
 // The prep warp walks the same lists / segments as the producer, cut into
 // chunks, and prepares each chunk (scales, activation rows, descriptor) at
 // most two chunks ahead of the consumers.  Segment metadata goes to
-// seg[segment & 3]: when segment S+4 is written the consumers have started
-// S+3, hence the finish of S+1 ... and of S is done.
+// seg[segment % kSegRing]: when segment S+R is written the consumers have
+// started S+R-2, so they found the slots of S+R-2-ns and S+R-3-ns finished;
+// one of the two has the parity of S, and each finish warp finishes its
+// segments in order, so S is finished once R >= ns + 3.
 __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int lane, int epoch) {
     long long c = 0;         // chunks prepared
     long long sidx = 0;      // segments started
@@ -548,7 +563,7 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 m.slot = ue;
                 m.shared_static = 0;
             }
-            m.valid = m.expert >= 0 && m.expert < a.n_experts && m.p0 >= 0 && m.ntok >= 1 && m.ntok <= kMaxTok &&
+            m.valid = m.expert >= 0 && m.expert < a.n_experts && m.p0 >= 0 && m.ntok >= 1 && m.ntok <= a.max_ntok &&
                       m.p0 + m.ntok <= a.max_pairs;
             if (!m.valid) {
                 if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
@@ -582,7 +597,7 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 const int ub = min(m.ku1, ua + cu);
                 const int cs = static_cast<int>(c & 1);
                 if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
-                if (ua == m.ku0 && lane == 0) sm.seg[sidx & 3] = m;
+                if (ua == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
                 ChunkDesc d;
                 d.kind = m.kind;
                 d.ku0 = ua;
@@ -609,11 +624,13 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
     if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
 }
 
-// Finish warp rs finishes segments rs, rs+2, rs+4, ... (result slot rs) as
-// the consumers publish them, until the consumers pass on the end marker.
-__device__ __forceinline__ void finish_warp(const StreamArgs& a, SmemTail& sm, int rs, int lane, int epoch) {
-    for (long long sidx = rs;; sidx += 2) {
-        mbar_wait_or_abort(&sm.res_full[rs], static_cast<uint32_t>((sidx >> 1) & 1), sm, a.status);
+// Finish warp w finishes segments w, w+2, w+4, ... in order as the
+// consumers publish them, until the consumers pass on the end marker.
+__device__ __forceinline__ void finish_warp(const StreamArgs& a, SmemTail& sm, int w, int lane, int epoch) {
+    const ResRing ring(a);
+    for (long long sidx = w;; sidx += 2) {
+        const int rs = ring.slot(sidx);
+        mbar_wait_or_abort(&sm.res_full[rs], ring.parity(sidx), sm, a.status);
         if (sm.abort_flag || sidx >= static_cast<volatile int&>(sm.n_segments)) break;
         finish_segment(a, sm, sidx, lane, epoch);
         __syncwarp();
@@ -704,22 +721,21 @@ __device__ __forceinline__ float reduce8(float v) {
 }
 
 // One segment, chunk after chunk, for one consumer warp.  Leaves one sum per
-// (row of this warp, token) in result slot rs.  MODE 1/2: up to that many
+// (row of this warp, token) in the result slot res (row stride ld).  MODE 1/2: up to that many
 // tokens with running sums in registers; MODE 0: any count, two tokens at a
 // time, each K group reduced across lanes into the result slot.
 template <int KIND, int MODE>
-__device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
-                                                int cw, int lane, long long& c, long long& it) {
+__device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, float* res,
+                                                int ld, int cw, int lane, long long& c, long long& it) {
     constexpr int MT = MODE == 0 ? 2 : MODE;
     constexpr int PASSES = KIND == kKindGU ? 4 : 2;   // 4-row passes per warp and tile
     // gate_up: warp w covers rows (w%8)*16.. of tile w/8; down: rows w*8.. of both tiles
     const int tile_w = KIND == kKindGU ? (cw >> 3) : 0;
     const int rows_base = KIND == kKindGU ? (cw & 7) * 16 : cw * 8;
     const int acc_row0 = KIND == kKindGU ? tile_w * 128 + rows_base : rows_base;
-    float* res = sm.res[rs];
     const int ntok = sm.chunk[c & 1].ntok;
     if (MODE == 0)
-        for (int i = lane; i < PASSES * 4 * ntok; i += 32) res[(acc_row0 + i / ntok) * kAccLd + i % ntok] = 0.f;
+        for (int i = lane; i < PASSES * 4 * ntok; i += 32) res[(acc_row0 + i / ntok) * ld + i % ntok] = 0.f;
     float acc[PASSES][MT];
 #pragma unroll
     for (int p = 0; p < PASSES; ++p)
@@ -759,7 +775,7 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
                             for (int t = 0; t < 2; ++t) {
                                 const float v = reduce8(part[p][t]);
                                 if ((lane & 7) == 0 && t0 + t < ntok)
-                                    res[row * kAccLd + t0 + t] += v * (act_s[(t0 + t) * d.ng + gl] * swg);
+                                    res[row * ld + t0 + t] += v * (act_s[(t0 + t) * d.ng + gl] * swg);
                             }
                         }
                     }
@@ -780,7 +796,7 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const float v = reduce8(acc[p][t]);
-                if ((lane & 7) == 0 && t < ntok) res[row * kAccLd + t] = v;
+                if ((lane & 7) == 0 && t < ntok) res[row * ld + t] = v;
             }
         }
     }
@@ -789,20 +805,20 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
 // Every mode runs out of line: each gets the whole register budget for its
 // streaming loop, and the consumer's outer state is saved once per segment.
 template <int KIND, int MODE>
-__device__ __noinline__ void consume_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
-                                                  int cw, int lane, long long& c, long long& it) {
-    consume_segment<KIND, MODE>(a, sm, stages, rs, cw, lane, c, it);
+__device__ __noinline__ void consume_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, float* res,
+                                                  int ld, int cw, int lane, long long& c, long long& it) {
+    consume_segment<KIND, MODE>(a, sm, stages, res, ld, cw, lane, c, it);
 }
 
 template <int KIND>
-__device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int rs,
-                                                 int ntok, int cw, int lane, long long& c, long long& it) {
+__device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, float* res,
+                                                 int ld, int ntok, int cw, int lane, long long& c, long long& it) {
     if (ntok <= 1)
-        consume_segment_cold<KIND, 1>(a, sm, stages, rs, cw, lane, c, it);
+        consume_segment_cold<KIND, 1>(a, sm, stages, res, ld, cw, lane, c, it);
     else if (ntok <= 2)
-        consume_segment_cold<KIND, 2>(a, sm, stages, rs, cw, lane, c, it);
+        consume_segment_cold<KIND, 2>(a, sm, stages, res, ld, cw, lane, c, it);
     else
-        consume_segment_cold<KIND, 0>(a, sm, stages, rs, cw, lane, c, it);
+        consume_segment_cold<KIND, 0>(a, sm, stages, res, ld, cw, lane, c, it);
 }
 
 struct ConsumerSync {
@@ -859,6 +875,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.prep_full[s], 1);
             mbar_init(&sm.act_empty[s], kCW);
+        }
+        for (int s = 0; s < kMaxRes; ++s) {
             mbar_init(&sm.res_full[s], kCW);
             mbar_init(&sm.res_empty[s], 1);
         }
@@ -911,29 +929,33 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         consumer_sync();
         if (tid == 0) atomicAdd(a.a_cnt, 1);
     }
+    const ResRing ring(a);
     long long c = 0, it = 0, sidx = 0;
     for (;;) {
-        const int rs = static_cast<int>(sidx & 1);
-        if (sidx >= 2) mbar_wait_or_abort(&sm.res_empty[rs], static_cast<uint32_t>(((sidx >> 1) - 1) & 1), sm, a.status);
+        const int rs = ring.slot(sidx);
+        // the slot's previous segment (sidx - ns) must be finished
+        if (sidx >= ring.ns) mbar_wait_or_abort(&sm.res_empty[rs], ring.parity(sidx) ^ 1u, sm, a.status);
         const int cs = static_cast<int>(c & 1);
         mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
         const int kind = sm.chunk[cs].kind;
         if (kind < 0 || sm.abort_flag) {
-            // pass the end on to both finish warps (slot rs now, the other
-            // slot once its last segment is finished)
+            // pass the end on to both finish warps: as segment sidx (the
+            // warp of its parity waits for it) and as segment sidx + 1 (the
+            // other warp), each in its slot once that slot is free
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.res_full[rs]);
             const long long s2 = sidx + 1;
-            if (s2 >= 2) mbar_wait_or_abort(&sm.res_empty[s2 & 1], static_cast<uint32_t>(((s2 >> 1) - 1) & 1), sm, a.status);
+            if (s2 >= ring.ns) mbar_wait_or_abort(&sm.res_empty[ring.slot(s2)], ring.parity(s2) ^ 1u, sm, a.status);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.res_full[s2 & 1]);
+            if (lane == 0) mbar_arrive(&sm.res_full[ring.slot(s2)]);
             break;
         }
         const int ntok = sm.chunk[cs].ntok;
+        float* res = ring.at(sm, sidx);
         if (kind == kKindGU)
-            consume_dispatch<kKindGU>(a, sm, stages, rs, ntok, cw, lane, c, it);
+            consume_dispatch<kKindGU>(a, sm, stages, res, ring.ld, ntok, cw, lane, c, it);
         else
-            consume_dispatch<kKindDN>(a, sm, stages, rs, ntok, cw, lane, c, it);
+            consume_dispatch<kKindDN>(a, sm, stages, res, ring.ld, ntok, cw, lane, c, it);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.res_full[rs]);
         ++sidx;

@@ -179,7 +179,10 @@ moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k,
 /*   q_x_opt [M, H], s_x_opt [M, H/128]: optional dump of the codes and     */
 /*           scales the fused prologue used, for the tokens of the plan's   */
 /*           last unique expert (the shared expert, which serves them all)  */
-/* H and I multiples of 128, H <= MOEQ_MAX_K.                               */
+/* H and I multiples of 128, H <= MOEQ_MAX_K.  An expert holds at most M    */
+/* pairs (its tokens are distinct); a plan that breaks this, or names an    */
+/* expert or pair out of range, leaves MOEQ_ERR_INVALID_ARG in the          */
+/* workspace status (moeq_read_device_status).                              */
 /* ------------------------------------------------------------------------ */
 moeq_status moeq_expert_gemm_gateup_swiglu(
     const void* x, moeq_dtype x_dtype, int M, int H, int I,
@@ -200,6 +203,9 @@ moeq_status moeq_expert_gemm_gateup_swiglu(
 /*   q_a_opt [max_pairs, K], s_a_opt [max_pairs, K/128]: optional dump of   */
 /*           the fused prologue's codes and scales                          */
 /* A plan for a dense layer is uniq = {0}, offs = {0, M}, n_uniq = 1.       */
+/* An expert holds at most min(max_pairs, MOEQ_MAX_TOKENS) pairs; a plan    */
+/* that breaks this, or names an expert or pair out of range, leaves        */
+/* MOEQ_ERR_INVALID_ARG in the workspace status.                            */
 /* ------------------------------------------------------------------------ */
 moeq_status moeq_expert_gemm_down(
     const void* a, moeq_dtype a_dtype, int K, int N,
