@@ -51,7 +51,7 @@ moeq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOE
 
 // ------------------------------------------------------------------ workspace
 // Header (256 B): status word, epoch, done ticket, route flag.
-constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffRouteFlag = 12, kOffACnt = 16, kHeader = 256;
+constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffACnt = 16, kHeader = 256;
 
 struct StreamWs {
     size_t aq[2], as[2];
@@ -97,7 +97,10 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.h = align_up(l.plan + moeq_route_plan_bytes(M, E, k), 256);
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
     const size_t after = l.y + sizeof(float) * static_cast<size_t>(mp) * H;
-    const int tk[6] = {I / 128, mu * (I / 128), mu * (I / 128), H / 128, mu * (H / 128), mu * (H / 128)};
+    // tickets of the layer's lists: M == 1 uses the first two (whole lists),
+    // M > 1 all six (shared, half A, half B of each kind)
+    const int rbmax = mu * ((H > I ? H : I) / 128);
+    const int tk[6] = {rbmax, rbmax, rbmax, rbmax, rbmax, rbmax};
     const int rows[2] = {M, mp}, ks[2] = {H, I};
     l.s = stream_ws_layout(after, rows, ks, 6, tk, grid, mu * (I / 128), M * (H / 128));
     return l;
@@ -145,7 +148,6 @@ void fill_ws(StreamArgs& a, void* ws, const StreamWs& l, int grid) {
     a.status = reinterpret_cast<int*>(base + kOffStatus);
     a.epoch = reinterpret_cast<int*>(base + kOffEpoch);
     a.done = reinterpret_cast<int*>(base + kOffDone);
-    a.route_flag = reinterpret_cast<int*>(base + kOffRouteFlag);
     a.a_cnt = reinterpret_cast<int*>(base + kOffACnt);
     for (int k = 0; k < 2; ++k) {
         a.op[k].aq = reinterpret_cast<float*>(base + l.aq[k]);
@@ -299,7 +301,6 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     o.RB = I / 128;
     o.a = x;
     o.a_f32 = x_dtype == MOEQ_F32;
-    o.a_row = pair_tok;
     o.rows_a = M;
     o.out = h;
     o.out_ld = I;
@@ -347,7 +348,6 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     o.RB = N / 128;
     o.a = a_in;
     o.a_f32 = a_dtype == MOEQ_F32;
-    o.a_row = nullptr;
     o.rows_a = max_pairs;
     o.out = y;
     o.out_ld = N;
@@ -412,7 +412,6 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     g.RB = I / 128;
     g.a = x;
     g.a_f32 = 0;
-    g.a_row = plan.pair_tok;
     g.rows_a = M;
     g.out = h;
     g.out_ld = I;
@@ -426,16 +425,29 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     d.RB = H / 128;
     d.a = h;
     d.a_f32 = 1;
-    d.a_row = nullptr;
     d.rows_a = mp;
     d.out = y;
     d.out_ld = H;
-    a.n_lists = 6;
-    const int kinds[6] = {kKindGU, kKindGU, kKindGU, kKindDN, kKindDN, kKindDN};
-    const int srcs[6] = {kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB, kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB};
-    for (int i = 0; i < 6; ++i) {
-        a.list_kind[i] = kinds[i];
-        a.list_src[i] = srcs[i];
+    if (M == 1) {
+        // one token: the routed experts' blocks and the shared expert's cost
+        // the same, so each kind is one list dealt out in whole row blocks
+        a.n_lists = 2;
+        a.list_kind[0] = kKindGU;
+        a.list_src[0] = kSrcLayer;
+        a.list_kind[1] = kKindDN;
+        a.list_src[1] = kSrcLayer;
+    } else {
+        // the shared expert serves all M tokens (M times a routed block's
+        // arithmetic): its own lists spread it over every CTA; the routed
+        // experts come in two halves so that down of the first hides the
+        // finish of the second's h
+        a.n_lists = 6;
+        const int kinds[6] = {kKindGU, kKindGU, kKindGU, kKindDN, kKindDN, kKindDN};
+        const int srcs[6] = {kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB, kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB};
+        for (int i = 0; i < 6; ++i) {
+            a.list_kind[i] = kinds[i];
+            a.list_src[i] = srcs[i];
+        }
     }
     a.n_uniq = plan.n_uniq;
     a.uniq = plan.uniq;

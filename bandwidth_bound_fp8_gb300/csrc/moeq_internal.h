@@ -16,10 +16,11 @@ constexpr int kMaxTokens = MOEQ_MAX_TOKENS;
 constexpr int kMaxLists = 6;
 constexpr int kKindGU = 0;  // gate_up: a stage holds the gate tile and the up tile of one K group
 constexpr int kKindDN = 1;  // down: a stage holds two consecutive K tiles of one row block
-constexpr int kSrcShared = 0;     // the layer's shared expert, known before routing
-constexpr int kSrcPlanAll = 1;    // every unique expert of the plan (standalone calls)
-constexpr int kSrcPlanRoutedA = 2; // the first half of the plan's routed experts
-constexpr int kSrcPlanRoutedB = 3; // the second half (down of half A hides the finish of half B's h)
+constexpr int kSrcShared = 0;      // the layer's shared expert alone, known before routing
+constexpr int kSrcPlanAll = 1;     // every unique expert of the caller's plan (standalone calls)
+constexpr int kSrcLayer = 2;       // the layer: its shared expert first, then the plan's routed experts
+constexpr int kSrcPlanRoutedA = 3; // the first half of the plan's routed experts
+constexpr int kSrcPlanRoutedB = 4; // the second half (down of half A hides the finish of half B's h)
 
 // One GEMM operand set.  Weights are tile-major: tile (e, nb, kb) -- the
 // 128 x 128 block of rows nb*128.. and columns kb*128.. of expert e -- is 16
@@ -29,9 +30,8 @@ struct Operand {
     const uint8_t* w;
     const float* sw;      // [E, NB, KB]
     int K, KB, NB, RB;    // RB = output row blocks per expert (I/128 for gate_up, N/128 for down)
-    const void* a;        // activations [rows_a, K], bf16 or fp32
+    const void* a;        // activations [rows_a, K], bf16 or fp32 (gate_up: token rows; down: pair rows)
     int a_f32;
-    const int32_t* a_row; // gate_up: row of `a` used by pair p (pair_tok); nullptr = p
     int rows_a;
     float* out;           // [max_pairs, out_ld]
     int out_ld;
@@ -59,7 +59,7 @@ struct StreamArgs {
     int shared_id, shared_p0, M;
     int max_ntok;             // largest token (pair) count of one expert: 1 .. kMaxTokens
     // layer fusion
-    int fused_route;          // CTA 0 computes the plan, the others wait for route_flag
+    int fused_route;          // every CTA computes the plan into shared memory; CTA 0 writes `plan`
     const float* logits;
     int E_routed, top_k;
     moeq_route_plan plan;     // writable plan (fused route)
@@ -69,7 +69,6 @@ struct StreamArgs {
     int* status;
     int* epoch;
     int* done;
-    int* route_flag;
     int* a_cnt;               // CTAs done with the input quantisation phase (epoch * grid when all are)
     int h_to_dn;              // layer: the gate_up finish also quantises h into op[down].aq/as
     int* tickets[kMaxLists];

@@ -12,13 +12,17 @@
 // Work.  A unit is one stage: for gate_up the gate tile and the up tile of
 // one 128-row block at one 128-wide K group (32 KiB), for down two
 // consecutive K tiles of one 128-row block (32 KiB).  Work comes in lists
-// (for the layer: shared-expert gate_up, routed gate_up, shared down, routed
-// down); every CTA takes a contiguous, equal share of every list.  A share
-// splits into segments (runs of one row block); only its first and last can
-// be partial in K, so each CTA leaves at most two fp32 partials per list; the
-// last CTA to finish a row block (atomic ticket) sums them in CTA order and
-// runs the epilogue, so results do not depend on timing.  A segment splits
-// into chunks whose quantised activations fit one shared-memory slot.
+// (for the layer: gate_up, then down, each over the shared expert first and
+// then the routed experts of the plan).  When the row blocks of a list
+// nearly fill the grid in whole numbers per CTA (one token: 144 gate_up
+// blocks on 152 SMs, 3 down blocks per CTA), each CTA takes whole row blocks
+// and nothing is split.  Otherwise every CTA takes a contiguous, equal share
+// of the list's units (stream-K); a share splits into segments (runs of one
+// row block) of which only the first and last can be partial in K, so each
+// CTA leaves at most two fp32 partials per list; the last CTA to finish a
+// row block (atomic ticket) sums them in CTA order and runs the epilogue, so
+// results do not depend on timing.  A segment splits into chunks whose
+// quantised activations fit one shared-memory slot.
 //
 // Warp roles (640 threads):
 //   warps 0-15  consumers: per stage, each lane widens 16 weight bytes of a
@@ -42,12 +46,13 @@
 // (res_full/res_empty); no role waits on another CTA while the others owe
 // it progress, so the cross-CTA dependencies (plan, h) cannot deadlock.
 //
-// Layer fusion (cooperative launch, all CTAs resident): CTA 0's consumers
-// compute the routing plan while the other CTAs stream the shared expert,
-// which needs no routing; gate_up finishes publish per-(expert, row block)
-// readiness of h (already quantised); the helper waits (bounded) for an
-// expert's h before loading it for down, while the producer already streams
-// down weights;
+// Layer fusion (cooperative launch, all CTAs resident): every CTA computes
+// the routing plan itself into shared memory (a few microseconds, no
+// cross-CTA wait; CTA 0 also writes it out), while CTAs whose first blocks
+// belong to the shared expert already stream them; gate_up finishes publish
+// per-(expert, row block) readiness of h (already quantised); the prep warp
+// waits (bounded) for an expert's h before loading it for down, while the
+// producer already streams down weights;
 // the down finish that completes the last expert of a (token, row block)
 // also writes the combined bf16 output.
 #include "moeq_device.cuh"
@@ -88,20 +93,48 @@ struct SegMeta {       // what the helper needs to finish a segment
     int KU, RB;
 };
 
+// The layer's routing plan, computed by every CTA into shared memory (same
+// members as moeq_route_plan; M <= kMaxTok, top_k <= kRouteMaxK).
+constexpr int kLocalUniq = kMaxTok * kRouteMaxK + 1;
+constexpr int kLocalPairs = kMaxTok * (kRouteMaxK + 1);
+struct LocalPlan {
+    int topk_id[kMaxTok * kRouteMaxK];
+    float topk_w[kMaxTok * kRouteMaxK];
+    int n_uniq;
+    int uniq[kLocalUniq];
+    int offs[kLocalUniq + 1];
+    int pair_tok[kLocalPairs];
+    int pair_of[kLocalPairs];
+};
+
+// Where the roles read the plan: the CTA's LocalPlan (layer) or the caller's
+// plan in global memory (standalone calls).  Generic pointers.
+struct PlanView {
+    const int* n_uniq;
+    const int* uniq;
+    const int* offs;
+    const int* pair_tok;
+    const int* pair_of;
+    const float* topk_w;
+};
+
 struct SmemTail {
     union {
         float act[2][kActSlot];          // decoded activations [tok][group][permuted k]
-        RouteScratch route;              // plan computation (CTA 0, before any activation)
+        RouteScratch route;              // plan computation, before any activation
     };
     float act_s[2][kChunkGroups];        // activation scales [tok][group]
     float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
     float res[kResPool];                 // result slots: one sum per (row, token), see ResRing
     ChunkDesc chunk[2];
     SegMeta seg[kSegRing];               // by segment index % kSegRing (see prep_warp)
+    LocalPlan plan;
+    PlanView pv;
     int n_segments;                      // total, written by the prep warp before its end marker
     int finish_done;                     // finish warps that have ended
     uint64_t full[kStages], empty[kStages];
     uint64_t prep_full[2], act_empty[2], res_full[kMaxRes], res_empty[kMaxRes];
+    uint64_t plan_bar;                   // the LocalPlan is complete (layer)
     int abort_flag;
 };
 
@@ -133,8 +166,10 @@ __device__ __forceinline__ int act_pos(int k) { return (((k & 15) >> 2) * 8 + (k
 
 // ------------------------------------------------------------------ work lists
 struct ListInfo {
-    int kind, src, n_exp, e0, RB, KU;  // experts e0 .. e0+n_exp-1 of the plan (or the static shared one)
-    long long T, G, c;   // units, participating CTAs, this CTA's index among them
+    int kind, src, n_exp, e0, RB, KU;  // experts e0 .. e0+n_exp-1 of the list's source (see list_expert)
+    bool dp;             // whole row blocks: `per` consecutive blocks per CTA
+    int per;
+    long long T, G, c;   // units, CTAs, this CTA's index
     long long lo, hi;    // this CTA's share [lo, hi)
 };
 
@@ -143,34 +178,89 @@ __device__ __forceinline__ long long cta_of_unit(long long u, long long T, long 
     return ((u + 1) * G - 1) / T;
 }
 
-__device__ __forceinline__ bool list_needs_plan(const StreamArgs& a, int li) {
-    return a.list_src[li] != kSrcShared;
+// Row blocks per CTA when whole blocks are dealt out: used when the CTAs
+// that get `per` blocks are at least 90% of the grid (the rest idle in this
+// list; the streaming rate is the memory's, not the SM count's).
+__device__ __forceinline__ int dp_blocks_per_cta(long long n_rb, long long G) {
+    if (n_rb <= 0) return 0;
+    const long long per = (n_rb + G - 1) / G, used = (n_rb + per - 1) / per;
+    return used * 10 >= G * 9 ? static_cast<int>(per) : 0;
 }
 
+// Whether this CTA needs the plan to know its share of list li.  The layer's
+// lists start with the shared expert, which needs none: with whole blocks
+// per CTA, the CTAs whose blocks all belong to it start before the plan.
+__device__ __forceinline__ bool list_needs_plan(const StreamArgs& a, int li) {
+    if (a.list_src[li] == kSrcShared || a.list_src[li] == kSrcPlanAll) return false;
+    if (a.list_src[li] != kSrcLayer) return true;
+    const Operand& op = a.op[a.list_kind[li]];
+    const int per = dp_blocks_per_cta(static_cast<long long>(a.max_uniq) * op.RB, gridDim.x);
+    return !(per > 0 && (static_cast<long long>(blockIdx.x) + 1) * per <= op.RB);
+}
+
+// U: unique experts of the plan (shared included), or -1 while unknown
+// (only where list_needs_plan is false).
 __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U) {
     ListInfo L;
     L.kind = a.list_kind[li];
     L.src = a.list_src[li];
-    const int routed = U > 1 ? U - 1 : 0, half = (routed + 1) / 2;
-    L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
-    L.n_exp = L.src == kSrcShared ? 1
-            : L.src == kSrcPlanAll ? U
-            : L.src == kSrcPlanRoutedA ? half : routed - half;
     const Operand& op = a.op[L.kind];
     L.RB = op.RB;
     L.KU = L.kind == kKindGU ? op.KB : (op.KB + 1) / 2;
+    const int routed = U > 1 ? U - 1 : 0, half = (routed + 1) / 2;
+    L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
+    L.n_exp = L.src == kSrcShared ? 1
+            : (L.src == kSrcLayer || L.src == kSrcPlanAll) ? (U < 0 ? 1 : U)
+            : L.src == kSrcPlanRoutedA ? half : routed - half;
+    L.G = gridDim.x;
+    L.c = blockIdx.x;
     L.T = static_cast<long long>(L.n_exp) * L.RB * L.KU;
-    // While CTA 0 routes, the shared expert's gate_up goes to the other CTAs.
-    const bool skip0 = a.fused_route && L.src == kSrcShared && L.kind == kKindGU && gridDim.x > 1;
-    L.G = gridDim.x - (skip0 ? 1 : 0);
-    L.c = static_cast<long long>(blockIdx.x) - (skip0 ? 1 : 0);
-    if (L.c < 0 || L.T == 0) {
+    // the layer decides on the plan's bound (known before the plan), a
+    // standalone call on its plan's actual expert count
+    const long long n_dec = L.src == kSrcLayer ? a.max_uniq : L.n_exp;
+    L.per = dp_blocks_per_cta(n_dec * L.RB, L.G);
+    L.dp = L.per > 0;
+    if (L.dp) {
+        const long long n_rb = static_cast<long long>(L.n_exp) * L.RB;
+        L.lo = min(L.c * L.per, n_rb) * L.KU;
+        L.hi = min((L.c + 1) * L.per, n_rb) * L.KU;
+    } else if (L.T == 0) {
         L.lo = L.hi = 0;
     } else {
         L.lo = unit_lo(L.c, L.T, L.G);
         L.hi = unit_lo(L.c + 1, L.T, L.G);
     }
     return L;
+}
+
+// Expert e_local of a list.  The layer's shared expert (tokens 0..M-1, its
+// pairs after the routed ones, known before the plan) is a list of its own
+// or the first expert of a kSrcLayer list, followed there by the plan's
+// routed experts; the halves are runs of the plan's routed experts; a
+// standalone call's list is its plan.
+struct ExpertRef {
+    int expert, p0, ntok, slot, shared_static;
+};
+
+__device__ __forceinline__ ExpertRef list_expert(const StreamArgs& a, const PlanView& pv, const ListInfo& L,
+                                                 int e_local) {
+    const int src = L.src;
+    ExpertRef r;
+    if (src == kSrcShared || (src == kSrcLayer && e_local == 0)) {
+        r.expert = a.shared_id;
+        r.p0 = a.shared_p0;
+        r.ntok = a.M;
+        r.slot = a.max_uniq - 1;
+        r.shared_static = 1;
+    } else {
+        const int ue = L.e0 + e_local - (src == kSrcLayer ? 1 : 0);
+        r.expert = pv.uniq[ue];
+        r.p0 = pv.offs[ue];
+        r.ntok = pv.offs[ue + 1] - r.p0;
+        r.slot = ue;
+        r.shared_static = 0;
+    }
+    return r;
 }
 
 __device__ __forceinline__ const uint8_t* tile_ptr(const Operand& op, int e, int nb, int kb) {
@@ -206,16 +296,12 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint8_t* stages, int epoch) {
     const uint64_t pol = l2_evict_first_policy();
     long long issued = 0;
-    int U = 0;
-    bool have_plan = !a.fused_route;
+    int U = -1;
     for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
-        if (list_needs_plan(a, li)) {
-            if (!have_plan) {
-                wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
-                have_plan = true;
-            }
-            U = __ldcg(a.n_uniq);
-            if (U < 0 || U > a.max_uniq) U = 0;  // reported by the helper
+        if (U < 0 && (list_needs_plan(a, li) || a.list_src[li] == kSrcPlanAll)) {
+            if (a.fused_route) mbar_wait_or_abort(&sm.plan_bar, 0, sm, a.status);
+            U = *sm.pv.n_uniq;
+            if (U < 0 || U > a.max_uniq) U = 0;  // reported by the prep warp
         }
         const ListInfo L = list_info(a, li, U);
         const Operand& op = a.op[L.kind];
@@ -227,7 +313,7 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
             const int rb = rem / L.KU, ku = rem - rb * L.KU;
             if (e_local != cur) {
                 cur = e_local;
-                expert = L.src == kSrcShared ? a.shared_id : __ldcg(a.uniq + L.e0 + e_local);
+                expert = list_expert(a, sm.pv, L, e_local).expert;
                 if (expert < 0 || expert >= a.n_experts) expert = 0;
             }
             const int s = static_cast<int>(issued % kStages);
@@ -286,9 +372,9 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     int row = 0;
     if (lane < m.ntok) {
         const int p = m.p0 + lane;
-        // gate_up reads token rows (the shared expert's pairs are tokens 0..M-1
-        // before any plan exists); down reads pair rows.
-        row = op.a_row ? (m.shared_static ? lane : __ldcg(op.a_row + p)) : p;
+        // gate_up reads token rows (the shared expert's pairs are tokens
+        // 0..M-1); down reads pair rows.
+        row = m.kind == kKindGU ? (m.shared_static ? lane : sm.pv.pair_tok[p]) : p;
         if (row < 0 || row >= op.rows_a) {
             record_error(a.status, MOEQ_ERR_INVALID_ARG);
             row = 0;
@@ -337,8 +423,8 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
 // and (layer) the readiness flag of (expert, row block); down -> y and
 // (layer) the combine of every token whose last expert this was.
-__device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta& m, const float* res, int ld,
-                                             int lane, int epoch) {
+__device__ __noinline__ void helper_epilogue(const StreamArgs& a, const PlanView& pv, const SegMeta& m,
+                                             const float* res, int ld, int lane, int epoch) {
     const Operand& op = a.op[m.kind];
     if (m.valid && m.kind == kKindGU) {
         // lane owns h columns 4*lane .. 4*lane+3 of this row block; in the
@@ -380,7 +466,7 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
         __syncwarp();   // y rows of every lane before the (acq_rel) combine tickets
         int tok = -1, last = 0;
         if (lane < m.ntok && m.valid) {
-            tok = m.shared_static ? lane : __ldcg(a.pair_tok + m.p0 + lane);
+            tok = m.shared_static ? lane : pv.pair_tok[m.p0 + lane];
             if (tok >= 0 && tok < a.M) last = atom_add_acq_rel(a.comb + tok * op.RB + m.rb, 1) == a.top_k;
         }
         uint32_t todo = __ballot_sync(0xffffffffu, last);
@@ -389,10 +475,10 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
             const int src = __ffs(todo) - 1;
             todo &= todo - 1;
             const int tk = __shfl_sync(0xffffffffu, tok, src);
-            const int* po = a.pair_of + tk * (a.top_k + 1);
+            const int* po = pv.pair_of + tk * (a.top_k + 1);
             // lane owns columns 4*lane .. 4*lane+3; all slots' rows in flight
             const int n = m.rb * 128 + 4 * lane;
-            const int ps = __ldcg(po + a.top_k);
+            const int ps = po[a.top_k];
             float4 accv = __ldcg(reinterpret_cast<const float4*>(op.out + static_cast<size_t>(ps) * op.out_ld + n));
             for (int j0 = 0; j0 < a.top_k; j0 += 4) {
                 float4 yv[4];
@@ -400,8 +486,8 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const SegMeta&
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (j0 + j < a.top_k) {
-                        const int pj = __ldcg(po + j0 + j);
-                        wv[j] = __ldcg(a.topk_w + tk * a.top_k + j0 + j);
+                        const int pj = po[j0 + j];
+                        wv[j] = pv.topk_w[tk * a.top_k + j0 + j];
                         yv[j] = __ldcg(reinterpret_cast<const float4*>(op.out + static_cast<size_t>(pj) * op.out_ld + n));
                     }
                 }
@@ -502,10 +588,10 @@ __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, l
             }
             __syncwarp();
             if (lane == 0) a.tickets[m.li][rblk] = 0;
-            helper_epilogue(a, m, res, ld, lane, epoch);
+            helper_epilogue(a, sm.pv, m, res, ld, lane, epoch);
         }
     } else {
-        helper_epilogue(a, m, res, ld, lane, epoch);
+        helper_epilogue(a, sm.pv, m, res, ld, lane, epoch);
     }
 }
 
@@ -520,21 +606,18 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
     long long c = 0;         // chunks prepared
     long long sidx = 0;      // segments started
     bool have_input = false;
-    int U = 0;
-    bool have_plan = !a.fused_route;
+    // The plan's scratch shares memory with the activation slots: the layer's
+    // prep warp starts once the CTA's plan is complete.
+    if (a.fused_route) {
+        if (lane == 0) mbar_wait_or_abort(&sm.plan_bar, 0, sm, a.status);
+        __syncwarp();
+    }
+    int U = *sm.pv.n_uniq;
+    if (U < 0 || U > a.max_uniq) {
+        if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
+        U = 0;
+    }
     for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
-        if (list_needs_plan(a, li)) {
-            if (!have_plan) {
-                if (lane == 0) wait_flag(a.route_flag, epoch, a.status, &sm.abort_flag);
-                __syncwarp();
-                have_plan = true;
-            }
-            U = __ldcg(a.n_uniq);
-            if (U < 0 || U > a.max_uniq) {
-                if (lane == 0) record_error(a.status, MOEQ_ERR_INVALID_ARG);
-                U = 0;
-            }
-        }
         const ListInfo L = list_info(a, li, U);
         const Operand& op = a.op[L.kind];
         const int GPU = L.kind == kKindGU ? 1 : 2;
@@ -549,20 +632,12 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
             m.ku0 = rem - m.rb * L.KU;
             const int seg_end_u = min(static_cast<int>(L.hi), u - m.ku0 + L.KU);
             m.ku1 = m.ku0 + (seg_end_u - u);
-            if (L.src == kSrcShared) {
-                m.expert = a.shared_id;
-                m.p0 = a.shared_p0;
-                m.ntok = a.M;
-                m.slot = a.max_uniq - 1;
-                m.shared_static = 1;
-            } else {
-                const int ue = L.e0 + m.e_local;
-                m.expert = __ldcg(a.uniq + ue);
-                m.p0 = __ldcg(a.offs + ue);
-                m.ntok = __ldcg(a.offs + ue + 1) - m.p0;
-                m.slot = ue;
-                m.shared_static = 0;
-            }
+            const ExpertRef er = list_expert(a, sm.pv, L, m.e_local);
+            m.expert = er.expert;
+            m.p0 = er.p0;
+            m.ntok = er.ntok;
+            m.slot = er.slot;
+            m.shared_static = er.shared_static;
             m.valid = m.expert >= 0 && m.expert < a.n_experts && m.p0 >= 0 && m.ntok >= 1 && m.ntok <= a.max_ntok &&
                       m.p0 + m.ntok <= a.max_pairs;
             if (!m.valid) {
@@ -828,14 +903,10 @@ struct ConsumerSync {
 // The kernel's first phase: the inputs given as activations (x for gate_up;
 // for a standalone down call, its input) are live-quantised once, each
 // (row, 128-group) by one consumer warp of one CTA, into the decoded
-// consumer layout that chunk loads copy from.  CTA 0 routes instead when the
-// layer is fused.
+// consumer layout that chunk loads copy from.
 template <bool kGuF32, bool kDnF32>
 __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int lane) {
-    const bool skip0 = a.fused_route && gridDim.x > 1;
-    const long long G = gridDim.x - (skip0 ? 1 : 0);
-    const long long c = static_cast<long long>(blockIdx.x) - (skip0 ? 1 : 0);
-    if (c < 0) return;
+    const long long G = gridDim.x, c = blockIdx.x;
     const long long n0 = a.op[0].quant_input ? static_cast<long long>(a.op[0].rows_a) * a.op[0].KB : 0;
     const long long n1 = a.op[1].quant_input ? static_cast<long long>(a.op[1].rows_a) * a.op[1].KB : 0;
     const long long n = n0 + n1;
@@ -860,6 +931,24 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
     }
 }
 
+// CTA 0 hands its copy of the plan to the caller (the kernel never reads it).
+__device__ __noinline__ void copy_plan_out(const StreamArgs& a, const LocalPlan& lp, int tid) {
+    const int M = a.M, k = a.top_k, U = lp.n_uniq, P = M * (k + 1);
+    for (int i = tid; i < M * k; i += kConsumers) {
+        a.plan.topk_id[i] = lp.topk_id[i];
+        a.plan.topk_w[i] = lp.topk_w[i];
+    }
+    for (int i = tid; i <= U; i += kConsumers) {
+        if (i < U) a.plan.uniq[i] = lp.uniq[i];
+        a.plan.offs[i] = lp.offs[i];
+    }
+    for (int i = tid; i < P; i += kConsumers) {
+        a.plan.pair_tok[i] = lp.pair_tok[i];
+        a.plan.pair_of[i] = lp.pair_of[i];
+    }
+    if (tid == 0) *a.plan.n_uniq = U;
+}
+
 template <bool kGuF32, bool kDnF32>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ StreamArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -880,6 +969,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(&sm.res_full[s], kCW);
             mbar_init(&sm.res_empty[s], 1);
         }
+        mbar_init(&sm.plan_bar, 1);
+        if (a.fused_route) {
+            sm.pv.n_uniq = &sm.plan.n_uniq;
+            sm.pv.uniq = sm.plan.uniq;
+            sm.pv.offs = sm.plan.offs;
+            sm.pv.pair_tok = sm.plan.pair_tok;
+            sm.pv.pair_of = sm.plan.pair_of;
+            sm.pv.topk_w = sm.plan.topk_w;
+        } else {
+            sm.pv.n_uniq = a.n_uniq;
+            sm.pv.uniq = a.uniq;
+            sm.pv.offs = a.offs;
+            sm.pv.pair_tok = a.pair_tok;
+            sm.pv.pair_of = a.pair_of;
+            sm.pv.topk_w = a.topk_w;
+        }
         sm.abort_flag = 0;
         sm.n_segments = 0x7fffffff;
         sm.finish_done = 0;
@@ -893,8 +998,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         return;
     }
     if (warp == kPrepWarp) {
-        // CTA 0's consumers write the routing plan into the activation slots'
-        // memory first; the prep warp waits for the plan before touching them.
         prep_warp(a, sm, lane, epoch);
         return;
     }
@@ -915,19 +1018,25 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp;
-    if (a.fused_route && blockIdx.x == 0) {
-        // CTA 0 has no share of the input quantisation while it routes
-        if (tid == 0) atomicAdd(a.a_cnt, 1);
-        route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, a.plan, sm.route, tid, ConsumerSync{});
-        __threadfence();
+    quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
+    fence_proxy_async();
+    __threadfence();
+    consumer_sync();
+    if (tid == 0) atomicAdd(a.a_cnt, 1);
+    if (a.fused_route) {
+        // every CTA routes for itself (identical, deterministic plans)
+        moeq_route_plan lp;
+        lp.topk_id = sm.plan.topk_id;
+        lp.topk_w = sm.plan.topk_w;
+        lp.n_uniq = &sm.plan.n_uniq;
+        lp.uniq = sm.plan.uniq;
+        lp.offs = sm.plan.offs;
+        lp.pair_tok = sm.plan.pair_tok;
+        lp.pair_of = sm.plan.pair_of;
+        route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, lp, sm.route, tid, ConsumerSync{});
         consumer_sync();
-        if (tid == 0) st_release(a.route_flag, epoch);
-    } else {
-        quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
-        fence_proxy_async();
-        __threadfence();
-        consumer_sync();
-        if (tid == 0) atomicAdd(a.a_cnt, 1);
+        if (blockIdx.x == 0) copy_plan_out(a, sm.plan, tid);
+        if (tid == 0) mbar_arrive(&sm.plan_bar);
     }
     const ResRing ring(a);
     long long c = 0, it = 0, sidx = 0;
