@@ -896,8 +896,9 @@ __device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& 
         consume_segment_cold<KIND, 0>(a, sm, stages, res, ld, cw, lane, c, it);
 }
 
-struct ConsumerSync {
-    __device__ __forceinline__ void operator()() const { consumer_sync(); }
+// the routing half of the consumers (warps 0 .. kCW/2-1)
+struct RouteSync {
+    __device__ __forceinline__ void operator()() const { named_sync(2, kConsumers / 2); }
 };
 
 // The kernel's first phase: the inputs given as activations (x for gate_up;
@@ -905,13 +906,13 @@ struct ConsumerSync {
 // (row, 128-group) by one consumer warp of one CTA, into the decoded
 // consumer layout that chunk loads copy from.
 template <bool kGuF32, bool kDnF32>
-__device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int lane) {
+__device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int nwarps, int lane) {
     const long long G = gridDim.x, c = blockIdx.x;
     const long long n0 = a.op[0].quant_input ? static_cast<long long>(a.op[0].rows_a) * a.op[0].KB : 0;
     const long long n1 = a.op[1].quant_input ? static_cast<long long>(a.op[1].rows_a) * a.op[1].KB : 0;
     const long long n = n0 + n1;
     const long long lo = c * n / G, hi = (c + 1) * n / G;
-    for (long long i = lo + warp; i < hi; i += kCW) {
+    for (long long i = lo + warp; i < hi; i += nwarps) {
         const int k = i < n0 ? 0 : 1;
         const Operand& op = a.op[k];
         const long long j = i < n0 ? i : i - n0;
@@ -934,15 +935,16 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
 // CTA 0 hands its copy of the plan to the caller (the kernel never reads it).
 __device__ __noinline__ void copy_plan_out(const StreamArgs& a, const LocalPlan& lp, int tid) {
     const int M = a.M, k = a.top_k, U = lp.n_uniq, P = M * (k + 1);
-    for (int i = tid; i < M * k; i += kConsumers) {
+    constexpr int kN = kConsumers / 2;
+    for (int i = tid; i < M * k; i += kN) {
         a.plan.topk_id[i] = lp.topk_id[i];
         a.plan.topk_w[i] = lp.topk_w[i];
     }
-    for (int i = tid; i <= U; i += kConsumers) {
+    for (int i = tid; i <= U; i += kN) {
         if (i < U) a.plan.uniq[i] = lp.uniq[i];
         a.plan.offs[i] = lp.offs[i];
     }
-    for (int i = tid; i < P; i += kConsumers) {
+    for (int i = tid; i < P; i += kN) {
         a.plan.pair_tok[i] = lp.pair_tok[i];
         a.plan.pair_of[i] = lp.pair_of[i];
     }
@@ -1018,13 +1020,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp;
-    quantise_inputs<kGuF32, kDnF32>(a, cw, lane);
-    fence_proxy_async();
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) atomicAdd(a.a_cnt, 1);
-    if (a.fused_route) {
-        // every CTA routes for itself (identical, deterministic plans)
+    if (!a.fused_route) {
+        quantise_inputs<kGuF32, kDnF32>(a, cw, kCW, lane);
+        fence_proxy_async();
+        __threadfence();
+        consumer_sync();
+        if (tid == 0) atomicAdd(a.a_cnt, 1);
+    } else if (cw >= kCW / 2) {
+        // half the consumers quantise this CTA's share of the inputs ...
+        quantise_inputs<kGuF32, kDnF32>(a, cw - kCW / 2, kCW / 2, lane);
+        fence_proxy_async();
+        __threadfence();
+        named_sync(3, kConsumers / 2);
+        if (cw == kCW / 2 && lane == 0) atomicAdd(a.a_cnt, 1);
+    } else {
+        // ... while the other half routes: every CTA for itself (identical,
+        // deterministic plans)
         moeq_route_plan lp;
         lp.topk_id = sm.plan.topk_id;
         lp.topk_w = sm.plan.topk_w;
@@ -1033,8 +1044,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         lp.offs = sm.plan.offs;
         lp.pair_tok = sm.plan.pair_tok;
         lp.pair_of = sm.plan.pair_of;
-        route_compute<kConsumers>(a.logits, a.M, a.E_routed, a.top_k, lp, sm.route, tid, ConsumerSync{});
-        consumer_sync();
+        route_compute<kConsumers / 2>(a.logits, a.M, a.E_routed, a.top_k, lp, sm.route, tid, RouteSync{});
+        RouteSync{}();
         if (blockIdx.x == 0) copy_plan_out(a, sm.plan, tid);
         if (tid == 0) mbar_arrive(&sm.plan_bar);
     }
