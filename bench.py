@@ -153,7 +153,7 @@ class ClockSampler:
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("moeq_gemm.cu", "moeq_device.cuh"):
+    for f in ("moeq_stream.cu", "moeq_device.cuh", "moeq_route.cuh", "moeq_internal.h"):
         with open(os.path.join(ROOT, "bandwidth_bound_fp8_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -401,6 +401,37 @@ def reference_arm(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ profiling case
+def profile_case(M: int, reps: int):
+    """A small launch for ncu captures: the layer kernel with 8 routed experts
+    and top-8, so that a one-token launch does exactly the full layer's work
+    (8 routed + the shared expert, ~340 MB) on ~350 MB of weights."""
+    from bandwidth_bound_fp8_gb300 import build as b
+    b.build()
+    from bandwidth_bound_fp8_gb300 import moeq
+    Er = 8
+    gq = torch.empty((Er + 1, 2 * I, H), dtype=torch.uint8, device="cuda")
+    gs = torch.empty((Er + 1, 2 * I // 128, H // 128), dtype=torch.float32, device="cuda")
+    dq = torch.empty((Er + 1, H, I), dtype=torch.uint8, device="cuda")
+    ds = torch.empty((Er + 1, H // 128, I // 128), dtype=torch.float32, device="cuda")
+    for e in range(Er + 1):
+        w = synth.weight_f32(2 * I, H, synth.expert_seed(CFG["seed"], 0, e, 0), device="cuda")
+        moeq.moeq_quant_weight(w[None], gq[e:e + 1], gs[e:e + 1])
+        w = synth.weight_f32(H, I, synth.expert_seed(CFG["seed"], 0, e, 1), device="cuda")
+        moeq.moeq_quant_weight(w[None], dq[e:e + 1], ds[e:e + 1])
+    del w
+    x = synth.activations_bf16(M, H, 3, CFG["n_outlier"], CFG["outlier_scale"], device="cuda")
+    lg = synth.logits_f32(M, Er, 4, device="cuda")
+    out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, Er + 1, TOPK))
+    for _ in range(reps):
+        moeq.moeq_moe_layer(x, lg, H, I, Er, TOPK, gq, gs, dq, ds, out, ws)
+    torch.cuda.synchronize()
+    if moeq.moeq_read_device_status(ws.t, ws.nbytes) != 0:
+        raise RuntimeError("device status word set")
+    print(json.dumps({"profile_case": f"moe_layer_m{M}_h{H}_i{I}_e{Er}_top{TOPK}_shared1", "launches": reps}))
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -414,7 +445,13 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run a few launches of the small ncu case (8 routed experts, top-8) and exit")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.M, args.reps)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     world, rank, local = dist_setup()
@@ -470,7 +507,7 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp8e4m3 x fp8e4m3 -> f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"moe_layer_m{args.M}_h6144_i2048_e256_top8_shared1",
                        "M": args.M, "hidden": H, "intermediate": I, "experts": E, "top_k": TOPK, "shared": 1,
                        "layers_rotated": args.layers, "unique_experts_mean": r["U_mean"],
