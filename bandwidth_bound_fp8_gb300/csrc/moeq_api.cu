@@ -367,6 +367,101 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
 
+// ------------------------------------------------------------------ no-alloc down
+// moeq_expert_gemm_down without a caller workspace, for callers that cannot
+// lend one and cannot allocate on their path: a plain C host issuing one
+// projection with no device buffer of its own to spare, or an engine whose
+// device memory is wholly committed to its own pools, where cudaMalloc (which
+// may synchronise the device) is not allowed in the decode step.  Its scratch
+// is this file's static device array; a launch needs at most
+// kNoAllocScratchBytes of it (header, decoded activations and scales,
+// tickets, split-K partials), larger problems are refused.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of this device's copy of the scratch, looked up once per
+// device (with that device current) and cached.
+static moeq_status noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static std::vector<void*> addr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOEQ_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (static_cast<int>(addr.size()) <= dev) addr.resize(dev + 1, nullptr);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return MOEQ_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return MOEQ_OK;
+}
+
+moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, int K, int N, const uint8_t* w_d,
+                                          const float* s_d, int n_experts, const int32_t* uniq, const int32_t* offs,
+                                          const int32_t* n_uniq_dev, int max_uniq, int max_pairs, float* y,
+                                          uint8_t* q_a_opt, float* s_a_opt, int32_t* device_status_opt,
+                                          void* stream) {
+    if (!a_in || !w_d || !s_d || !uniq || !offs || !n_uniq_dev || !y) return MOEQ_ERR_INVALID_ARG;
+    if (!aligned16(a_in) || !aligned16(w_d) || !aligned16(y) || !aligned4(s_d)) return MOEQ_ERR_INVALID_ARG;
+    if ((q_a_opt == nullptr) != (s_a_opt == nullptr)) return MOEQ_ERR_INVALID_ARG;
+    if (q_a_opt && !aligned16(q_a_opt)) return MOEQ_ERR_INVALID_ARG;
+    if (device_status_opt && !aligned4(device_status_opt)) return MOEQ_ERR_INVALID_ARG;
+    if (a_dtype != MOEQ_BF16 && a_dtype != MOEQ_F32) return MOEQ_ERR_INVALID_ARG;
+    if (n_experts < 1 || max_uniq < 1 || max_pairs < 1) return MOEQ_ERR_INVALID_ARG;
+    if (K <= 0 || N <= 0 || K % 128 || N % 128 || K > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    const DeviceInfo dev = current_device();
+    if (!dev.ok) return MOEQ_ERR_DEVICE;
+    const StreamWs wl = gemm_ws_layout(1, N / 128, K, max_pairs, max_uniq, dev.sms);
+    if (wl.end > kNoAllocScratchBytes) return MOEQ_ERR_WORKSPACE;   // beyond the static maximum
+    void* ws = nullptr;
+    const moeq_status st = noalloc_scratch(&ws);
+    if (st != MOEQ_OK) return st;
+    cudaStream_t cs = as_stream(stream);
+    // The counters (status word, epoch, input-quantisation count, tickets)
+    // must be zero when a launch starts: zero them on the stream first.
+    if (cudaMemsetAsync(ws, 0, wl.partials, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
+    StreamArgs a = {};
+    Operand& o = a.op[kKindDN];
+    o.quant_input = 1;
+    o.w = w_d;
+    o.sw = s_d;
+    o.K = K;
+    o.KB = K / 128;
+    o.NB = N / 128;
+    o.RB = N / 128;
+    o.a = a_in;
+    o.a_f32 = a_dtype == MOEQ_F32;
+    o.rows_a = max_pairs;
+    o.out = y;
+    o.out_ld = N;
+    o.qdump = q_a_opt;
+    o.sdump = s_a_opt;
+    a.n_lists = 1;
+    a.list_kind[0] = kKindDN;
+    a.list_src[0] = kSrcPlanAll;
+    a.n_uniq = n_uniq_dev;
+    a.uniq = uniq;
+    a.offs = offs;
+    a.n_experts = n_experts;
+    a.max_uniq = max_uniq;
+    a.max_pairs = max_pairs;
+    a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
+    fill_ws(a, ws, wl, dev.sms);
+    if (launch_stream(a, dev.sms, true, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
+    if (device_status_opt &&
+        cudaMemcpyAsync(device_status_opt, static_cast<char*>(ws) + kOffStatus, sizeof(int32_t),
+                        cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
+    return MOEQ_OK;
+}
+
 moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k, void* out_bf16,
                          void* stream) {
     if (!y || !plan || !plan->pair_of || !out_bf16 || (top_k > 0 && !plan->topk_w)) return MOEQ_ERR_INVALID_ARG;

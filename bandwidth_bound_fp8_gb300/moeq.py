@@ -34,7 +34,7 @@ EXPORTS = [
     "moeq_route_plan_bytes", "moeq_route_plan_carve", "moeq_workspace_size",
     "moeq_gemm_workspace_size", "moeq_workspace_init", "moeq_read_device_status",
     "moeq_quant_act", "moeq_quant_weight", "moeq_pack_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
-    "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer",
+    "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer", "moeq_expert_gemm_down_noalloc",
 ]
 
 
@@ -83,6 +83,8 @@ def load(path: str = LIB_PATH):
         "moeq_expert_gemm_down": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _i,
                                        _vp, _vp, _vp, _vp, _sz, _vp]),
         "moeq_combine": (_i, [_vp, _i, ctypes.POINTER(moeq_route_plan), _i, _i, _vp, _vp]),
+        "moeq_expert_gemm_down_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _i,
+                                               _vp, _vp, _vp, _vp, _vp]),
         "moeq_moe_layer": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                                 ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _sz, _vp]),
     }
@@ -238,6 +240,15 @@ def moeq_expert_gemm_gateup_swiglu(x, H, I, w_gu, s_gu, n_experts, uniq, offs, p
     _check("moeq_expert_gemm_gateup_swiglu", load().moeq_expert_gemm_gateup_swiglu(
         _p(x), _dtype(x), M, H, I, _p(w_gu), _p(s_gu), n_experts, _p(uniq), _p(offs), _p(pair_tok),
         _p(n_uniq), max_uniq, max_pairs, _p(h), _p(q_x), _p(s_x), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def moeq_expert_gemm_down_noalloc(a, K, N, w_d, s_d, n_experts, uniq, offs, n_uniq, max_uniq, max_pairs, y,
+                                  q_a=None, s_a=None, device_status=None, stream=None) -> None:
+    """moeq_expert_gemm_down on the library's static scratch (no workspace);
+    device_status: optional device int32 tensor that receives the status word."""
+    _check("moeq_expert_gemm_down_noalloc", load().moeq_expert_gemm_down_noalloc(
+        _p(a), _dtype(a), K, N, _p(w_d), _p(s_d), n_experts, _p(uniq), _p(offs), _p(n_uniq),
+        max_uniq, max_pairs, _p(y), _p(q_a), _p(s_a), _p(device_status), _stream(stream)))
 
 
 def moeq_expert_gemm_down(a, K, N, w_d, s_d, n_experts, uniq, offs, n_uniq, max_uniq, max_pairs, y,

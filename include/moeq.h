@@ -215,6 +215,41 @@ moeq_status moeq_expert_gemm_down(
     float* y, uint8_t* q_a_opt, float* s_a_opt,
     void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* moeq_expert_gemm_down_noalloc -- moeq_expert_gemm_down with no caller     */
+/* workspace.  The pages have no counterpart: it exists for callers that     */
+/* cannot lend a workspace and cannot allocate on their path (a plain C      */
+/* host issuing one projection with no device buffer to spare, or an engine  */
+/* whose device memory is committed to its own pools and whose decode step   */
+/* may not call cudaMalloc, which can synchronise the device).               */
+/*   Arguments, layouts and results are those of moeq_expert_gemm_down,      */
+/*   without ws / ws_bytes.                                                  */
+/*   device_status_opt: NULL, or a caller-owned device int32 that receives   */
+/*   the launch's device status word (0 = MOEQ_OK, else a moeq_status) on    */
+/*   the stream after the launch.                                            */
+/* Scratch: the library's own static device array of 8 MiB per device       */
+/*   (decoded activations and scales, split-K tickets and partials).  A      */
+/*   problem whose scratch would exceed it returns MOEQ_ERR_WORKSPACE and    */
+/*   launches nothing; the dense projection (K 2048, N 4096, one token)      */
+/*   needs ~5 MiB, and K = 32768 with 16 rows ~7 MiB.  Its counters must be  */
+/*   zero when a launch starts: every call zeroes them on `stream` itself    */
+/*   (cudaMemsetAsync), so nothing has to be zero beforehand.                */
+/* Set-up: the first call on each device looks up that device's scratch      */
+/*   address (cudaGetSymbolAddress, with the device current) and caches it;  */
+/*   make that first call before any stream capture.                         */
+/* Concurrency: every call on a device uses the same scratch, so calls that  */
+/*   may overlap in time (other streams, other host threads) race: issue     */
+/*   them on one stream.                                                     */
+/* Allocates no device or host memory.                                       */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_expert_gemm_down_noalloc(
+    const void* a, moeq_dtype a_dtype, int K, int N,
+    const uint8_t* w_d, const float* s_d, int n_experts,
+    const int32_t* uniq, const int32_t* offs, const int32_t* n_uniq_dev,
+    int max_uniq, int max_pairs,
+    float* y, uint8_t* q_a_opt, float* s_a_opt,
+    int32_t* device_status_opt, void* stream);
+
 /* moeq_combine -- out[m] = bf16_RNE(y[pair_of[m][top_k]] +                 */
 /*   sum_{j < top_k} topk_w[m][j] * y[pair_of[m][j]]), fp32, in slot order. */
 /* y [max_pairs, N] fp32, out [M, N] bf16.  top_k may be 0 (dense layer:    */
