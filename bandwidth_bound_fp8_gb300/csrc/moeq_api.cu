@@ -317,6 +317,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = M;   // the pairs of one expert are distinct tokens
+    a.mma = a.max_ntok >= kMmaMinTokens;
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
@@ -363,6 +364,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
+    a.mma = a.max_ntok >= kMmaMinTokens;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
@@ -531,6 +533,18 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
         a.list_src[0] = kSrcLayer;
         a.list_kind[1] = kKindDN;
         a.list_src[1] = kSrcLayer;
+    } else if (M >= kMmaMinTokens) {
+        // tcgen05 path: a stage costs the same for 1 or 16 tokens.  The shared
+        // expert's gate_up, spread over every CTA, needs no plan and covers
+        // the routing; its down (whose h is ready first) covers the finish of
+        // the routed experts' h
+        a.n_lists = 4;
+        const int kinds[4] = {kKindGU, kKindGU, kKindDN, kKindDN};
+        const int srcs[4] = {kSrcShared, kSrcPlanRouted, kSrcShared, kSrcPlanRouted};
+        for (int i = 0; i < 4; ++i) {
+            a.list_kind[i] = kinds[i];
+            a.list_src[i] = srcs[i];
+        }
     } else {
         // the shared expert serves all M tokens (M times a routed block's
         // arithmetic): its own lists spread it over every CTA; the routed
@@ -554,6 +568,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.max_uniq = mu;
     a.max_pairs = mp;
     a.max_ntok = M;
+    a.mma = M >= kMmaMinTokens;
     a.shared_id = E_routed;
     a.shared_p0 = M * top_k;
     a.M = M;

@@ -13,6 +13,7 @@
 namespace moeq {
 
 constexpr int kMaxTokens = MOEQ_MAX_TOKENS;
+constexpr int kMmaMinTokens = 8;  // launches with this many tokens per expert (or more) run the tcgen05 path
 constexpr int kMaxLists = 6;
 constexpr int kKindGU = 0;  // gate_up: a stage holds the gate tile and the up tile of one K group
 constexpr int kKindDN = 1;  // down: a stage holds two consecutive K tiles of one row block
@@ -21,6 +22,7 @@ constexpr int kSrcPlanAll = 1;     // every unique expert of the caller's plan (
 constexpr int kSrcLayer = 2;       // the layer: its shared expert first, then the plan's routed experts
 constexpr int kSrcPlanRoutedA = 3; // the first half of the plan's routed experts
 constexpr int kSrcPlanRoutedB = 4; // the second half (down of half A hides the finish of half B's h)
+constexpr int kSrcPlanRouted = 5;  // all of the plan's routed experts
 
 // One GEMM operand set.  Weights are tile-major: tile (e, nb, kb) -- the
 // 128 x 128 block of rows nb*128.. and columns kb*128.. of expert e -- is 16
@@ -71,6 +73,7 @@ struct StreamArgs {
     int* done;
     int* a_cnt;               // CTAs done with the input quantisation phase (epoch * grid when all are)
     int h_to_dn;              // layer: the gate_up finish also quantises h into op[down].aq/as
+    int mma;                  // 1: tcgen05 path (activation codes kept as E4M3 bytes in aq)
     int* tickets[kMaxLists];
     float* partials;          // per list: 2 * grid slots of kMaxTokens * 256 floats
     size_t partial_list_floats;

@@ -73,6 +73,17 @@ constexpr int kStageBytes = 2 * kTile;
 constexpr int kStages = 4;
 constexpr int kActSlot = 6144;           // decoded activation floats per slot
 constexpr int kChunkGroups = kActSlot / kGroup;
+// tcgen05 path: a slot holds the chunk's activation codes as the MMA's B
+// operand, 2 KiB per K group (16 token rows x 128 bytes, 128-byte swizzle).
+constexpr int kMmaN = 16;                              // tokens per MMA (rows of B)
+constexpr int kMmaGroupBytes = kMmaN * 128;
+constexpr int kMmaChunkGroups = kActSlot * 4 / kMmaGroupBytes;   // 12
+constexpr int kActScales = kMaxTok * kMmaChunkGroups;           // >= kChunkGroups
+constexpr int kTmemBufs = 4;                           // accumulator sets (one per stage in flight)
+constexpr int kTmemCols = kTmemBufs * 2 * kMmaN;       // 128 columns: 2 tiles x 16 tokens per set
+constexpr int kEpiSets = 2;                            // epilogue warp sets, alternating stages
+constexpr int kEpiWarps = 4 * kEpiSets;                // warps 0-7: warp w reads TMEM lanes 32*(w%4) ..
+constexpr int kMmaWarp = kEpiWarps;
 constexpr int kUnitRows = 256;           // rows of a gate_up unit (gate + up); down units use 128
 constexpr int kResPool = 2 * kUnitRows * (kMaxTok + 1);   // result slot floats (two at 16 tokens)
 constexpr int kMaxRes = 8;               // result slots at most
@@ -123,7 +134,7 @@ struct SmemTail {
         float act[2][kActSlot];          // decoded activations [tok][group][permuted k]
         RouteScratch route;              // plan computation, before any activation
     };
-    float act_s[2][kChunkGroups];        // activation scales [tok][group]
+    float act_s[2][kActScales];          // activation scales: [tok][group]; tcgen05 path [group][16 tok]
     float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
     float res[kResPool];                 // result slots: one sum per (row, token), see ResRing
     ChunkDesc chunk[2];
@@ -135,6 +146,8 @@ struct SmemTail {
     uint64_t full[kStages], empty[kStages];
     uint64_t prep_full[2], act_empty[2], res_full[kMaxRes], res_empty[kMaxRes];
     uint64_t plan_bar;                   // the LocalPlan is complete (layer)
+    uint64_t mma_done[kTmemBufs], tmem_empty[kTmemBufs];   // tcgen05 path
+    uint32_t tmem_base;
     int abort_flag;
 };
 
@@ -211,6 +224,7 @@ __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U
     L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
     L.n_exp = L.src == kSrcShared ? 1
             : (L.src == kSrcLayer || L.src == kSrcPlanAll) ? (U < 0 ? 1 : U)
+            : L.src == kSrcPlanRouted ? routed
             : L.src == kSrcPlanRoutedA ? half : routed - half;
     L.G = gridDim.x;
     L.c = blockIdx.x;
@@ -382,42 +396,72 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     }
     const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
     fence_proxy_async();
-    if (lane < m.ntok)
+    if (a.mma) {
+        // B operand: token t's codes of group gl at row t of that group's
+        // 16 x 128-byte block, chunk c at c ^ (t % 8); 16-byte async copies
+        const uint8_t* codes = reinterpret_cast<const uint8_t*>(op.aq);
+        uint8_t* slot = reinterpret_cast<uint8_t*>(sm.act[cs]);
+        const int total = ng * m.ntok * 8;
+        for (int base = 0; base < total; base += 32) {
+            const int i = base + lane, c = i & 7, tg = i >> 3;
+            const int t = min(tg % m.ntok, m.ntok - 1), gl = tg / m.ntok;
+            const int rt = __shfl_sync(0xffffffffu, row, t);
+            if (i < total)
+                cp_async16(slot + gl * kMmaGroupBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((c ^ (t & 7)) << 4),
+                           codes + static_cast<size_t>(rt) * op.K + (g0 + gl) * kGroup + c * 16);
+        }
+    } else if (lane < m.ntok) {
         bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
                   &sm.prep_full[cs], l2_evict_first_policy());
-    // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all loads first
-    const int n_as = m.ntok * ng, n_sw = ng * (m.kind == kKindGU ? 2 : 1);
-    constexpr int kPer = (kChunkGroups * 3 + 31) / 32;   // <= 48 + 96 values over 32 lanes
+    }
+    // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all
+    // loads first; only as many 32-wide passes as there are values
+    const int n_as = m.ntok * ng, n_all = n_as + ng * (m.kind == kKindGU ? 2 : 1);
+    const float* sw0 = op.sw + (static_cast<size_t>(m.expert) * op.NB + m.rb) * op.KB + g0;
+    const size_t sw_up = static_cast<size_t>(L.RB) * op.KB;   // the up tile's row block
+    constexpr int kPer = (kActScales + 2 * kChunkGroups + 31) / 32;
     float v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
+        if (32 * j >= n_all) break;                  // uniform
         const int i = lane + 32 * j;
-        // every lane shuffles (the token index is clamped for lanes past the
-        // activation scales), then each loads its own value
-        const int rt = __shfl_sync(0xffffffffu, row, min(i / ng, m.ntok - 1));
+        int rt = 0;
+        if (32 * j < n_as) rt = __shfl_sync(0xffffffffu, row, min(i / ng, m.ntok - 1));   // uniform
         float x = 0.0f;
         if (i < n_as) {
             x = __ldcg(op.as + static_cast<size_t>(rt) * op.KB + g0 + i % ng);
-        } else if (i < n_as + n_sw) {
-            const int q = i - n_as, b = q / ng, gl = q % ng;
-            const int nb = m.rb + (b ? L.RB : 0);
-            x = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + g0 + gl);
+        } else if (i < n_all) {
+            const int q = i - n_as, b = q >= ng;
+            x = __ldg(sw0 + (b ? sw_up : 0) + (q - b * ng));
         }
         v[j] = x;
     }
+    if (a.mma) {
+        // token-minor, padded with zeros to kMmaN tokens
+        for (int i = lane; i < ng * kMmaN; i += 32) sm.act_s[cs][i] = 0.0f;
+        __syncwarp();
+    }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
+        if (32 * j >= n_all) break;
         const int i = lane + 32 * j;
         if (i < n_as) {
-            sm.act_s[cs][i] = v[j];
-        } else if (i < n_as + n_sw) {
-            const int q = i - n_as;
-            sm.sw[cs][q / ng][q % ng] = v[j];
+            sm.act_s[cs][a.mma ? (i % ng) * kMmaN + i / ng : i] = v[j];
+        } else if (i < n_all) {
+            const int q = i - n_as, b = q >= ng;
+            sm.sw[cs][b][q - b * ng] = v[j];
         }
     }
     if (lane == 0) sm.chunk[cs] = d;
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
+    if (a.mma) {
+        cp_async_wait_all();
+        fence_proxy_async();   // the MMA reads the codes through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
+    } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
+    }
 }
 
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
@@ -446,8 +490,11 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const PlanView
             if (a.h_to_dn) {
                 float sc;
                 float4 dec;
-                quant_group_warp(h4, &sc, &dec);
-                *reinterpret_cast<float4*>(dn.aq + (p * dn.KB + m.rb) * kGroup + act_pos(4 * lane)) = dec;
+                const uint32_t hc = quant_group_warp(h4, &sc, &dec);
+                if (a.mma)
+                    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(dn.aq) + p * dn.K + m.rb * kGroup + 4 * lane) = hc;
+                else
+                    *reinterpret_cast<float4*>(dn.aq + (p * dn.KB + m.rb) * kGroup + act_pos(4 * lane)) = dec;
                 if (lane == 0) dn.as[p * dn.KB + m.rb] = sc;
             }
         }
@@ -667,7 +714,8 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 __syncwarp();
                 fence_proxy_async();
             }
-            const int cu = max(1, (kActSlot / (kGroup * m.ntok)) / GPU);  // units per chunk
+            const int cu = a.mma ? kMmaChunkGroups / GPU                       // units per chunk
+                                 : max(1, (kActSlot / (kGroup * m.ntok)) / GPU);
             for (int ua = m.ku0; ua < m.ku1; ua += cu) {
                 const int ub = min(m.ku1, ua + cu);
                 const int cs = static_cast<int>(c & 1);
@@ -896,6 +944,183 @@ __device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& 
         consume_segment_cold<KIND, 0>(a, sm, stages, res, ld, cw, lane, c, it);
 }
 
+// ------------------------------------------------------------------ tcgen05 path
+// Swap-AB: the 128 weight rows of a tile are the MMA's M, the (up to 16)
+// tokens of the segment its N, K = 128 per tile in four K = 32 steps.  Each
+// stage's tiles accumulate into their own TMEM columns (a fresh sum per
+// 128-wide K group), so the per-group scales are applied in fp32 by the
+// epilogue warps, as the CUDA-core path does.  One lane issues the MMAs; its
+// commits free the weight stage and hand the accumulators to the epilogue.
+__device__ __noinline__ void mma_issue_loop(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int lane) {
+    constexpr uint32_t kIdesc = umma_idesc_e4m3(128, kMmaN);
+    const uint32_t tmem = sm.tmem_base, stage0 = smem_u32(stages);
+    long long c = 0, it = 0, last = -1;
+    bool ok = true;
+    while (ok) {
+        const int cs = static_cast<int>(c & 1);
+        if (!mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status)) break;
+        const ChunkDesc d = sm.chunk[cs];
+        if (d.kind < 0 || sm.abort_flag) break;
+        const uint32_t bslot = smem_u32(sm.act[cs]);
+        for (int ku = d.ku0; ku < d.ku1; ++ku, ++it) {
+            const int s = static_cast<int>(it % kStages), b = static_cast<int>(it % kTmemBufs);
+            ok = mbar_wait_or_abort(&sm.full[s], static_cast<uint32_t>((it / kStages) & 1), sm, a.status);
+            if (ok && it >= kTmemBufs)
+                ok = mbar_wait_or_abort(&sm.tmem_empty[b], static_cast<uint32_t>(((it / kTmemBufs) - 1) & 1), sm,
+                                        a.status);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const int ntile = d.kind == kKindGU ? 2 : min(2, a.op[kKindDN].KB - 2 * ku);
+                for (int tt = 0; tt < ntile; ++tt) {
+                    const int gl = (d.kind == kKindGU ? ku : 2 * ku + tt) - d.g0;
+                    const uint32_t aaddr = stage0 + static_cast<uint32_t>(s * kStageBytes + tt * kTile);
+                    const uint32_t baddr = bslot + static_cast<uint32_t>(gl * kMmaGroupBytes);
+                    const uint32_t dcol = tmem + static_cast<uint32_t>((b * 2 + tt) * kMmaN);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_f8(dcol, umma_desc_sw128(aaddr + 32 * k), umma_desc_sw128(baddr + 32 * k), kIdesc, k);
+                }
+                umma_commit(&sm.mma_done[b]);
+                umma_commit(&sm.empty[s]);
+            }
+            __syncwarp();
+            last = it;
+        }
+        ++c;
+    }
+    // every MMA issued must have completed before TMEM is freed (bounded)
+    if (last >= 0) {
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(&sm.mma_done[last % kTmemBufs], static_cast<uint32_t>((last / kTmemBufs) & 1)) &&
+               global_timer_ns() - t0 < 100ull * 1000ull * 1000ull) {
+        }
+    }
+}
+
+// One stage for the epilogue: each tile's NT token columns of this thread's
+// TMEM lane, scaled by s_a[t][g] * s_w and added to the running sums.
+template <int NT>
+__device__ __forceinline__ void mma_epi_stage(const SmemTail& sm, uint32_t tcol, int cs, const ChunkDesc& d, int ku,
+                                              int kb_dn, float (&acc0)[kMmaN], float (&acc1)[kMmaN]) {
+    const int ntile = d.kind == kKindGU ? 2 : min(2, kb_dn - 2 * ku);
+    for (int tt = 0; tt < ntile; ++tt) {
+        float v[NT];
+        tmem_ld<NT>(tcol + static_cast<uint32_t>(tt * kMmaN), v);
+        const int gl = (d.kind == kKindGU ? ku : 2 * ku + tt) - d.g0;
+        const float swg = sm.sw[cs][d.kind == kKindGU ? tt : 0][gl];
+        const float4* s4 = reinterpret_cast<const float4*>(&sm.act_s[cs][gl * kMmaN]);
+        const bool up = d.kind == kKindGU && tt == 1;
+#pragma unroll
+        for (int q = 0; q < NT / 4; ++q) {
+            const float4 sa = s4[q];
+            const float sc[4] = {sa.x * swg, sa.y * swg, sa.z * swg, sa.w * swg};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * q + u;
+                if (up)
+                    acc1[t] = fmaf(v[t], sc[u], acc1[t]);
+                else
+                    acc0[t] = fmaf(v[t], sc[u], acc0[t]);
+            }
+        }
+    }
+}
+
+// The epilogue warps: set e (warps 4e .. 4e+3) takes the stages with
+// it % 2 == e; warp w owns TMEM lanes 32*(w%4) .. +31 = rows of each tile.
+// At a segment's end set 1 stores its sums in the result slot and set 0 adds
+// its own (a fixed order) and publishes the slot like the CUDA-core consumers.
+template <int NT>
+__device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, int set, uint32_t tlane, int kind,
+                                             long long& c, long long& it, float (&acc0)[kMmaN],
+                                             float (&acc1)[kMmaN]) {
+    const int kb_dn = a.op[kKindDN].KB;
+    const int lane = threadIdx.x & 31;
+    for (bool first = true;; first = false) {
+        const int cs = static_cast<int>(c & 1);
+        if (!first) mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
+        const ChunkDesc d = sm.chunk[cs];
+        for (int ku = d.ku0; ku < d.ku1 && !sm.abort_flag; ++ku, ++it) {
+            if ((it & 1) != set) continue;
+            const int b = static_cast<int>(it % kTmemBufs);
+            if (!mbar_wait_or_abort(&sm.mma_done[b], static_cast<uint32_t>((it / kTmemBufs) & 1), sm, a.status))
+                break;
+            tc_fence_after();
+            mma_epi_stage<NT>(sm, tlane + static_cast<uint32_t>(b * 2 * kMmaN), cs, d, ku, kb_dn, acc0, acc1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tmem_empty[b]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.act_empty[cs]);
+        ++c;
+        if (d.seg_end || sm.abort_flag) break;
+    }
+    (void)kind;
+}
+
+__device__ __noinline__ void mma_epilogue_loop(const StreamArgs& a, SmemTail& sm, int warp, int lane) {
+    const ResRing ring(a);
+    const int set = warp / 4, quad = warp % 4;
+    const uint32_t tlane = sm.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const int r = quad * 32 + lane;
+    long long c = 0, it = 0, sidx = 0;
+    for (;;) {
+        const int rs = ring.slot(sidx);
+        if (sidx >= ring.ns) mbar_wait_or_abort(&sm.res_empty[rs], ring.parity(sidx) ^ 1u, sm, a.status);
+        const int cs0 = static_cast<int>(c & 1);
+        mbar_wait_or_abort(&sm.prep_full[cs0], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
+        const int kind = sm.chunk[cs0].kind;
+        if (kind < 0 || sm.abort_flag) {
+            if (set == 0) {
+                // pass the end on to both finish warps (see the CUDA-core consumers)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+                const long long s2 = sidx + 1;
+                if (s2 >= ring.ns)
+                    mbar_wait_or_abort(&sm.res_empty[ring.slot(s2)], ring.parity(s2) ^ 1u, sm, a.status);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.res_full[ring.slot(s2)]);
+            }
+            break;
+        }
+        const int ntok = sm.chunk[cs0].ntok;
+        float acc0[kMmaN], acc1[kMmaN];   // gate (or down) and up sums per token
+#pragma unroll
+        for (int t = 0; t < kMmaN; ++t) acc0[t] = acc1[t] = 0.0f;
+        if (ntok <= 4)
+            mma_epi_segment<4>(a, sm, set, tlane, kind, c, it, acc0, acc1);
+        else if (ntok <= 8)
+            mma_epi_segment<8>(a, sm, set, tlane, kind, c, it, acc0, acc1);
+        else
+            mma_epi_segment<16>(a, sm, set, tlane, kind, c, it, acc0, acc1);
+        float* res = ring.at(sm, sidx);
+        if (set == 1) {
+#pragma unroll
+            for (int t = 0; t < kMmaN; ++t) {
+                if (t < ntok) {
+                    res[r * ring.ld + t] = acc0[t];
+                    if (kind == kKindGU) res[(128 + r) * ring.ld + t] = acc1[t];
+                }
+            }
+        }
+        named_sync(5, kEpiWarps * 32);
+        if (set == 0) {
+#pragma unroll
+            for (int t = 0; t < kMmaN; ++t) {
+                if (t < ntok) {
+                    res[r * ring.ld + t] += acc0[t];
+                    if (kind == kKindGU) res[(128 + r) * ring.ld + t] += acc1[t];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+        }
+        ++sidx;
+    }
+}
+
 // the routing half of the consumers (warps 0 .. kCW/2-1)
 struct RouteSync {
     __device__ __forceinline__ void operator()() const { named_sync(2, kConsumers / 2); }
@@ -923,7 +1148,11 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
         float sc;
         float4 dec;
         const uint32_t codes = quant_group_warp(v, &sc, &dec);
-        *reinterpret_cast<float4*>(op.aq + (static_cast<size_t>(row) * op.KB + g) * kGroup + act_pos(lane * 4)) = dec;
+        if (a.mma)
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(op.aq) + static_cast<size_t>(row) * op.K + g * kGroup +
+                                         lane * 4) = codes;
+        else
+            *reinterpret_cast<float4*>(op.aq + (static_cast<size_t>(row) * op.KB + g) * kGroup + act_pos(lane * 4)) = dec;
         if (lane == 0) op.as[static_cast<size_t>(row) * op.KB + g] = sc;
         if (op.qdump) {
             *reinterpret_cast<uint32_t*>(op.qdump + static_cast<size_t>(row) * op.K + g * kGroup + lane * 4) = codes;
@@ -959,17 +1188,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
+        // the tcgen05 path frees a stage by one MMA commit and has four
+        // epilogue warps in place of the sixteen consumer warps
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kCW);
+            mbar_init(&sm.empty[s], a.mma ? 1 : kCW);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.prep_full[s], 1);
-            mbar_init(&sm.act_empty[s], kCW);
+            mbar_init(&sm.act_empty[s], a.mma ? kEpiWarps : kCW);
         }
         for (int s = 0; s < kMaxRes; ++s) {
-            mbar_init(&sm.res_full[s], kCW);
+            mbar_init(&sm.res_full[s], a.mma ? 4 : kCW);   // tcgen05 path: epilogue set 0 publishes
             mbar_init(&sm.res_empty[s], 1);
+        }
+        for (int b = 0; b < kTmemBufs; ++b) {
+            mbar_init(&sm.mma_done[b], 1);
+            mbar_init(&sm.tmem_empty[b], 4);   // the four warps of the set that owns the buffer
         }
         mbar_init(&sm.plan_bar, 1);
         if (a.fused_route) {
@@ -991,6 +1226,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         sm.n_segments = 0x7fffffff;
         sm.finish_done = 0;
         fence_mbar_init();
+    }
+    if (a.mma && warp == kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tc_fence_before();
     }
     const int epoch = ld_relaxed(a.epoch) + 1;
     __syncthreads();
@@ -1048,6 +1287,26 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         RouteSync{}();
         if (blockIdx.x == 0) copy_plan_out(a, sm.plan, tid);
         if (tid == 0) mbar_arrive(&sm.plan_bar);
+    }
+    if (a.mma) {
+        // tcgen05 path: warps 0-7 read the accumulators, warp 8 issues the
+        // MMAs and owns the TMEM allocation; the other consumer warps are done
+        if (cw < kEpiWarps) {
+            tc_fence_after();
+            mma_epilogue_loop(a, sm, cw, lane);
+            tc_fence_before();
+        } else if (cw == kMmaWarp) {
+            tc_fence_after();
+            mma_issue_loop(a, sm, stages, lane);
+        }
+        if (cw <= kMmaWarp) {
+            named_sync(4, (kEpiWarps + 1) * 32);
+            if (cw == kMmaWarp) {
+                tc_fence_after();
+                tmem_dealloc(sm.tmem_base, kTmemCols);
+            }
+        }
+        return;
     }
     const ResRing ring(a);
     long long c = 0, it = 0, sidx = 0;
