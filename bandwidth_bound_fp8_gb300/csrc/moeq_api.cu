@@ -525,26 +525,16 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     d.rows_a = mp;
     d.out = y;
     d.out_ld = H;
-    if (M == 1) {
-        // one token: the routed experts' blocks and the shared expert's cost
-        // the same, so each kind is one list dealt out in whole row blocks
+    if (M == 1 || M >= kMmaMinTokens) {
+        // one token, or the tcgen05 path (where a stage costs the same for 1
+        // or 16 tokens): the routed experts' blocks and the shared expert's
+        // cost the same, so each kind is one list, dealt out in whole row
+        // blocks where they nearly fill the grid
         a.n_lists = 2;
         a.list_kind[0] = kKindGU;
         a.list_src[0] = kSrcLayer;
         a.list_kind[1] = kKindDN;
         a.list_src[1] = kSrcLayer;
-    } else if (M >= kMmaMinTokens) {
-        // tcgen05 path: a stage costs the same for 1 or 16 tokens.  The shared
-        // expert's gate_up, spread over every CTA, needs no plan and covers
-        // the routing; its down (whose h is ready first) covers the finish of
-        // the routed experts' h
-        a.n_lists = 4;
-        const int kinds[4] = {kKindGU, kKindGU, kKindDN, kKindDN};
-        const int srcs[4] = {kSrcShared, kSrcPlanRouted, kSrcShared, kSrcPlanRouted};
-        for (int i = 0; i < 4; ++i) {
-            a.list_kind[i] = kinds[i];
-            a.list_src[i] = srcs[i];
-        }
     } else {
         // the shared expert serves all M tokens (M times a routed block's
         // arithmetic): its own lists spread it over every CTA; the routed

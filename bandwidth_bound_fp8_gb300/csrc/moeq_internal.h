@@ -22,7 +22,6 @@ constexpr int kSrcPlanAll = 1;     // every unique expert of the caller's plan (
 constexpr int kSrcLayer = 2;       // the layer: its shared expert first, then the plan's routed experts
 constexpr int kSrcPlanRoutedA = 3; // the first half of the plan's routed experts
 constexpr int kSrcPlanRoutedB = 4; // the second half (down of half A hides the finish of half B's h)
-constexpr int kSrcPlanRouted = 5;  // all of the plan's routed experts
 
 // One GEMM operand set.  Weights are tile-major: tile (e, nb, kb) -- the
 // 128 x 128 block of rows nb*128.. and columns kb*128.. of expert e -- is 16

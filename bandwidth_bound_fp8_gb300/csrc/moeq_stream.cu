@@ -98,7 +98,7 @@ struct ChunkDesc {
 };
 
 struct SegMeta {       // what the helper needs to finish a segment
-    int kind, li, e_local, rb, ku0, ku1;
+    int kind, li, e_local, rb, j, ku0, ku1;   // j: the row block's position in the list
     int expert, p0, ntok, slot, shared_static, valid;
     long long T, G, c, lo;
     int KU, RB;
@@ -201,11 +201,12 @@ __device__ __forceinline__ int dp_blocks_per_cta(long long n_rb, long long G) {
 }
 
 // Whether this CTA needs the plan to know its share of list li.  The layer's
-// lists start with the shared expert, which needs none: with whole blocks
-// per CTA, the CTAs whose blocks all belong to it start before the plan.
+// lists start with the shared expert, which needs none: for one token (where
+// the plan's expert count is known in advance) with whole blocks per CTA, the
+// CTAs whose blocks all belong to it start before the plan.
 __device__ __forceinline__ bool list_needs_plan(const StreamArgs& a, int li) {
     if (a.list_src[li] == kSrcShared || a.list_src[li] == kSrcPlanAll) return false;
-    if (a.list_src[li] != kSrcLayer) return true;
+    if (a.list_src[li] != kSrcLayer || a.M > 1) return true;
     const Operand& op = a.op[a.list_kind[li]];
     const int per = dp_blocks_per_cta(static_cast<long long>(a.max_uniq) * op.RB, gridDim.x);
     return !(per > 0 && (static_cast<long long>(blockIdx.x) + 1) * per <= op.RB);
@@ -224,14 +225,13 @@ __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U
     L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
     L.n_exp = L.src == kSrcShared ? 1
             : (L.src == kSrcLayer || L.src == kSrcPlanAll) ? (U < 0 ? 1 : U)
-            : L.src == kSrcPlanRouted ? routed
             : L.src == kSrcPlanRoutedA ? half : routed - half;
     L.G = gridDim.x;
     L.c = blockIdx.x;
     L.T = static_cast<long long>(L.n_exp) * L.RB * L.KU;
-    // the layer decides on the plan's bound (known before the plan), a
-    // standalone call on its plan's actual expert count
-    const long long n_dec = L.src == kSrcLayer ? a.max_uniq : L.n_exp;
+    // one-token layers decide on the plan's bound (their expert count, known
+    // before the plan), everything else on the plan's actual expert count
+    const long long n_dec = (L.src == kSrcLayer && a.M == 1) ? a.max_uniq : L.n_exp;
     L.per = dp_blocks_per_cta(n_dec * L.RB, L.G);
     L.dp = L.per > 0;
     if (L.dp) {
@@ -277,6 +277,30 @@ __device__ __forceinline__ ExpertRef list_expert(const StreamArgs& a, const Plan
     return r;
 }
 
+// The (expert, row block) at row-block position j of a list.  Lists of a
+// multi-token layer spread the shared expert's row blocks evenly among the
+// routed ones (block k at position floor(k * n / RB) of n): its blocks carry
+// every token, so no CTA gets more than its share of them.  Otherwise
+// positions run expert by expert.
+__device__ __forceinline__ void list_rb(const StreamArgs& a, const ListInfo& L, int j, int& e_local, int& rb) {
+    if (L.src == kSrcLayer && a.M > 1 && L.n_exp > 1) {
+        const long long n = static_cast<long long>(L.n_exp) * L.RB, R = L.RB;
+        const int before = static_cast<int>((j * R + n - 1) / n);          // shared blocks at positions < j
+        const int upto = static_cast<int>(((j + 1) * R + n - 1) / n);      // ... at positions <= j
+        if (upto > before) {
+            e_local = 0;
+            rb = before;
+        } else {
+            const int q = j - before;
+            e_local = 1 + q / L.RB;
+            rb = q % L.RB;
+        }
+    } else {
+        e_local = j / L.RB;
+        rb = j % L.RB;
+    }
+}
+
 __device__ __forceinline__ const uint8_t* tile_ptr(const Operand& op, int e, int nb, int kb) {
     return op.w + ((static_cast<size_t>(e) * op.NB + nb) * op.KB + kb) * kTile;
 }
@@ -319,12 +343,11 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
         }
         const ListInfo L = list_info(a, li, U);
         const Operand& op = a.op[L.kind];
-        const int upe = L.RB * L.KU;
         int cur = -1, expert = 0;
         for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi); ++u) {
-            const int e_local = u / upe;
-            const int rem = u - e_local * upe;
-            const int rb = rem / L.KU, ku = rem - rb * L.KU;
+            const int jb = u / L.KU, ku = u - jb * L.KU;
+            int e_local, rb;
+            list_rb(a, L, jb, e_local, rb);
             if (e_local != cur) {
                 cur = e_local;
                 expert = list_expert(a, sm.pv, L, e_local).expert;
@@ -568,7 +591,7 @@ __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail& sm, l
     if (!(m.ku0 == 0 && m.ku1 == m.KU)) {
         // split K: publish this CTA's partial, take a ticket, and if this is
         // the last contribution sum all of them in CTA order.
-        const long long rblk = static_cast<long long>(m.e_local) * m.RB + m.rb;
+        const long long rblk = m.j;   // the row block's position: its units are rblk*KU ..
         const long long c_lo = cta_of_unit(rblk * m.KU, m.T, m.G);
         const long long c_hi = cta_of_unit(rblk * m.KU + m.KU - 1, m.T, m.G);
         const int n_c = static_cast<int>(c_hi - c_lo + 1);   // CTAs the row block spans
@@ -668,15 +691,13 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
         const ListInfo L = list_info(a, li, U);
         const Operand& op = a.op[L.kind];
         const int GPU = L.kind == kKindGU ? 1 : 2;
-        const int upe = L.RB * L.KU;
         for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi) && !sm.abort_flag;) {
             SegMeta m;
             m.kind = L.kind;
             m.li = li;
-            m.e_local = u / upe;
-            const int rem = u - m.e_local * upe;
-            m.rb = rem / L.KU;
-            m.ku0 = rem - m.rb * L.KU;
+            m.j = u / L.KU;
+            m.ku0 = u - m.j * L.KU;
+            list_rb(a, L, m.j, m.e_local, m.rb);
             const int seg_end_u = min(static_cast<int>(L.hi), u - m.ku0 + L.KU);
             m.ku1 = m.ku0 + (seg_end_u - u);
             const ExpertRef er = list_expert(a, sm.pv, L, m.e_local);
@@ -929,8 +950,11 @@ __device__ __forceinline__ void consume_segment(const StreamArgs& a, SmemTail& s
 // streaming loop, and the consumer's outer state is saved once per segment.
 template <int KIND, int MODE>
 __device__ __noinline__ void consume_segment_cold(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, float* res,
-                                                  int ld, int cw, int lane, long long& c, long long& it) {
+                                                  int ld, int cw, int lane, long long& c_io, long long& it_io) {
+    long long c = c_io, it = it_io;   // in registers for the streaming loop
     consume_segment<KIND, MODE>(a, sm, stages, res, ld, cw, lane, c, it);
+    c_io = c;
+    it_io = it;
 }
 
 template <int KIND>
@@ -1031,12 +1055,17 @@ __device__ __forceinline__ void mma_epi_stage(const SmemTail& sm, uint32_t tcol,
 // it % 2 == e; warp w owns TMEM lanes 32*(w%4) .. +31 = rows of each tile.
 // At a segment's end set 1 stores its sums in the result slot and set 0 adds
 // its own (a fixed order) and publishes the slot like the CUDA-core consumers.
+// One segment, with its running sums in registers (NT token columns).
 template <int NT>
-__device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, int set, uint32_t tlane, int kind,
-                                             long long& c, long long& it, float (&acc0)[kMmaN],
-                                             float (&acc1)[kMmaN]) {
+__device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, int set, uint32_t tlane, int r, int kind,
+                                             int ntok, float* res, int ld, int rs, long long& c_io,
+                                             long long& it_io) {
     const int kb_dn = a.op[kKindDN].KB;
     const int lane = threadIdx.x & 31;
+    long long c = c_io, it = it_io;
+    float acc0[kMmaN], acc1[kMmaN];   // gate (or down) and up sums per token (NT used)
+#pragma unroll
+    for (int t = 0; t < kMmaN; ++t) acc0[t] = acc1[t] = 0.0f;
     for (bool first = true;; first = false) {
         const int cs = static_cast<int>(c & 1);
         if (!first) mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
@@ -1057,7 +1086,29 @@ __device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, 
         ++c;
         if (d.seg_end || sm.abort_flag) break;
     }
-    (void)kind;
+    c_io = c;
+    it_io = it;
+    if (set == 1) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < ntok) {
+                res[r * ld + t] = acc0[t];
+                if (kind == kKindGU) res[(128 + r) * ld + t] = acc1[t];
+            }
+        }
+    }
+    named_sync(5, kEpiWarps * 32);
+    if (set == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < ntok) {
+                res[r * ld + t] += acc0[t];
+                if (kind == kKindGU) res[(128 + r) * ld + t] += acc1[t];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.res_full[rs]);
+    }
 }
 
 __device__ __noinline__ void mma_epilogue_loop(const StreamArgs& a, SmemTail& sm, int warp, int lane) {
@@ -1086,37 +1137,13 @@ __device__ __noinline__ void mma_epilogue_loop(const StreamArgs& a, SmemTail& sm
             break;
         }
         const int ntok = sm.chunk[cs0].ntok;
-        float acc0[kMmaN], acc1[kMmaN];   // gate (or down) and up sums per token
-#pragma unroll
-        for (int t = 0; t < kMmaN; ++t) acc0[t] = acc1[t] = 0.0f;
-        if (ntok <= 4)
-            mma_epi_segment<4>(a, sm, set, tlane, kind, c, it, acc0, acc1);
-        else if (ntok <= 8)
-            mma_epi_segment<8>(a, sm, set, tlane, kind, c, it, acc0, acc1);
-        else
-            mma_epi_segment<16>(a, sm, set, tlane, kind, c, it, acc0, acc1);
         float* res = ring.at(sm, sidx);
-        if (set == 1) {
-#pragma unroll
-            for (int t = 0; t < kMmaN; ++t) {
-                if (t < ntok) {
-                    res[r * ring.ld + t] = acc0[t];
-                    if (kind == kKindGU) res[(128 + r) * ring.ld + t] = acc1[t];
-                }
-            }
-        }
-        named_sync(5, kEpiWarps * 32);
-        if (set == 0) {
-#pragma unroll
-            for (int t = 0; t < kMmaN; ++t) {
-                if (t < ntok) {
-                    res[r * ring.ld + t] += acc0[t];
-                    if (kind == kKindGU) res[(128 + r) * ring.ld + t] += acc1[t];
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.res_full[rs]);
-        }
+        if (ntok <= 4)
+            mma_epi_segment<4>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
+        else if (ntok <= 8)
+            mma_epi_segment<8>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
+        else
+            mma_epi_segment<16>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
         ++sidx;
     }
 }
