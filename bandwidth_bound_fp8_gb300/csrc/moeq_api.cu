@@ -67,8 +67,10 @@ StreamWs stream_ws_layout(size_t base, const int* aq_rows, const int* aq_k, int 
     StreamWs l;
     size_t off = align_up(base, 256);
     for (int k = 0; k < 2; ++k) {
+        // decoded fp32 codes (CUDA-core path) or 8 swizzle phases of the
+        // E4M3 codes (tcgen05 path): 8 bytes per element covers both
         l.aq[k] = off;
-        off = align_up(off + sizeof(float) * static_cast<size_t>(aq_rows[k]) * aq_k[k], 256);
+        off = align_up(off + 8 * static_cast<size_t>(aq_rows[k]) * aq_k[k], 256);
         l.as[k] = off;
         off = align_up(off + sizeof(float) * static_cast<size_t>(aq_rows[k]) * (aq_k[k] / 128), 256);
     }

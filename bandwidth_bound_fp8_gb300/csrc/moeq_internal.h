@@ -38,7 +38,9 @@ struct Operand {
     int out_ld;
     uint8_t* qdump;       // optional [rows_a, K]
     float* sdump;         // optional [rows_a, K/128]
-    float* aq;            // workspace: decoded activation codes [rows_a, K] in the consumer layout
+    float* aq;            // workspace: decoded activation codes [rows_a, K] in the consumer layout, or
+                          // (tcgen05 path) E4M3 codes [8][rows_a, K]: phase p holds each 128-byte
+                          // group with its 16-byte chunk c at chunk c ^ p
     float* as;            // workspace: activation scales [rows_a, K/128]
     int quant_input;      // 1: the kernel's first phase quantises `a` into aq/as
 };

@@ -177,6 +177,15 @@ __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(
 // eight lanes of a row hit eight consecutive 16-byte chunks.
 __device__ __forceinline__ int act_pos(int k) { return (((k & 15) >> 2) * 8 + (k >> 4)) * 4 + (k & 3); }
 
+// tcgen05 path: lane l's four codes (bytes 4l .. 4l+3 of a 128-byte group)
+// into all 8 swizzle phases of that group: phase p at chunk (l/4) ^ p.
+__device__ __forceinline__ void store_code_phases(uint8_t* group0, size_t phase_stride, int lane, uint32_t codes) {
+    const int c = lane >> 2, off = (lane & 3) * 4;
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+        *reinterpret_cast<uint32_t*>(group0 + p * phase_stride + ((c ^ p) << 4) + off) = codes;
+}
+
 // ------------------------------------------------------------------ work lists
 struct ListInfo {
     int kind, src, n_exp, e0, RB, KU;  // experts e0 .. e0+n_exp-1 of the list's source (see list_expert)
@@ -403,8 +412,10 @@ __device__ __forceinline__ bool wait_count(const int* cnt, int want, int* status
 // (decoded, consumer-layout) activation rows of groups [g0, g0+ng), their
 // scales, the weight scales and the descriptor.  Every load is issued before
 // any is waited for; prep_full[cs] completes when the copied bytes land.
-__device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& op, SmemTail& sm, int cs,
-                                           const SegMeta& m, const ListInfo& L, const ChunkDesc& d, int lane) {
+__device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& op, SmemTail& sm, long long c,
+                                           long long sidx, const SegMeta& m, const ListInfo& L, const ChunkDesc& d,
+                                           int lane) {
+    const int cs = static_cast<int>(c & 1);
     const int g0 = d.g0, ng = d.ng;
     int row = 0;
     if (lane < m.ntok) {
@@ -416,26 +427,6 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
             record_error(a.status, MOEQ_ERR_INVALID_ARG);
             row = 0;
         }
-    }
-    const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
-    fence_proxy_async();
-    if (a.mma) {
-        // B operand: token t's codes of group gl at row t of that group's
-        // 16 x 128-byte block, chunk c at c ^ (t % 8); 16-byte async copies
-        const uint8_t* codes = reinterpret_cast<const uint8_t*>(op.aq);
-        uint8_t* slot = reinterpret_cast<uint8_t*>(sm.act[cs]);
-        const int total = ng * m.ntok * 8;
-        for (int base = 0; base < total; base += 32) {
-            const int i = base + lane, c = i & 7, tg = i >> 3;
-            const int t = min(tg % m.ntok, m.ntok - 1), gl = tg / m.ntok;
-            const int rt = __shfl_sync(0xffffffffu, row, t);
-            if (i < total)
-                cp_async16(slot + gl * kMmaGroupBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((c ^ (t & 7)) << 4),
-                           codes + static_cast<size_t>(rt) * op.K + (g0 + gl) * kGroup + c * 16);
-        }
-    } else if (lane < m.ntok) {
-        bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
-                  &sm.prep_full[cs], l2_evict_first_policy());
     }
     // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all
     // loads first; only as many 32-wide passes as there are values
@@ -459,6 +450,33 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
         }
         v[j] = x;
     }
+    // The slot is free once the consumers are done with chunk c - 2: the
+    // scale loads above are already in flight while this waits.
+    if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
+    if (d.ku0 == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
+    const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
+    fence_proxy_async();
+    if (a.mma) {
+        // B operand: token t's codes of group gl become row t of that group's
+        // 16 x 128-byte block, whose 128-byte swizzle puts chunk c at c ^ (t % 8):
+        // one bulk copy per (token, group) from the code phase t % 8
+        const uint8_t* codes = reinterpret_cast<const uint8_t*>(op.aq);
+        const size_t phase_stride = static_cast<size_t>(op.rows_a) * op.K;
+        uint8_t* slot = reinterpret_cast<uint8_t*>(sm.act[cs]);
+        const int total = ng * m.ntok;
+        for (int base = 0; base < total; base += 32) {
+            const int i = base + lane;
+            const int t = i % m.ntok, gl = i / m.ntok;
+            const int rt = __shfl_sync(0xffffffffu, row, t);
+            if (i < total)
+                bulk_load(slot + gl * kMmaGroupBytes + (t >> 3) * 1024 + (t & 7) * 128,
+                          codes + (t & 7) * phase_stride + static_cast<size_t>(rt) * op.K + (g0 + gl) * kGroup, 128,
+                          &sm.prep_full[cs], l2_evict_first_policy());
+        }
+    } else if (lane < m.ntok) {
+        bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
+                  &sm.prep_full[cs], l2_evict_first_policy());
+    }
     if (a.mma) {
         // token-minor, padded with zeros to kMmaN tokens
         for (int i = lane; i < ng * kMmaN; i += 32) sm.act_s[cs][i] = 0.0f;
@@ -476,15 +494,10 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
         }
     }
     if (lane == 0) sm.chunk[cs] = d;
-    if (a.mma) {
-        cp_async_wait_all();
-        fence_proxy_async();   // the MMA reads the codes through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.prep_full[cs]);
-    } else {
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&sm.prep_full[cs], bytes * static_cast<uint32_t>(m.ntok));
-    }
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive_expect_tx(&sm.prep_full[cs], a.mma ? static_cast<uint32_t>(ng * m.ntok) * 128u
+                                                       : bytes * static_cast<uint32_t>(m.ntok));
 }
 
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
@@ -515,7 +528,8 @@ __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const PlanView
                 float4 dec;
                 const uint32_t hc = quant_group_warp(h4, &sc, &dec);
                 if (a.mma)
-                    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(dn.aq) + p * dn.K + m.rb * kGroup + 4 * lane) = hc;
+                    store_code_phases(reinterpret_cast<uint8_t*>(dn.aq) + p * dn.K + m.rb * kGroup,
+                                      static_cast<size_t>(dn.rows_a) * dn.K, lane, hc);
                 else
                     *reinterpret_cast<float4*>(dn.aq + (p * dn.KB + m.rb) * kGroup + act_pos(4 * lane)) = dec;
                 if (lane == 0) dn.as[p * dn.KB + m.rb] = sc;
@@ -735,13 +749,13 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 __syncwarp();
                 fence_proxy_async();
             }
-            const int cu = a.mma ? kMmaChunkGroups / GPU                       // units per chunk
-                                 : max(1, (kActSlot / (kGroup * m.ntok)) / GPU);
+            // units per chunk: as many as a slot holds, evened out over the
+            // row block's chunks (so no chunk is a short remainder)
+            const int cu_max = a.mma ? kMmaChunkGroups / GPU : max(1, (kActSlot / (kGroup * m.ntok)) / GPU);
+            const int n_chunks = (L.KU + cu_max - 1) / cu_max;
+            const int cu = (L.KU + n_chunks - 1) / n_chunks;
             for (int ua = m.ku0; ua < m.ku1; ua += cu) {
                 const int ub = min(m.ku1, ua + cu);
-                const int cs = static_cast<int>(c & 1);
-                if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
-                if (ua == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
                 ChunkDesc d;
                 d.kind = m.kind;
                 d.ku0 = ua;
@@ -750,7 +764,7 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 d.ng = min(op.KB, ub * GPU) - d.g0;
                 d.ntok = m.ntok;
                 d.seg_end = ub == m.ku1;
-                prep_chunk(a, op, sm, cs, m, L, d, lane);   // ends with the prep_full arrival
+                prep_chunk(a, op, sm, c, sidx, m, L, d, lane);   // ends with the prep_full arrival
                 ++c;
             }
             ++sidx;
@@ -1023,30 +1037,58 @@ __device__ __noinline__ void mma_issue_loop(const StreamArgs& a, SmemTail& sm, c
 }
 
 // One stage for the epilogue: each tile's NT token columns of this thread's
-// TMEM lane, scaled by s_a[t][g] * s_w and added to the running sums.
-template <int NT>
+// TMEM lane, scaled by s_a[t][g] * s_w and added to the running sums.  Both
+// tiles' loads (and their scales) are issued before the one wait.
+template <int NT, int NA>
+__device__ __forceinline__ void epi_fma(float (&acc)[NA], const uint32_t (&r)[NT], const float4* sa, float sw) {
+#pragma unroll
+    for (int q = 0; q < NT / 4; ++q) {
+        const float4 x = sa[q];
+        acc[4 * q] = fmaf(__uint_as_float(r[4 * q]), x.x * sw, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(__uint_as_float(r[4 * q + 1]), x.y * sw, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(__uint_as_float(r[4 * q + 2]), x.z * sw, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(__uint_as_float(r[4 * q + 3]), x.w * sw, acc[4 * q + 3]);
+    }
+}
+
+// One stage for the epilogue: each tile's NT token columns of this thread's
+// TMEM lane, scaled by s_a[t][g] * s_w and added to the running sums (gate_up:
+// the gate and up tiles to acc0 and acc1; down: both K groups to acc0).  Up
+// to 8 columns both tiles' loads are issued before one wait; with 16 the two
+// tiles' registers do not fit beside the sums, so they go one after the other.
+template <int NT, int KIND, int NA>
 __device__ __forceinline__ void mma_epi_stage(const SmemTail& sm, uint32_t tcol, int cs, const ChunkDesc& d, int ku,
-                                              int kb_dn, float (&acc0)[kMmaN], float (&acc1)[kMmaN]) {
-    const int ntile = d.kind == kKindGU ? 2 : min(2, kb_dn - 2 * ku);
-    for (int tt = 0; tt < ntile; ++tt) {
-        float v[NT];
-        tmem_ld<NT>(tcol + static_cast<uint32_t>(tt * kMmaN), v);
-        const int gl = (d.kind == kKindGU ? ku : 2 * ku + tt) - d.g0;
-        const float swg = sm.sw[cs][d.kind == kKindGU ? tt : 0][gl];
-        const float4* s4 = reinterpret_cast<const float4*>(&sm.act_s[cs][gl * kMmaN]);
-        const bool up = d.kind == kKindGU && tt == 1;
-#pragma unroll
-        for (int q = 0; q < NT / 4; ++q) {
-            const float4 sa = s4[q];
-            const float sc[4] = {sa.x * swg, sa.y * swg, sa.z * swg, sa.w * swg};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * q + u;
-                if (up)
-                    acc1[t] = fmaf(v[t], sc[u], acc1[t]);
-                else
-                    acc0[t] = fmaf(v[t], sc[u], acc0[t]);
-            }
+                                              int kb_dn, float (&acc0)[kMmaN], float (&acc1)[NA]) {
+    constexpr bool gu = KIND == kKindGU;
+    const bool two = gu || 2 * ku + 1 < kb_dn;
+    const int gl0 = (gu ? ku : 2 * ku) - d.g0, gl1 = gu ? gl0 : gl0 + 1;
+    const float sw0 = sm.sw[cs][0][gl0], sw1 = sm.sw[cs][gu ? 1 : 0][gl1];
+    const float4* a0 = reinterpret_cast<const float4*>(&sm.act_s[cs][gl0 * kMmaN]);
+    const float4* a1 = reinterpret_cast<const float4*>(&sm.act_s[cs][gl1 * kMmaN]);
+    if constexpr (NT <= 8) {
+        uint32_t r0[NT], r1[NT];
+        tmem_ld_nowait<NT>(tcol, r0);
+        if (two) tmem_ld_nowait<NT>(tcol + static_cast<uint32_t>(kMmaN), r1);
+        tmem_wait_ld();
+        epi_fma<NT>(acc0, r0, a0, sw0);
+        if (two) {
+            if constexpr (gu)
+                epi_fma<NT>(acc1, r1, a1, sw1);
+            else
+                epi_fma<NT>(acc0, r1, a1, sw1);
+        }
+    } else {
+        uint32_t r[NT];
+        tmem_ld_nowait<NT>(tcol, r);
+        tmem_wait_ld();
+        epi_fma<NT>(acc0, r, a0, sw0);
+        if (two) {
+            tmem_ld_nowait<NT>(tcol + static_cast<uint32_t>(kMmaN), r);
+            tmem_wait_ld();
+            if constexpr (gu)
+                epi_fma<NT>(acc1, r, a1, sw1);
+            else
+                epi_fma<NT>(acc0, r, a1, sw1);
         }
     }
 }
@@ -1056,16 +1098,19 @@ __device__ __forceinline__ void mma_epi_stage(const SmemTail& sm, uint32_t tcol,
 // At a segment's end set 1 stores its sums in the result slot and set 0 adds
 // its own (a fixed order) and publishes the slot like the CUDA-core consumers.
 // One segment, with its running sums in registers (NT token columns).
-template <int NT>
-__device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, int set, uint32_t tlane, int r, int kind,
+template <int NT, int KIND>
+__device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, int set, uint32_t tlane, int r,
                                              int ntok, float* res, int ld, int rs, long long& c_io,
                                              long long& it_io) {
+    constexpr int NA = KIND == kKindGU ? kMmaN : 1;   // up-tile sums: gate_up only
     const int kb_dn = a.op[kKindDN].KB;
     const int lane = threadIdx.x & 31;
     long long c = c_io, it = it_io;
-    float acc0[kMmaN], acc1[kMmaN];   // gate (or down) and up sums per token (NT used)
+    float acc0[kMmaN], acc1[NA];   // gate (or down) and up sums per token (NT used)
 #pragma unroll
-    for (int t = 0; t < kMmaN; ++t) acc0[t] = acc1[t] = 0.0f;
+    for (int t = 0; t < kMmaN; ++t) acc0[t] = 0.0f;
+#pragma unroll
+    for (int t = 0; t < NA; ++t) acc1[t] = 0.0f;
     for (bool first = true;; first = false) {
         const int cs = static_cast<int>(c & 1);
         if (!first) mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
@@ -1076,7 +1121,7 @@ __device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, 
             if (!mbar_wait_or_abort(&sm.mma_done[b], static_cast<uint32_t>((it / kTmemBufs) & 1), sm, a.status))
                 break;
             tc_fence_after();
-            mma_epi_stage<NT>(sm, tlane + static_cast<uint32_t>(b * 2 * kMmaN), cs, d, ku, kb_dn, acc0, acc1);
+            mma_epi_stage<NT, KIND, NA>(sm, tlane + static_cast<uint32_t>(b * 2 * kMmaN), cs, d, ku, kb_dn, acc0, acc1);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.tmem_empty[b]);
@@ -1093,7 +1138,7 @@ __device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, 
         for (int t = 0; t < NT; ++t) {
             if (t < ntok) {
                 res[r * ld + t] = acc0[t];
-                if (kind == kKindGU) res[(128 + r) * ld + t] = acc1[t];
+                if constexpr (KIND == kKindGU) res[(128 + r) * ld + t] = acc1[t];
             }
         }
     }
@@ -1103,7 +1148,7 @@ __device__ __noinline__ void mma_epi_segment(const StreamArgs& a, SmemTail& sm, 
         for (int t = 0; t < NT; ++t) {
             if (t < ntok) {
                 res[r * ld + t] += acc0[t];
-                if (kind == kKindGU) res[(128 + r) * ld + t] += acc1[t];
+                if constexpr (KIND == kKindGU) res[(128 + r) * ld + t] += acc1[t];
             }
         }
         __syncwarp();
@@ -1138,12 +1183,21 @@ __device__ __noinline__ void mma_epilogue_loop(const StreamArgs& a, SmemTail& sm
         }
         const int ntok = sm.chunk[cs0].ntok;
         float* res = ring.at(sm, sidx);
-        if (ntok <= 4)
-            mma_epi_segment<4>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
-        else if (ntok <= 8)
-            mma_epi_segment<8>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
-        else
-            mma_epi_segment<16>(a, sm, set, tlane, r, kind, ntok, res, ring.ld, rs, c, it);
+        if (kind == kKindGU) {
+            if (ntok <= 4)
+                mma_epi_segment<4, kKindGU>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+            else if (ntok <= 8)
+                mma_epi_segment<8, kKindGU>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+            else
+                mma_epi_segment<16, kKindGU>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+        } else {
+            if (ntok <= 4)
+                mma_epi_segment<4, kKindDN>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+            else if (ntok <= 8)
+                mma_epi_segment<8, kKindDN>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+            else
+                mma_epi_segment<16, kKindDN>(a, sm, set, tlane, r, ntok, res, ring.ld, rs, c, it);
+        }
         ++sidx;
     }
 }
@@ -1176,8 +1230,8 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
         float4 dec;
         const uint32_t codes = quant_group_warp(v, &sc, &dec);
         if (a.mma)
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(op.aq) + static_cast<size_t>(row) * op.K + g * kGroup +
-                                         lane * 4) = codes;
+            store_code_phases(reinterpret_cast<uint8_t*>(op.aq) + static_cast<size_t>(row) * op.K + g * kGroup,
+                              static_cast<size_t>(op.rows_a) * op.K, lane, codes);
         else
             *reinterpret_cast<float4*>(op.aq + (static_cast<size_t>(row) * op.KB + g) * kGroup + act_pos(lane * 4)) = dec;
         if (lane == 0) op.as[static_cast<size_t>(row) * op.KB + g] = sc;
