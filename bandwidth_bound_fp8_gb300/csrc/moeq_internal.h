@@ -84,6 +84,7 @@ struct StreamArgs {
 
 size_t stream_partials_floats(int grid);
 cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);
+cudaError_t launch_stream_mma(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);
 
 cudaError_t launch_quant_act(const void* x, int x_f32, int M, int K, uint8_t* q, float* s,
                              cudaStream_t stream);
