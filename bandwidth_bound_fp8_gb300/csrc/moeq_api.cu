@@ -2,6 +2,7 @@
 // layout and the launches.  Every check
 // runs on the host before anything is launched.
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -40,6 +41,19 @@ DeviceInfo current_device() {
         cache[dev].ok = (major == 10 && minor == 3);
     }
     return cache[dev];
+}
+
+// Token count (per expert) from which launches take the tcgen05 path: 8,
+// where it measured faster than the CUDA cores; the environment variable
+// MOEQ_MMA_MIN_TOKENS overrides it (read once; 17 or more keeps every launch
+// on the CUDA cores, 1 sends every launch to the tensor cores).
+int mma_min_tokens() {
+    static const int v = [] {
+        const char* e = std::getenv("MOEQ_MMA_MIN_TOKENS");
+        const int x = e ? std::atoi(e) : 0;
+        return x >= 1 ? x : kMmaMinTokens;
+    }();
+    return v;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -319,7 +333,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = M;   // the pairs of one expert are distinct tokens
-    a.mma = a.max_ntok >= kMmaMinTokens;
+    a.mma = a.max_ntok >= mma_min_tokens();
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
@@ -366,7 +380,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
-    a.mma = a.max_ntok >= kMmaMinTokens;
+    a.mma = a.max_ntok >= mma_min_tokens();
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
 }
@@ -527,7 +541,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     d.rows_a = mp;
     d.out = y;
     d.out_ld = H;
-    if (M == 1 || M >= kMmaMinTokens) {
+    if (M == 1 || M >= mma_min_tokens()) {
         // one token, or the tcgen05 path (where a stage costs the same for 1
         // or 16 tokens): the routed experts' blocks and the shared expert's
         // cost the same, so each kind is one list, dealt out in whole row
@@ -560,7 +574,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.max_uniq = mu;
     a.max_pairs = mp;
     a.max_ntok = M;
-    a.mma = M >= kMmaMinTokens;
+    a.mma = M >= mma_min_tokens();
     a.shared_id = E_routed;
     a.shared_p0 = M * top_k;
     a.M = M;
