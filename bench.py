@@ -153,7 +153,8 @@ class ClockSampler:
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("moeq_stream.cu", "moeq_device.cuh", "moeq_route.cuh", "moeq_internal.h"):
+    for f in ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_device.cuh", "moeq_route.cuh",
+              "moeq_internal.h"):
         with open(os.path.join(ROOT, "bandwidth_bound_fp8_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
