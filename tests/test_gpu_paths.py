@@ -1,0 +1,31 @@
+"""Both engine paths at every token count.
+
+By default a launch with 8 or more tokens per expert runs on tcgen05 and
+smaller ones on the CUDA cores.  The library reads MOEQ_MMA_MIN_TOKENS once
+per process, so these tests re-run the GEMM and reduced-layer parity tests
+in child processes:
+  * with the crossover at 1, every launch runs on tcgen05 (one-token
+    experts, ragged K tails, split-K at every size);
+  * with it at 17, every launch runs on the CUDA cores (16-token experts on
+    the shared-memory accumulation mode).
+The children use the same oracle comparisons and tolerances as the default
+run."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.parametrize("crossover", ["1", "17"])
+def test_parity_with_forced_path(crossover):
+    env = dict(os.environ, MOEQ_MMA_MIN_TOKENS=crossover)
+    cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+           os.path.join(HERE, "test_gpu_gemm.py"), os.path.join(HERE, "test_gpu_layer.py"),
+           "-k", "not full_size and not full_m1 and not multi_token_sampled"]
+    r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, f"crossover {crossover}:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"
