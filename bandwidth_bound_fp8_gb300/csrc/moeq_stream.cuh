@@ -458,8 +458,11 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
     if (d.ku0 == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
     const uint32_t bytes = static_cast<uint32_t>(ng) * kGroup * 4u;
+    // after an abort no copy is issued (the consumers stop reading)
+    const bool live = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0, 0);
     fence_proxy_async();
-    if constexpr (kMma) {
+    if (!live) {
+    } else if constexpr (kMma) {
         // B operand: token t's codes of group gl become row t of that group's
         // 16 x 128-byte block, whose 128-byte swizzle puts chunk c at c ^ (t % 8):
         // one bulk copy per (token, group) from the code phase t % 8
@@ -476,9 +479,10 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
                           codes + (t & 7) * phase_stride + static_cast<size_t>(rt) * op.K + (g0 + gl) * kGroup, 128,
                           &sm.prep_full[cs], l2_evict_first_policy());
         }
-    } else if (lane < m.ntok) {
-        bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup, bytes,
-                  &sm.prep_full[cs], l2_evict_first_policy());
+    } else {
+        if (lane < m.ntok)
+            bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup,
+                      bytes, &sm.prep_full[cs], l2_evict_first_policy());
     }
     if constexpr (kMma) {
         // token-minor, padded with zeros to kMmaN tokens
@@ -498,9 +502,13 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     }
     if (lane == 0) sm.chunk[cs] = d;
     __syncwarp();
-    if (lane == 0)
-        mbar_arrive_expect_tx(&sm.prep_full[cs], kMma ? static_cast<uint32_t>(ng * m.ntok) * 128u
-                                                       : bytes * static_cast<uint32_t>(m.ntok));
+    if (lane == 0) {
+        if (live)
+            mbar_arrive_expect_tx(&sm.prep_full[cs], kMma ? static_cast<uint32_t>(ng * m.ntok) * 128u
+                                                           : bytes * static_cast<uint32_t>(m.ntok));
+        else
+            mbar_arrive(&sm.prep_full[cs]);
+    }
 }
 
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
@@ -773,6 +781,16 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
             }
             ++sidx;
             u = seg_end_u;
+        }
+    }
+    if (sm.abort_flag) {
+        // Copies of the last two chunks may still be landing in their slots:
+        // wait for them (bounded) before the CTA may exit.
+        for (long long j = c > 2 ? c - 2 : 0; j < c; ++j) {
+            const unsigned long long t0 = global_timer_ns();
+            while (!mbar_try_wait(&sm.prep_full[j & 1], static_cast<uint32_t>((j >> 1) & 1)) &&
+                   global_timer_ns() - t0 < 100ull * 1000ull * 1000ull) {
+            }
         }
     }
     // end marker (the consumers pass it on to the finish warp)

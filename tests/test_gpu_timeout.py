@@ -1,0 +1,44 @@
+"""Failure detection without a GPU fault: every device wait in the engine is
+bounded (2 s) and ends in MOEQ_ERR_TIMEOUT in the workspace status word, with
+the kernel draining its copies and returning, so the context stays usable.
+
+The test makes one wait run out on purpose: the input-quantisation counter
+in the workspace header (byte offset 16) is set far below anything the
+launch can reach, so the chunk-preparing warps of every CTA give up after
+the limit.  It then checks the status, re-initialises the workspace and
+checks that a normal call on the same context still matches the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from moeq_testlib import STRICT, Experts, assert_close, device_plan, to_np
+from test_gpu_gemm import oracle_down
+
+pytestmark = pytest.mark.gpu
+
+A_CNT_INT_OFFSET = 16 // 4   # int32 index of the input-quantisation counter
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_bounded_wait_reports_timeout_and_the_context_survives(orc, M):
+    from bandwidth_bound_fp8_gb300 import moeq
+    K, N = 256, 256
+    ex = Experts(1, N, K, base_seed=71, which=1)
+    a = synth.activations_bf16(M, K, 73, 2, 20.0, device="cuda")
+    du, do, _, dn = device_plan([0], [0, M], [0])
+    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, M, 1, 0))
+    ws.t.view(torch.int32)[A_CNT_INT_OFFSET] = -(1 << 30)   # a count the launch can never reach
+    y = torch.zeros((M, N), device="cuda")
+    moeq.moeq_expert_gemm_down(a, K, N, ex.q, ex.s, 1, du, do, dn, 1, M, y, ws)
+    torch.cuda.synchronize()   # returns: the kernel gave up instead of hanging
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == moeq.MOEQ_ERR_TIMEOUT
+
+    # the same context, a fresh workspace state: a normal call is correct
+    moeq.moeq_workspace_init(ws.t, ws.nbytes)
+    y = torch.full((M, N), float("nan"), device="cuda")
+    moeq.moeq_expert_gemm_down(a, K, N, ex.q, ex.s, 1, du, do, dn, 1, M, y, ws)
+    torch.cuda.synchronize()
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
+    y_ref, T, _, _ = oracle_down(orc, to_np(a.contiguous().view(torch.uint16)), ex, [0], [0, M])
+    assert_close(to_np(y), y_ref, T, STRICT, what="after a timeout")
