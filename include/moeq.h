@@ -130,7 +130,9 @@ size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int t
  * Depends on the current device's SM count; 0 on invalid arguments. */
 size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up);
 /* Zero the workspace (split-K tickets and the device status word) on
- * `stream`.  Needed once after allocation; kernels leave it zeroed. */
+ * `stream`.  Needed once after allocation; kernels leave it zeroed.  After a
+ * launch that recorded an error (e.g. a bounded wait that gave up, which
+ * ends the kernel early) the workspace state is undefined: zero it again. */
 moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /* SYNCHRONOUS: copy the device status word (0 or a moeq_status that a
  * kernel recorded, e.g. MOEQ_ERR_TIMEOUT) to *device_status.  Waits for the
