@@ -1232,8 +1232,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 }
 
 // Launch one instantiation (persistent, one CTA per SM, all shared memory).
+// Internal linkage: each library instance (and translation unit) keeps its
+// own per-device "attribute set" flags and kernel handles.
 template <bool G32, bool D32, bool kMma>
-cudaError_t launch_t(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream) {
+static cudaError_t launch_t(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream) {
     static int configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
@@ -1257,7 +1259,7 @@ cudaError_t launch_t(const StreamArgs& args, int grid, bool cooperative, cudaStr
 }
 
 template <bool kMma>
-cudaError_t launch_mode(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream) {
+static cudaError_t launch_mode(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream) {
     const bool g = args.op[kKindGU].a_f32 != 0, d = args.op[kKindDN].a_f32 != 0;
     if (g)
         return d ? launch_t<true, true, kMma>(args, grid, cooperative, stream)
