@@ -3,7 +3,6 @@
 // and the E4M3 conversions, plus the per-group live activation quantiser.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -78,17 +77,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
-// 2-D tiled bulk-tensor load of one box into shared memory, completing on `bar`.
-// x is the innermost (byte) coordinate and must be a multiple of 16.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 // 1-D bulk copy of `bytes` (multiple of 16, 16-byte aligned ends) into
 // shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
@@ -150,33 +138,8 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 
 // N consecutive fp32 columns (N = 4, 8 or 16) of this thread's TMEM lane
-// (warp w reads lanes 32*(w%4) ..), then wait for the load.
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
-    uint32_t r[N];
-    if constexpr (N == 4) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(taddr));
-    } else if constexpr (N == 8) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                     : "r"(taddr));
-    } else {
-        static_assert(N == 16, "tmem_ld: 4, 8 or 16 columns");
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr));
-    }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < N; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// The same load without the wait (the registers are valid only after
-// tmem_wait_ld): lets several loads overlap.
+// (warp w reads lanes 32*(w%4) ..), without waiting: the registers are valid
+// after tmem_wait_ld, so several loads can overlap.
 template <int N>
 __device__ __forceinline__ void tmem_ld_nowait(uint32_t taddr, uint32_t (&r)[N]) {
     if constexpr (N == 4) {
@@ -220,10 +183,6 @@ __device__ __forceinline__ int ld_relaxed(const int* p) {
     int v;
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Orders generic-proxy memory accesses with async-proxy (bulk copy) ones.

@@ -2,7 +2,6 @@
 // (include/moeq.h) validates arguments and then calls these launchers.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
