@@ -15,7 +15,8 @@ the step touches / step time, in GB/s, at M = 1; the sweep key adds
 M = 1, 2, 4, 8, 16.  `roofline` reports the one kernel of the step (the fused
 layer kernel) against the measured HBM copy bandwidth; `e2e` is the same metric
 with the per-step host->device copy of x and logits and the device->host
-copy of the output inside the timed region; `cpu_baseline` is the oracle
+copy of the output inside the timed region (the copies run on their own
+streams, double-buffered, overlapping the neighbouring steps' compute); `cpu_baseline` is the oracle
 (test infrastructure, single-threaded C) on one M = 1 layer.
 
 --impl reference runs the oracle as the reference arm on the host cores
@@ -287,7 +288,11 @@ def bench_M(stack, M, steps, warmup, ws_world, seed, events_every=8):
 
 
 def bench_e2e(stack, M, steps, seed):
-    """Same metric through the public call, with host<->device copies per step."""
+    """Same metric through the public call, with host<->device copies per step:
+    each step copies its x and logits from pinned host memory and reads its
+    output back.  The copies run on their own streams, double-buffered, so that
+    step j+1's inputs and step j-1's output move while step j computes; the
+    timed region still holds every step's copies."""
     from bandwidth_bound_fp8_gb300 import moeq
     pool = 16
     xs, lg = make_inputs(pool, M, seed)
@@ -295,29 +300,46 @@ def bench_e2e(stack, M, steps, seed):
     hx = xs.cpu().pin_memory()
     hl = lg.cpu().pin_memory()
     hout = torch.empty((2, M, H), dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
-    dl = torch.empty((M, E), dtype=torch.float32, device="cuda")
-    dout = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    dx = [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dl = [torch.empty((M, E), dtype=torch.float32, device="cuda") for _ in range(2)]
+    dout = [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, E + 1, TOPK))
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot b landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # the layer that used slot b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # slot b's output read back
 
     def step(j):
-        s, l = j % pool, j % stack.L
-        dx.copy_(hx[s], non_blocking=True)
-        dl.copy_(hl[s], non_blocking=True)
-        moeq.moeq_moe_layer(dx, dl, H, I, E, TOPK, stack.gu_q[l], stack.gu_s[l], stack.dn_q[l], stack.dn_s[l],
-                            dout, ws)
-        hout[j % 2].copy_(dout, non_blocking=True)
+        b, s, l = j % 2, j % pool, j % stack.L
+        with torch.cuda.stream(up):
+            if j >= 2:
+                up.wait_event(ev_done[b])              # slot b's previous inputs are consumed
+            dx[b].copy_(hx[s], non_blocking=True)
+            dl[b].copy_(hl[s], non_blocking=True)
+            ev_in[b].record(up)
+        comp.wait_event(ev_in[b])
+        if j >= 2:
+            comp.wait_event(ev_out[b])                 # slot b's previous output is read back
+        moeq.moeq_moe_layer(dx[b], dl[b], H, I, E, TOPK, stack.gu_q[l], stack.gu_s[l], stack.dn_q[l],
+                            stack.dn_s[l], dout[b], ws, stream=comp)
+        ev_done[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            hout[b].copy_(dout[b], non_blocking=True)
+            ev_out[b].record(down)
 
     for j in range(5):
         step(j)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(comp)
     for j in range(steps):
         step(5 + j)
-    b.record()
+    comp.wait_stream(down)                             # the last output is on the host
+    e.record(comp)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
+    ms = a.elapsed_time(e)
     byts = sum(U[(5 + j) % pool] * EXPERT_BYTES for j in range(steps))
     h2d = M * H * 2 + M * E * 4
     d2h = M * H * 2
