@@ -64,8 +64,9 @@ inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 moeq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOEQ_OK : MOEQ_ERR_CUDA; }
 
 // ------------------------------------------------------------------ workspace
-// Header (256 B): status word, epoch, done ticket, route flag.
-constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffACnt = 16, kHeader = 256;
+// Header (256 B): status word, epoch, done ticket, input-quantisation count,
+// down-by-K-group count.
+constexpr size_t kOffStatus = 0, kOffEpoch = 4, kOffDone = 8, kOffACnt = 16, kOffDcCnt = 20, kHeader = 256;
 
 struct StreamWs {
     size_t aq[2], as[2];
@@ -102,7 +103,7 @@ StreamWs stream_ws_layout(size_t base, const int* aq_rows, const int* aq_k, int 
 }
 
 struct LayerWs {
-    size_t plan, h, y;
+    size_t plan, h, y, dc;
     StreamWs s;
 };
 
@@ -112,7 +113,9 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.plan = kHeader;
     l.h = align_up(l.plan + moeq_route_plan_bytes(M, E, k), 256);
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
-    const size_t after = l.y + sizeof(float) * static_cast<size_t>(mp) * H;
+    // one token: down by K group's sums per (pair, K group of down, column)
+    l.dc = align_up(l.y + sizeof(float) * static_cast<size_t>(mp) * H, 256);
+    const size_t after = l.dc + (M == 1 ? sizeof(float) * static_cast<size_t>(mp) * (I / 128) * H : 0);
     // tickets of the layer's lists: M == 1 uses the first two (whole lists),
     // M > 1 all six (shared, half A, half B of each kind)
     const int rbmax = mu * ((H > I ? H : I) / 128);
@@ -165,6 +168,7 @@ void fill_ws(StreamArgs& a, void* ws, const StreamWs& l, int grid) {
     a.epoch = reinterpret_cast<int*>(base + kOffEpoch);
     a.done = reinterpret_cast<int*>(base + kOffDone);
     a.a_cnt = reinterpret_cast<int*>(base + kOffACnt);
+    a.dc_cnt = reinterpret_cast<int*>(base + kOffDcCnt);
     for (int k = 0; k < 2; ++k) {
         a.op[k].aq = reinterpret_cast<float*>(base + l.aq[k]);
         a.op[k].as = reinterpret_cast<float*>(base + l.as[k]);
@@ -541,6 +545,13 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     d.rows_a = mp;
     d.out = y;
     d.out_ld = H;
+    a.mma = M >= mma_min_tokens();
+    // One token on the CUDA cores (unless y is asked for): down by K group.
+    // The CTA that finished gate_up row block kb of a pair goes on with
+    // down's tiles (nb, kb) for every nb, so no CTA waits for another's h;
+    // a combine over the K groups' sums ends the launch.
+    const int dc_cols = (H + dev.sms - 1) / dev.sms;
+    a.dc = M == 1 && !a.mma && !y_opt && (H / 128) % 2 == 0 && mp * dc_cols <= kDcCombineFloats;
     if (M == 1 || M >= mma_min_tokens()) {
         // one token, or the tcgen05 path (where a stage costs the same for 1
         // or 16 tokens): the routed experts' blocks and the shared expert's
@@ -549,7 +560,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
         a.n_lists = 2;
         a.list_kind[0] = kKindGU;
         a.list_src[0] = kSrcLayer;
-        a.list_kind[1] = kKindDN;
+        a.list_kind[1] = a.dc ? kKindDC : kKindDN;
         a.list_src[1] = kSrcLayer;
     } else {
         // the shared expert serves all M tokens (M times a routed block's
@@ -574,7 +585,6 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.max_uniq = mu;
     a.max_pairs = mp;
     a.max_ntok = M;
-    a.mma = M >= mma_min_tokens();
     a.shared_id = E_routed;
     a.shared_p0 = M * top_k;
     a.M = M;
@@ -587,6 +597,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.out_bf16 = static_cast<__nv_bfloat16*>(out);
     a.h_to_dn = 1;
     fill_ws(a, ws, l.s, dev.sms);
+    a.dc_part = reinterpret_cast<float*>(base + l.dc);
 
     cudaStream_t st = as_stream(stream);
     if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)

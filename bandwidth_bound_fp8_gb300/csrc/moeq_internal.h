@@ -16,6 +16,10 @@ constexpr int kMmaMinTokens = 8;  // launches with this many tokens per expert (
 constexpr int kMaxLists = 6;
 constexpr int kKindGU = 0;  // gate_up: a stage holds the gate tile and the up tile of one K group
 constexpr int kKindDN = 1;  // down: a stage holds two consecutive K tiles of one row block
+constexpr int kKindDC = 2;  // down by K group (one token): a stage holds two row blocks' tiles of one K group
+// Down by K group needs the combine's per-pair sums of one CTA's output
+// columns in one activation slot: max_pairs * ceil(H / grid) floats at most.
+constexpr int kDcCombineFloats = 6144;
 constexpr int kSrcShared = 0;      // the layer's shared expert alone, known before routing
 constexpr int kSrcPlanAll = 1;     // every unique expert of the caller's plan (standalone calls)
 constexpr int kSrcLayer = 2;       // the layer: its shared expert first, then the plan's routed experts
@@ -79,6 +83,13 @@ struct StreamArgs {
     size_t partial_list_floats;
     int* h_ready;             // [max_uniq, RB of gate_up]: epoch of the last write of h
     int* comb;                // [M, RB of down]
+    // down by K group (layer, one token, CUDA cores): the CTA that finished
+    // h's row block kb of a pair streams down's tiles (nb, kb) for every nb
+    // and leaves fp32 sums per (pair, kb, output column); after every CTA
+    // has counted itself in dc_cnt, each CTA combines a slice of columns.
+    int dc;
+    float* dc_part;           // [max_pairs, K groups of down, H]
+    int* dc_cnt;              // every launch adds one per CTA (epoch * grid once all have)
 };
 
 size_t stream_partials_floats(int grid);

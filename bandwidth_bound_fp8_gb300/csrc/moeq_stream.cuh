@@ -92,11 +92,12 @@ constexpr int kMaxRes = 8;               // result slots at most
 constexpr int kSegRing = 16;             // segment metadata entries (>= kMaxRes + 8, see prep_warp)
 
 struct ChunkDesc {
-    int kind;          // kKindGU / kKindDN; -1: no more work
+    int kind;          // kKindGU / kKindDN / kKindDC; -1: no more work
     int ku0, ku1;      // units [ku0, ku1) of the segment's row block
     int g0, ng;        // K groups of this chunk's activations
     int ntok;
     int seg_end;       // the segment's last chunk
+    int p0;            // down by K group: the pair whose sums the chunk leaves
 };
 
 struct SegMeta {       // what the helper needs to finish a segment
@@ -154,6 +155,7 @@ struct SmemTail {
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemTail);
+static_assert(kActSlot >= kDcCombineFloats, "the down-by-K-group combine works in one activation slot");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumers); }
@@ -173,6 +175,17 @@ struct ResRing {
     }
 };
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
+
+// The operand a list kind streams: down by K group streams down's tiles.
+__device__ __forceinline__ const Operand& kind_op(const StreamArgs& a, int kind) {
+    return a.op[kind == kKindDC ? kKindDN : kind];
+}
+
+// Row blocks per expert of a list kind: its output row blocks, or for down
+// by K group its K groups (each the h of one gate_up row block).
+__device__ __forceinline__ int kind_rbs(const StreamArgs& a, int kind) {
+    return kind == kKindDC ? a.op[kKindDN].KB : a.op[kind].RB;
+}
 
 // Position of element k (0..127) of a group in the shared activation layout:
 // lane l8 reads its four float4 (k = 16*l8 + 4i .. +3) at (8i + l8)*4, so the
@@ -218,9 +231,9 @@ __device__ __forceinline__ int dp_blocks_per_cta(long long n_rb, long long G) {
 __device__ __forceinline__ bool list_needs_plan(const StreamArgs& a, int li) {
     if (a.list_src[li] == kSrcShared || a.list_src[li] == kSrcPlanAll) return false;
     if (a.list_src[li] != kSrcLayer || a.M > 1) return true;
-    const Operand& op = a.op[a.list_kind[li]];
-    const int per = dp_blocks_per_cta(static_cast<long long>(a.max_uniq) * op.RB, gridDim.x);
-    return !(per > 0 && (static_cast<long long>(blockIdx.x) + 1) * per <= op.RB);
+    const int rbs = kind_rbs(a, a.list_kind[li]);
+    const int per = dp_blocks_per_cta(static_cast<long long>(a.max_uniq) * rbs, gridDim.x);
+    return !(per > 0 && (static_cast<long long>(blockIdx.x) + 1) * per <= rbs);
 }
 
 // U: unique experts of the plan (shared included), or -1 while unknown
@@ -229,9 +242,11 @@ __device__ __forceinline__ ListInfo list_info(const StreamArgs& a, int li, int U
     ListInfo L;
     L.kind = a.list_kind[li];
     L.src = a.list_src[li];
-    const Operand& op = a.op[L.kind];
-    L.RB = op.RB;
-    L.KU = L.kind == kKindGU ? op.KB : (op.KB + 1) / 2;
+    const Operand& op = kind_op(a, L.kind);
+    L.RB = kind_rbs(a, L.kind);
+    // units per row block: K groups (gate_up), K tile pairs (down), row
+    // block pairs (down by K group)
+    L.KU = L.kind == kKindGU ? op.KB : L.kind == kKindDC ? op.NB / 2 : (op.KB + 1) / 2;
     const int routed = U > 1 ? U - 1 : 0, half = (routed + 1) / 2;
     L.e0 = L.src == kSrcPlanRoutedB ? half : 0;
     L.n_exp = L.src == kSrcShared ? 1
@@ -353,7 +368,7 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
             if (U < 0 || U > a.max_uniq) U = 0;  // reported by the prep warp
         }
         const ListInfo L = list_info(a, li, U);
-        const Operand& op = a.op[L.kind];
+        const Operand& op = kind_op(a, L.kind);
         int cur = -1, expert = 0;
         for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi); ++u) {
             const int jb = u / L.KU, ku = u - jb * L.KU;
@@ -373,6 +388,11 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
                 bulk_load(dst, tile_ptr(op, expert, rb, ku), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, tile_ptr(op, expert, L.RB + rb, ku), kTile, &sm.full[s], pol);
+            } else if (L.kind == kKindDC) {
+                // row blocks 2ku and 2ku+1 of down at K group rb
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                bulk_load(dst, tile_ptr(op, expert, 2 * ku, rb), kTile, &sm.full[s], pol);
+                bulk_load(dst + kTile, tile_ptr(op, expert, 2 * ku + 1, rb), kTile, &sm.full[s], pol);
             } else {
                 const int nt = min(2, op.KB - 2 * ku);
                 mbar_arrive_expect_tx(&sm.full[s], nt * kTile);
@@ -511,6 +531,55 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     }
 }
 
+// Stage a chunk of down by K group into slot cs: the pair's quantised h
+// group m.rb (one 512-byte bulk copy), its scale, and the weight scales of
+// both tiles of each unit.  One token: the pair has one row.
+__device__ __forceinline__ void prep_chunk_dc(const StreamArgs& a, SmemTail& sm, long long c, long long sidx,
+                                           const SegMeta& m, const ChunkDesc& d, int lane) {
+    const Operand& op = a.op[kKindDN];
+    const int cs = static_cast<int>(c & 1);
+    const int n_sw = 2 * (d.ku1 - d.ku0);   // <= 2 * kChunkGroups
+    constexpr int kPer = (1 + 2 * kChunkGroups + 31) / 32;
+    float v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = lane + 32 * j;
+        float x = 0.0f;
+        if (i == 0) {
+            x = __ldcg(op.as + static_cast<size_t>(m.p0) * op.KB + m.rb);
+        } else if (i <= n_sw) {
+            const int q = i - 1, nb = 2 * (d.ku0 + (q >> 1)) + (q & 1);
+            x = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + m.rb);
+        }
+        v[j] = x;
+    }
+    if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
+    if (d.ku0 == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
+    const bool live = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0, 0);
+    fence_proxy_async();
+    if (live && lane == 0)
+        bulk_load(sm.act[cs], op.aq + (static_cast<size_t>(m.p0) * op.KB + m.rb) * kGroup, kGroup * 4u,
+                  &sm.prep_full[cs], l2_evict_first_policy());
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = lane + 32 * j;
+        if (i == 0) {
+            sm.act_s[cs][0] = v[j];
+        } else if (i <= n_sw) {
+            const int q = i - 1;
+            sm.sw[cs][q & 1][q >> 1] = v[j];
+        }
+    }
+    if (lane == 0) sm.chunk[cs] = d;
+    __syncwarp();
+    if (lane == 0) {
+        if (live)
+            mbar_arrive_expect_tx(&sm.prep_full[cs], kGroup * 4u);
+        else
+            mbar_arrive(&sm.prep_full[cs]);
+    }
+}
+
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
 // and (layer) the readiness flag of (expert, row block); down -> y and
 // (layer) the combine of every token whose last expert this was.
@@ -611,6 +680,7 @@ static __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail
     const ResRing ring(a);
     const int ld = ring.ld;
     const SegMeta m = sm.seg[sidx % kSegRing];
+    if (m.kind == kKindDC) return;   // its sums went out from the consumers
     float* res = ring.at(sm, sidx);
     const int rows = m.kind == kKindGU ? 256 : 128;
     if (!(m.ku0 == 0 && m.ku1 == m.KU)) {
@@ -715,8 +785,8 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
     }
     for (int li = 0; li < a.n_lists && !sm.abort_flag; ++li) {
         const ListInfo L = list_info(a, li, U);
-        const Operand& op = a.op[L.kind];
-        const int GPU = L.kind == kKindGU ? 1 : 2;
+        const Operand& op = kind_op(a, L.kind);
+        const int GPU = L.kind == kKindDN ? 2 : 1;   // K groups per unit
         for (int u = static_cast<int>(L.lo); u < static_cast<int>(L.hi) && !sm.abort_flag;) {
             SegMeta m;
             m.kind = L.kind;
@@ -761,9 +831,21 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 __syncwarp();
                 fence_proxy_async();
             }
-            // units per chunk: as many as a slot holds, evened out over the
-            // row block's chunks (so no chunk is a short remainder)
-            const int cu_max = kMma ? kMmaChunkGroups / GPU : max(1, (kActSlot / (kGroup * m.ntok)) / GPU);
+            // down by K group: the segment's one K group of h, from the
+            // gate_up row block that produced it (in the whole-block layout,
+            // this CTA's own)
+            if (m.kind == kKindDC) {
+                if (lane == 0)
+                    wait_flag(a.h_ready + static_cast<size_t>(m.slot) * a.op[kKindGU].RB + m.rb, epoch, a.status,
+                              &sm.abort_flag);
+                __syncwarp();
+                fence_proxy_async();
+            }
+            // units per chunk: as many as a slot holds (down by K group: as
+            // many as the weight-scale slots hold), evened out over the row
+            // block's chunks (so no chunk is a short remainder)
+            const int cu_max = m.kind == kKindDC ? kChunkGroups
+                             : kMma ? kMmaChunkGroups / GPU : max(1, (kActSlot / (kGroup * m.ntok)) / GPU);
             const int n_chunks = (L.KU + cu_max - 1) / cu_max;
             const int cu = (L.KU + n_chunks - 1) / n_chunks;
             for (int ua = m.ku0; ua < m.ku1; ua += cu) {
@@ -772,11 +854,16 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 d.kind = m.kind;
                 d.ku0 = ua;
                 d.ku1 = ub;
-                d.g0 = ua * GPU;
-                d.ng = min(op.KB, ub * GPU) - d.g0;
+                d.g0 = m.kind == kKindDC ? m.rb : ua * GPU;
+                d.ng = m.kind == kKindDC ? 1 : min(op.KB, ub * GPU) - d.g0;
                 d.ntok = m.ntok;
                 d.seg_end = ub == m.ku1;
-                prep_chunk<kMma>(a, op, sm, c, sidx, m, L, d, lane);   // ends with the prep_full arrival
+                d.p0 = m.p0;
+                // each ends with the prep_full arrival
+                if (m.kind == kKindDC)
+                    prep_chunk_dc(a, sm, c, sidx, m, d, lane);
+                else
+                    prep_chunk<kMma>(a, op, sm, c, sidx, m, L, d, lane);
                 ++c;
             }
             ++sidx;
@@ -1004,6 +1091,67 @@ __device__ __forceinline__ void consume_dispatch(const StreamArgs& a, SmemTail& 
         consume_segment_cold<KIND, 0>(a, sm, stages, res, ld, cw, lane, c, it);
 }
 
+// Down by K group, one token: a unit holds tiles (2u, kb) and (2u+1, kb),
+// 256 output rows over the one K group kb of h; warp w takes rows
+// (w%8)*16 .. +15 of tile w/8, as gate_up does.  Each unit's sums are
+// complete for that group: scaled by s_h * s_w and stored as the pair's
+// (kb, row) sums, 16 consecutive floats per warp.
+static __device__ __noinline__ void consume_dc(const StreamArgs& a, SmemTail& sm, const uint8_t* stages, int cw, int lane,
+                                        long long& c_io, long long& it_io) {
+    long long c = c_io, it = it_io;
+    const Operand& op = a.op[kKindDN];
+    const size_t H = static_cast<size_t>(op.NB) * 128;
+    const int tile_w = cw >> 3, rows_base = (cw & 7) * 16;
+    const int l8 = lane & 7, rsub = lane >> 3;
+    for (bool first = true;; first = false) {
+        const int cs = static_cast<int>(c & 1);
+        if (!first) mbar_wait_or_abort(&sm.prep_full[cs], static_cast<uint32_t>((c >> 1) & 1), sm, a.status);
+        const ChunkDesc d = sm.chunk[cs];
+        // the group's decoded codes, the same for every unit of the chunk
+        float2 av[8];
+        const float4* ap = reinterpret_cast<const float4*>(sm.act[cs]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 v = ap[i * 8 + l8];
+            av[2 * i] = make_float2(v.x, v.y);
+            av[2 * i + 1] = make_float2(v.z, v.w);
+        }
+        const float sa = sm.act_s[cs][0];
+        float* dst = a.dc_part + (static_cast<size_t>(d.p0) * op.KB + d.g0) * H + rows_base + lane;
+        for (int ku = d.ku0; ku < d.ku1; ++ku, ++it) {
+            const int s = static_cast<int>(it % kStages);
+            mbar_wait_or_abort(&sm.full[s], static_cast<uint32_t>((it / kStages) & 1), sm, a.status);
+            const uint8_t* tile = stages + static_cast<size_t>(s) * kStageBytes + tile_w * kTile;
+            float r = 0.0f;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int row = rows_base + p * 4 + rsub;
+                const uint4 w = *reinterpret_cast<const uint4*>(tile + row * 128 + ((l8 ^ (row & 7)) << 4));
+                float2 wf[8];
+                e4m3x4_to_f32(w.x, wf[0], wf[1]);
+                e4m3x4_to_f32(w.y, wf[2], wf[3]);
+                e4m3x4_to_f32(w.z, wf[4], wf[5]);
+                e4m3x4_to_f32(w.w, wf[6], wf[7]);
+                float2 dd = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dd = __ffma2_rn(wf[j], av[j], dd);
+                // row rows_base + 4p + q ends in lane 8q; lane 4p + q takes it
+                const float v = __shfl_sync(0xffffffffu, reduce8(dd.x + dd.y), (lane & 3) * 8);
+                if ((lane >> 2) == p) r = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            if (lane < 16) dst[static_cast<size_t>(2 * ku + tile_w) * 128] = r * (sa * sm.sw[cs][tile_w][ku - d.ku0]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.act_empty[cs]);
+        ++c;
+        if (d.seg_end || sm.abort_flag) break;
+    }
+    c_io = c;
+    it_io = it;
+}
+
 // ------------------------------------------------------------------ tcgen05 path
 // (defined in the translation unit that instantiates the tcgen05 kernels)
 template <bool kMma>
@@ -1048,6 +1196,42 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
             *reinterpret_cast<uint32_t*>(op.qdump + static_cast<size_t>(row) * op.K + g * kGroup + lane * 4) = codes;
             if (lane == 0) op.sdump[static_cast<size_t>(row) * op.KB + g] = sc;
         }
+    }
+}
+
+// The combine after down by K group (consumer threads, after their last
+// segment).  Every CTA counts itself in dc_cnt once its sums are out; then
+// CTA c combines output columns [c*H/G, (c+1)*H/G): per pair, the sum over
+// K groups in group order, then out = y_shared + sum_j w_j y_j in the
+// plan's order of picks, rounded once to bf16.  One token.
+static __device__ __noinline__ void dc_combine(const StreamArgs& a, SmemTail& sm, int tid, int epoch) {
+    __threadfence();   // this thread's sums, device-wide, before the count
+    consumer_sync();
+    if (tid == 0) {
+        atom_add_acq_rel(a.dc_cnt, 1);
+        wait_count(a.dc_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
+    }
+    consumer_sync();   // thread 0's acquire before every thread's loads
+    if (sm.abort_flag) return;
+    const Operand& op = a.op[kKindDN];
+    const int H = op.NB * 128, KB = op.KB, k = a.top_k, P = k + 1;
+    const long long G = gridDim.x, cta = blockIdx.x;
+    const int n0 = static_cast<int>(cta * H / G), W = static_cast<int>((cta + 1) * H / G) - n0;
+    float* ys = sm.act[0];   // [P][W]: the activation slots are idle now
+    for (int i = tid; i < P * W; i += kConsumers) {
+        const int p = i / W, n = n0 + i % W;
+        const float* src = a.dc_part + static_cast<size_t>(p) * KB * H + n;
+        float v = 0.0f;
+#pragma unroll 8
+        for (int kb = 0; kb < KB; ++kb) v += __ldcg(src + static_cast<size_t>(kb) * H);
+        ys[i] = v;
+    }
+    consumer_sync();
+    const int* po = sm.pv.pair_of;   // token 0
+    for (int i = tid; i < W; i += kConsumers) {
+        float acc = ys[po[k] * W + i];
+        for (int j = 0; j < k; ++j) acc = fmaf(sm.pv.topk_w[j], ys[po[j] * W + i], acc);
+        a.out_bf16[n0 + i] = __float2bfloat16_rn(acc);
     }
 }
 
@@ -1122,6 +1306,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         tc_fence_before();
     }
     const int epoch = ld_relaxed(a.epoch) + 1;
+    // every launch adds one per CTA to dc_cnt (keeping it at epoch * grid);
+    // down by K group counts in its combine
+    if (tid == 0 && !a.dc) atomicAdd(a.dc_cnt, 1);
     __syncthreads();
 
     if (warp == kProducerWarp) {
@@ -1223,12 +1410,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         float* res = ring.at(sm, sidx);
         if (kind == kKindGU)
             consume_dispatch<kKindGU>(a, sm, stages, res, ring.ld, ntok, cw, lane, c, it);
+        else if (kind == kKindDC)
+            consume_dc(a, sm, stages, cw, lane, c, it);
         else
             consume_dispatch<kKindDN>(a, sm, stages, res, ring.ld, ntok, cw, lane, c, it);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.res_full[rs]);
         ++sidx;
     }
+    if (a.dc) dc_combine(a, sm, tid, epoch);
 }
 
 // Launch one instantiation (persistent, one CTA per SM, all shared memory).

@@ -262,17 +262,24 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
 /* ------------------------------------------------------------------------ */
 /* moeq_moe_layer -- one MoE FFN layer for M tokens, in ONE kernel:         */
 /*   route -> [quant x + gate_up + SwiGLU] -> [quant h + down] -> combine   */
-/*   One persistent CTA per SM (cooperative launch): CTA 0 routes while     */
-/*   the others stream the shared expert, gate_up and down stream back to   */
-/*   back, down waits per expert for its h, and the combine runs in the     */
-/*   down epilogue.                                                         */
+/*   One persistent CTA per SM (cooperative launch): every CTA routes for   */
+/*   itself while CTAs whose first blocks are the shared expert's already   */
+/*   stream them, and gate_up and down stream back to back.  M > 1, or a   */
+/*   call that asks for y: down waits per expert for its h, and the         */
+/*   combine runs in the down epilogue.  M == 1 without y (CUDA-core path,  */
+/*   H/128 even): the CTA that finished gate_up row block kb of a pair      */
+/*   streams down's K group kb for every output row block ("down by K       */
+/*   group", no wait on other CTAs' h), and the launch ends with a combine  */
+/*   over the K groups' fp32 sums in a fixed order.  Both give out within   */
+/*   the same bound; their fp32 rounding orders differ.                     */
 /*   x      [M, H] bf16; logits [M, E_routed] fp32                          */
 /*   w_gu/s_gu, w_d/s_d: E_routed + 1 experts (tile-major codes), the       */
 /*           shared expert last                                             */
 /*   out    [M, H] bf16                                                     */
 /*   plan_opt, h_opt [max_pairs, I], y_opt [max_pairs, H]: optional         */
 /*           caller buffers that receive the plan and the intermediates     */
-/*           (NULL: kept in the workspace)                                  */
+/*           (NULL: kept in the workspace; a non-NULL y_opt selects the     */
+/*           row-block down path, which is the one that forms y)            */
 /*   events_opt: NULL, or 2 cudaEvent_t recorded on `stream` right before   */
 /*           and right after the layer's kernel, for the caller's timing    */
 /* A workspace serves one layer call at a time: consecutive calls on one    */

@@ -9,6 +9,10 @@ ragged group counts; the full MoE shape (hidden 6144, 256 routed experts of
 4096x6144 + 6144x2048, top-8 + 1 shared) runs at M = 1, 4 and 16, checked on
 every output at M = 1 and on sampled tokens at M = 4 and 16 (tokens are
 independent, a property pinned in the oracle).
+
+One token without the per-pair y output runs down by K group (each CTA's
+own h group against every output row block, then a combine over groups);
+asking for y keeps the row-block down path, so both are checked.
 """
 import numpy as np
 import pytest
@@ -27,13 +31,13 @@ class Layer:
         self.gu = Experts(E + 1, 2 * I, H, base_seed=seed, which=0, layer=layer)
         self.dn = Experts(E + 1, H, I, base_seed=seed, which=1, layer=layer)
 
-    def run(self, x, logits, k):
+    def run(self, x, logits, k, with_y=True):
         from bandwidth_bound_fp8_gb300 import moeq
         M = x.shape[0]
         plan = moeq.RoutePlan(M, self.E, k)
         P = plan.max_pairs
         h = torch.full((P, self.I), float("nan"), device="cuda")
-        y = torch.full((P, self.H), float("nan"), device="cuda")
+        y = torch.full((P, self.H), float("nan"), device="cuda") if with_y else None
         out = torch.empty((M, self.H), dtype=torch.bfloat16, device="cuda")
         ws = moeq.Workspace(moeq.moeq_workspace_size(M, self.H, self.I, self.E + 1, k))
         moeq.moeq_moe_layer(x, logits, self.H, self.I, self.E, k, self.gu.q, self.gu.s, self.dn.q, self.dn.s,
@@ -52,9 +56,9 @@ class Layer:
         return orc.moe_layer(x_bits, logits_np, k, experts, self.H, self.I), experts
 
 
-def check_layer(orc, lay, x, logits, k, rows=None):
+def check_layer(orc, lay, x, logits, k, rows=None, with_y=True):
     M = x.shape[0]
-    out, plan, h, y = lay.run(x, logits, k)
+    out, plan, h, y = lay.run(x, logits, k, with_y=with_y)
     rows = list(range(M)) if rows is None else rows
     x_bits, lg = bf16_bits(x), to_np(logits)
     for group in ([rows] if rows == list(range(M)) else [[m] for m in rows]):
@@ -93,13 +97,17 @@ def check_layer(orc, lay, x, logits, k, rows=None):
     return out
 
 
-@pytest.mark.parametrize("M,E,H,I,k", [(1, 16, 1024, 256, 4), (3, 16, 640, 384, 2), (16, 32, 512, 256, 8),
-                                       (5, 8, 768, 128, 8)])
-def test_layer_reduced(orc, M, E, H, I, k):
+@pytest.mark.parametrize("M,E,H,I,k,with_y", [(1, 16, 1024, 256, 4, True), (1, 16, 1024, 256, 4, False),
+                                              (1, 12, 1280, 384, 3, False), (1, 8, 640, 256, 2, False),
+                                              (3, 16, 640, 384, 2, True), (16, 32, 512, 256, 8, True),
+                                              (5, 8, 768, 128, 8, True)])
+def test_layer_reduced(orc, M, E, H, I, k, with_y):
+    # (1, 8, 640, ...): an odd number of output row blocks keeps one token
+    # on the row-block down path even without y
     lay = Layer(E, H, I, seed=50 + M + E)
     x = synth.activations_bf16(M, H, 51 + M, max(1, H // 100), 30.0, device="cuda")
     logits = synth.logits_f32(M, E, 52 + M, device="cuda")
-    check_layer(orc, lay, x, logits, k)
+    check_layer(orc, lay, x, logits, k, with_y=with_y)
 
 
 @pytest.fixture(scope="module")
@@ -108,11 +116,16 @@ def full_layer():
     return Layer(c["E"], c["H"], c["I"], seed=c["seed"])
 
 
-def test_layer_full_m1(orc, full_layer):
+@pytest.mark.parametrize("with_y", [True, False])
+def test_layer_full_m1(orc, full_layer, with_y):
     c = synth.MOE_LAYER
     x = synth.activations_bf16(1, c["H"], c["seed"], c["n_outlier"], c["outlier_scale"], device="cuda")
     logits = synth.logits_f32(1, c["E"], c["seed"] + 1, device="cuda")
-    check_layer(orc, full_layer, x, logits, c["top_k"])
+    out = check_layer(orc, full_layer, x, logits, c["top_k"], with_y=with_y)
+    if not with_y:
+        # determinism of the combine over K groups: a second run is bit-identical
+        out2, _, _, _ = full_layer.run(x, logits, c["top_k"], with_y=False)
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
 @pytest.mark.parametrize("M,rows", [(4, [0, 3]), (16, [5])])

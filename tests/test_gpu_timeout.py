@@ -6,7 +6,9 @@ The test makes one wait run out on purpose: the input-quantisation counter
 in the workspace header (byte offset 16) is set far below anything the
 launch can reach, so the chunk-preparing warps of every CTA give up after
 the limit.  It then checks the status, re-initialises the workspace and
-checks that a normal call on the same context still matches the oracle."""
+checks that a normal call on the same context still matches the oracle.
+A second case does the same to the count that the one-token layer's final
+combine waits for."""
 import numpy as np
 import pytest
 import torch
@@ -42,3 +44,29 @@ def test_bounded_wait_reports_timeout_and_the_context_survives(orc, M):
     assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
     y_ref, T, _, _ = oracle_down(orc, to_np(a.contiguous().view(torch.uint16)), ex, [0], [0, M])
     assert_close(to_np(y), y_ref, T, STRICT, what="after a timeout")
+
+
+DC_CNT_INT_OFFSET = 20 // 4  # int32 index of the down-by-K-group count
+
+
+def test_layer_combine_wait_reports_timeout_and_the_context_survives(orc):
+    """One token without y: the combine after down by K group waits for every
+    CTA's count.  With the count set out of reach that wait gives up, the
+    status says so, and after a re-initialisation the layer is correct."""
+    from test_gpu_layer import Layer, check_layer
+    from bandwidth_bound_fp8_gb300 import moeq
+    E, H, I, k = 8, 512, 256, 2
+    lay = Layer(E, H, I, seed=91)
+    x = synth.activations_bf16(1, H, 92, 2, 20.0, device="cuda")
+    logits = synth.logits_f32(1, E, 93, device="cuda")
+    out = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_workspace_size(1, H, I, E + 1, k))
+    ws.t.view(torch.int32)[DC_CNT_INT_OFFSET] = -(1 << 30)
+    moeq.moeq_moe_layer(x, logits, H, I, E, k, lay.gu.q, lay.gu.s, lay.dn.q, lay.dn.s, out, ws)
+    torch.cuda.synchronize()   # returns: the combine gave up instead of hanging
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == moeq.MOEQ_ERR_TIMEOUT
+    moeq.moeq_workspace_init(ws.t, ws.nbytes)
+    moeq.moeq_moe_layer(x, logits, H, I, E, k, lay.gu.q, lay.gu.s, lay.dn.q, lay.dn.s, out, ws)
+    torch.cuda.synchronize()
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
+    check_layer(orc, lay, x, logits, k, with_y=False)
