@@ -552,6 +552,12 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     // a combine over the K groups' sums ends the launch.
     const int dc_cols = (H + dev.sms - 1) / dev.sms;
     a.dc = M == 1 && !a.mma && !y_opt && (H / 128) % 2 == 0 && mp * dc_cols <= kDcCombineFloats;
+    // One gate_up block per CTA (whole blocks, as the engine deals them):
+    // each CTA quantises all of x for itself, and down by K group takes the
+    // h group the CTA finished itself from shared memory.
+    const bool one_block = dp_blocks_per_cta_host(static_cast<long long>(mu) * (I / 128), dev.sms) == 1;
+    a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block;
+    a.hloc = a.dc && one_block;
     if (M == 1 || M >= mma_min_tokens()) {
         // one token, or the tcgen05 path (where a stage costs the same for 1
         // or 16 tokens): the routed experts' blocks and the shared expert's

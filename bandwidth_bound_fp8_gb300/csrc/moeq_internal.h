@@ -90,7 +90,21 @@ struct StreamArgs {
     int dc;
     float* dc_part;           // [max_pairs, K groups of down, H]
     int* dc_cnt;              // every launch adds one per CTA (epoch * grid once all have)
+    // one token, whole blocks, one gate_up block per CTA: each CTA quantises
+    // all of x itself into its first activation slot (xloc), and hands the
+    // h group it finishes to its own down by K group in shared memory (hloc)
+    int xloc, hloc;
 };
+
+// Whole row blocks per CTA for n_rb blocks on G CTAs, or 0 for stream-K: the
+// engine's rule (whole blocks when the CTAs that get some are >= 90 % of G).
+inline int dp_blocks_per_cta_host(long long n_rb, long long G) {
+    if (n_rb <= 0) return 0;
+    const long long per = (n_rb + G - 1) / G, used = (n_rb + per - 1) / per;
+    return used * 10 >= G * 9 ? static_cast<int>(per) : 0;
+}
+// x fits one activation slot (decoded fp32 codes of one token)
+constexpr int kXLocalMaxK = 6144;
 
 size_t stream_partials_floats(int grid);
 cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);

@@ -133,13 +133,15 @@ struct PlanView {
 };
 
 struct SmemTail {
-    union {
-        float act[2][kActSlot];          // decoded activations [tok][group][permuted k]
-        RouteScratch route;              // plan computation, before any activation
-    };
+    float act[2][kActSlot];              // decoded activations [tok][group][permuted k]
     float act_s[2][kActScales];          // activation scales: [tok][group]; tcgen05 path [group][16 tok]
     float sw[2][2][kChunkGroups];        // weight scales per slot, per tile
-    float res[kResPool];                 // result slots: one sum per (row, token), see ResRing
+    union {
+        float res[kResPool];             // result slots: one sum per (row, token), see ResRing
+        RouteScratch route;              // plan computation: done before any chunk, so before any result
+    };
+    float hloc[kGroup];                  // one token: the h group this CTA finished (decoded codes) ...
+    float hloc_s;                        // ... and its scale
     ChunkDesc chunk[2];
     SegMeta seg[kSegRing];               // by segment index % kSegRing (see prep_warp)
     LocalPlan plan;
@@ -149,6 +151,8 @@ struct SmemTail {
     uint64_t full[kStages], empty[kStages];
     uint64_t prep_full[2], act_empty[2], res_full[kMaxRes], res_empty[kMaxRes];
     uint64_t plan_bar;                   // the LocalPlan is complete (layer)
+    uint64_t xq_bar;                     // x is quantised into act[0] / act_s[0] (xloc)
+    uint64_t hloc_bar;                   // hloc is written (hloc)
     uint64_t mma_done[kTmemBufs], tmem_empty[kTmemBufs];   // tcgen05 path
     uint32_t tmem_base;
     int abort_flag;
@@ -156,6 +160,7 @@ struct SmemTail {
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemTail);
 static_assert(kActSlot >= kDcCombineFloats, "the down-by-K-group combine works in one activation slot");
+static_assert(kActSlot >= kXLocalMaxK, "one token's x fits one activation slot");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumers); }
@@ -451,9 +456,12 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
             row = 0;
         }
     }
+    // one token's x quantised by this CTA itself: codes and scales are
+    // already in slot 0 (the first chunk's), only the weight scales remain
+    const bool xl = !kMma && a.xloc && m.kind == kKindGU && c == 0;
     // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all
     // loads first; only as many 32-wide passes as there are values
-    const int n_as = m.ntok * ng, n_all = n_as + ng * (m.kind == kKindGU ? 2 : 1);
+    const int n_as = xl ? 0 : m.ntok * ng, n_all = n_as + ng * (m.kind == kKindGU ? 2 : 1);
     const float* sw0 = op.sw + (static_cast<size_t>(m.expert) * op.NB + m.rb) * op.KB + g0;
     const size_t sw_up = static_cast<size_t>(L.RB) * op.KB;   // the up tile's row block
     constexpr int kPer = (kActScales + 2 * kChunkGroups + 31) / 32;
@@ -500,7 +508,7 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
                           &sm.prep_full[cs], l2_evict_first_policy());
         }
     } else {
-        if (lane < m.ntok)
+        if (!xl && lane < m.ntok)
             bulk_load(sm.act[cs] + lane * ng * kGroup, op.aq + (static_cast<size_t>(row) * op.KB + g0) * kGroup,
                       bytes, &sm.prep_full[cs], l2_evict_first_policy());
     }
@@ -523,7 +531,7 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     if (lane == 0) sm.chunk[cs] = d;
     __syncwarp();
     if (lane == 0) {
-        if (live)
+        if (live && !xl)
             mbar_arrive_expect_tx(&sm.prep_full[cs], kMma ? static_cast<uint32_t>(ng * m.ntok) * 128u
                                                            : bytes * static_cast<uint32_t>(m.ntok));
         else
@@ -532,48 +540,54 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
 }
 
 // Stage a chunk of down by K group into slot cs: the pair's quantised h
-// group m.rb (one 512-byte bulk copy), its scale, and the weight scales of
-// both tiles of each unit.  One token: the pair has one row.
+// group m.rb, its scale, and the weight scales of both tiles of each unit.
+// The weight scales are loaded first; then, for the segment's first chunk,
+// the wait for the h group: from this CTA's own finish warp in shared
+// memory (hloc), else the group's readiness flag and one 512-byte bulk copy
+// of its decoded codes.  One token: the pair has one row.
 __device__ __forceinline__ void prep_chunk_dc(const StreamArgs& a, SmemTail& sm, long long c, long long sidx,
-                                           const SegMeta& m, const ChunkDesc& d, int lane) {
+                                              const SegMeta& m, const ChunkDesc& d, int lane, int epoch) {
     const Operand& op = a.op[kKindDN];
     const int cs = static_cast<int>(c & 1);
     const int n_sw = 2 * (d.ku1 - d.ku0);   // <= 2 * kChunkGroups
-    constexpr int kPer = (1 + 2 * kChunkGroups + 31) / 32;
+    constexpr int kPer = (2 * kChunkGroups + 31) / 32;
     float v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-        const int i = lane + 32 * j;
-        float x = 0.0f;
-        if (i == 0) {
-            x = __ldcg(op.as + static_cast<size_t>(m.p0) * op.KB + m.rb);
-        } else if (i <= n_sw) {
-            const int q = i - 1, nb = 2 * (d.ku0 + (q >> 1)) + (q & 1);
-            x = __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + m.rb);
+        const int q = lane + 32 * j, nb = 2 * (d.ku0 + (q >> 1)) + (q & 1);
+        v[j] = q < n_sw ? __ldg(op.sw + (static_cast<size_t>(m.expert) * op.NB + nb) * op.KB + m.rb) : 0.0f;
+    }
+    if (d.ku0 == m.ku0) {
+        if (a.hloc) {
+            if (lane == 0) mbar_wait_or_abort(&sm.hloc_bar, 0, sm, a.status);
+        } else if (lane == 0) {
+            wait_flag(a.h_ready + static_cast<size_t>(m.slot) * a.op[kKindGU].RB + m.rb, epoch, a.status,
+                      &sm.abort_flag);
         }
-        v[j] = x;
+        __syncwarp();
     }
     if (c >= 2) mbar_wait_or_abort(&sm.act_empty[cs], static_cast<uint32_t>(((c >> 1) - 1) & 1), sm, a.status);
     if (d.ku0 == m.ku0 && lane == 0) sm.seg[sidx % kSegRing] = m;
     const bool live = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0, 0);
-    fence_proxy_async();
-    if (live && lane == 0)
-        bulk_load(sm.act[cs], op.aq + (static_cast<size_t>(m.p0) * op.KB + m.rb) * kGroup, kGroup * 4u,
-                  &sm.prep_full[cs], l2_evict_first_policy());
+    if (a.hloc) {
+        *reinterpret_cast<float4*>(sm.act[cs] + 4 * lane) = *reinterpret_cast<const float4*>(sm.hloc + 4 * lane);
+        if (lane == 0) sm.act_s[cs][0] = sm.hloc_s;
+    } else {
+        fence_proxy_async();
+        if (live && lane == 0)
+            bulk_load(sm.act[cs], op.aq + (static_cast<size_t>(m.p0) * op.KB + m.rb) * kGroup, kGroup * 4u,
+                      &sm.prep_full[cs], l2_evict_first_policy());
+        if (lane == 0) sm.act_s[cs][0] = __ldcg(op.as + static_cast<size_t>(m.p0) * op.KB + m.rb);
+    }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-        const int i = lane + 32 * j;
-        if (i == 0) {
-            sm.act_s[cs][0] = v[j];
-        } else if (i <= n_sw) {
-            const int q = i - 1;
-            sm.sw[cs][q & 1][q >> 1] = v[j];
-        }
+        const int q = lane + 32 * j;
+        if (q < n_sw) sm.sw[cs][q & 1][q >> 1] = v[j];
     }
     if (lane == 0) sm.chunk[cs] = d;
     __syncwarp();
     if (lane == 0) {
-        if (live)
+        if (live && !a.hloc)
             mbar_arrive_expect_tx(&sm.prep_full[cs], kGroup * 4u);
         else
             mbar_arrive(&sm.prep_full[cs]);
@@ -583,8 +597,9 @@ __device__ __forceinline__ void prep_chunk_dc(const StreamArgs& a, SmemTail& sm,
 // Finish one segment from its result slot: gate_up -> h = silu(gate) * up
 // and (layer) the readiness flag of (expert, row block); down -> y and
 // (layer) the combine of every token whose last expert this was.
-static __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const PlanView& pv, const SegMeta& m,
+static __device__ __noinline__ void helper_epilogue(const StreamArgs& a, SmemTail& sm, const SegMeta& m,
                                              const float* res, int ld, int lane, int epoch) {
+    const PlanView& pv = sm.pv;
     const Operand& op = a.op[m.kind];
     if (m.valid && m.kind == kKindGU) {
         // lane owns h columns 4*lane .. 4*lane+3 of this row block; in the
@@ -602,6 +617,17 @@ static __device__ __noinline__ void helper_epilogue(const StreamArgs& a, const P
             }
             const float4 h4 = make_float4(hv[0], hv[1], hv[2], hv[3]);
             const size_t p = static_cast<size_t>(m.p0 + t);
+            if (a.hloc) {
+                // this CTA's own down by K group takes the group from shared
+                // memory, before any of the global writes below
+                float sc;
+                float4 dec;
+                quant_group_warp(h4, &sc, &dec);
+                *reinterpret_cast<float4*>(sm.hloc + act_pos(4 * lane)) = dec;
+                if (lane == 0) sm.hloc_s = sc;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.hloc_bar);
+            }
             *reinterpret_cast<float4*>(op.out + p * op.out_ld + m.rb * 128 + 4 * lane) = h4;
             if (a.h_to_dn) {
                 float sc;
@@ -753,10 +779,10 @@ static __device__ __noinline__ void finish_segment(const StreamArgs& a, SmemTail
             }
             __syncwarp();
             if (lane == 0) a.tickets[m.li][rblk] = 0;
-            helper_epilogue(a, sm.pv, m, res, ld, lane, epoch);
+            helper_epilogue(a, sm, m, res, ld, lane, epoch);
         }
     } else {
-        helper_epilogue(a, sm.pv, m, res, ld, lane, epoch);
+        helper_epilogue(a, sm, m, res, ld, lane, epoch);
     }
 }
 
@@ -772,10 +798,17 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
     long long c = 0;         // chunks prepared
     long long sidx = 0;      // segments started
     bool have_input = false;
-    // The plan's scratch shares memory with the activation slots: the layer's
-    // prep warp starts once the CTA's plan is complete.
+    // The lists need the plan, and its scratch shares memory with the result
+    // slots: the layer's prep warp starts once the CTA's plan is complete (so
+    // every result is written after it).
     if (a.fused_route) {
         if (lane == 0) mbar_wait_or_abort(&sm.plan_bar, 0, sm, a.status);
+        __syncwarp();
+    }
+    // one token: this CTA's consumers quantise all of x into act[0] (the
+    // first chunk's slot); otherwise every CTA's share goes to the workspace
+    if (a.xloc) {
+        if (lane == 0) mbar_wait_or_abort(&sm.xq_bar, 0, sm, a.status);
         __syncwarp();
     }
     int U = *sm.pv.n_uniq;
@@ -817,7 +850,7 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
             m.KU = L.KU;
             m.RB = L.RB;
             // activations quantised by the kernel's first phase: all CTAs' shares
-            if (op.quant_input && !have_input) {
+            if (op.quant_input && !have_input && !a.xloc) {
                 if (lane == 0) wait_count(a.a_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
                 __syncwarp();
                 have_input = true;
@@ -828,16 +861,6 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 const int nrb = a.op[kKindGU].RB;
                 for (int j = lane; j < nrb; j += 32)
                     wait_flag(a.h_ready + static_cast<size_t>(m.slot) * nrb + j, epoch, a.status, &sm.abort_flag);
-                __syncwarp();
-                fence_proxy_async();
-            }
-            // down by K group: the segment's one K group of h, from the
-            // gate_up row block that produced it (in the whole-block layout,
-            // this CTA's own)
-            if (m.kind == kKindDC) {
-                if (lane == 0)
-                    wait_flag(a.h_ready + static_cast<size_t>(m.slot) * a.op[kKindGU].RB + m.rb, epoch, a.status,
-                              &sm.abort_flag);
                 __syncwarp();
                 fence_proxy_async();
             }
@@ -861,7 +884,7 @@ __device__ __forceinline__ void prep_warp(const StreamArgs& a, SmemTail& sm, int
                 d.p0 = m.p0;
                 // each ends with the prep_full arrival
                 if (m.kind == kKindDC)
-                    prep_chunk_dc(a, sm, c, sidx, m, d, lane);
+                    prep_chunk_dc(a, sm, c, sidx, m, d, lane, epoch);
                 else
                     prep_chunk<kMma>(a, op, sm, c, sidx, m, L, d, lane);
                 ++c;
@@ -1205,9 +1228,9 @@ __device__ __noinline__ void quantise_inputs(const StreamArgs& a, int warp, int 
 // K groups in group order, then out = y_shared + sum_j w_j y_j in the
 // plan's order of picks, rounded once to bf16.  One token.
 static __device__ __noinline__ void dc_combine(const StreamArgs& a, SmemTail& sm, int tid, int epoch) {
-    __threadfence();   // this thread's sums, device-wide, before the count
-    consumer_sync();
+    consumer_sync();   // every consumer's sums are stored ...
     if (tid == 0) {
+        __threadfence();   // ... and thread 0's fence releases them with the count
         atom_add_acq_rel(a.dc_cnt, 1);
         wait_count(a.dc_cnt, epoch * static_cast<int>(gridDim.x), a.status, &sm.abort_flag);
     }
@@ -1232,6 +1255,22 @@ static __device__ __noinline__ void dc_combine(const StreamArgs& a, SmemTail& sm
         float acc = ys[po[k] * W + i];
         for (int j = 0; j < k; ++j) acc = fmaf(sm.pv.topk_w[j], ys[po[j] * W + i], acc);
         a.out_bf16[n0 + i] = __float2bfloat16_rn(acc);
+    }
+}
+
+// One token, x quantised by each CTA for itself: every 128-group of row 0
+// by one warp, decoded codes straight into act[0] (group g at g*128, the
+// consumer layout) and the scales into act_s[0]: the first chunk's slot.
+template <bool kF32>
+__device__ __noinline__ void quantise_x_local(const StreamArgs& a, SmemTail& sm, int warp, int nwarps, int lane) {
+    const Operand& op = a.op[kKindGU];
+    for (int g = warp; g < op.KB; g += nwarps) {
+        const float4 v = load_act4<kF32>(op.a, static_cast<size_t>(op.K), 0, g * kGroup + lane * 4);
+        float sc;
+        float4 dec;
+        quant_group_warp(v, &sc, &dec);
+        *reinterpret_cast<float4*>(sm.act[0] + g * kGroup + act_pos(lane * 4)) = dec;
+        if (lane == 0) sm.act_s[0][g] = sc;
     }
 }
 
@@ -1281,6 +1320,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             mbar_init(&sm.tmem_empty[b], 4);   // the four warps of the set that owns the buffer
         }
         mbar_init(&sm.plan_bar, 1);
+        mbar_init(&sm.xq_bar, 1);
+        mbar_init(&sm.hloc_bar, 1);
         if (a.fused_route) {
             sm.pv.n_uniq = &sm.plan.n_uniq;
             sm.pv.uniq = sm.plan.uniq;
@@ -1342,6 +1383,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         __threadfence();
         consumer_sync();
         if (tid == 0) atomicAdd(a.a_cnt, 1);
+    } else if (cw >= kCW / 2 && a.xloc) {
+        // half the consumers quantise all of one token's x into this CTA's
+        // first activation slot (the count keeps a_cnt at epoch * grid) ...
+        quantise_x_local<kGuF32>(a, sm, cw - kCW / 2, kCW / 2, lane);
+        named_sync(3, kConsumers / 2);
+        if (cw == kCW / 2 && lane == 0) {
+            mbar_arrive(&sm.xq_bar);
+            atomicAdd(a.a_cnt, 1);
+        }
     } else if (cw >= kCW / 2) {
         // half the consumers quantise this CTA's share of the inputs ...
         quantise_inputs<kGuF32, kDnF32, kMma>(a, cw - kCW / 2, kCW / 2, lane);

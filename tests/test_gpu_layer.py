@@ -99,11 +99,14 @@ def check_layer(orc, lay, x, logits, k, rows=None, with_y=True):
 
 @pytest.mark.parametrize("M,E,H,I,k,with_y", [(1, 16, 1024, 256, 4, True), (1, 16, 1024, 256, 4, False),
                                               (1, 12, 1280, 384, 3, False), (1, 8, 640, 256, 2, False),
+                                              (1, 16, 512, 2432, 7, False), (1, 16, 512, 2432, 7, True),
                                               (3, 16, 640, 384, 2, True), (16, 32, 512, 256, 8, True),
                                               (5, 8, 768, 128, 8, True)])
 def test_layer_reduced(orc, M, E, H, I, k, with_y):
     # (1, 8, 640, ...): an odd number of output row blocks keeps one token
-    # on the row-block down path even without y
+    # on the row-block down path even without y; (1, 16, 512, 2432, 7): 8
+    # unique experts x 19 gate_up blocks = 152, one block per CTA on 152 SMs
+    # (x quantised by every CTA for itself, h handed over in shared memory)
     lay = Layer(E, H, I, seed=50 + M + E)
     x = synth.activations_bf16(M, H, 51 + M, max(1, H // 100), 30.0, device="cuda")
     logits = synth.logits_f32(M, E, 52 + M, device="cuda")
