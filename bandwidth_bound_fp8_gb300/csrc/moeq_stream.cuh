@@ -1245,7 +1245,7 @@ static __device__ __noinline__ void dc_combine(const StreamArgs& a, SmemTail& sm
         const int p = i / W, n = n0 + i % W;
         const float* src = a.dc_part + static_cast<size_t>(p) * KB * H + n;
         float v = 0.0f;
-#pragma unroll 8
+#pragma unroll 16
         for (int kb = 0; kb < KB; ++kb) v += __ldcg(src + static_cast<size_t>(kb) * H);
         ys[i] = v;
     }
@@ -1261,16 +1261,30 @@ static __device__ __noinline__ void dc_combine(const StreamArgs& a, SmemTail& sm
 // One token, x quantised by each CTA for itself: every 128-group of row 0
 // by one warp, decoded codes straight into act[0] (group g at g*128, the
 // consumer layout) and the scales into act_s[0]: the first chunk's slot.
+// The warp's groups are all loaded before any is quantised (one round trip).
+constexpr int kXLocalPer = kXLocalMaxK / kGroup / (kCW / 2);   // groups per warp of the quantising half
+static_assert(kXLocalPer * kGroup * (kCW / 2) == kXLocalMaxK, "x groups split evenly over the warps");
 template <bool kF32>
-__device__ __noinline__ void quantise_x_local(const StreamArgs& a, SmemTail& sm, int warp, int nwarps, int lane) {
+__device__ __noinline__ void quantise_x_local(const StreamArgs& a, SmemTail& sm, int warp, int lane) {
     const Operand& op = a.op[kKindGU];
-    for (int g = warp; g < op.KB; g += nwarps) {
-        const float4 v = load_act4<kF32>(op.a, static_cast<size_t>(op.K), 0, g * kGroup + lane * 4);
-        float sc;
-        float4 dec;
-        quant_group_warp(v, &sc, &dec);
-        *reinterpret_cast<float4*>(sm.act[0] + g * kGroup + act_pos(lane * 4)) = dec;
-        if (lane == 0) sm.act_s[0][g] = sc;
+    constexpr int nwarps = kCW / 2;
+    float4 v[kXLocalPer];
+#pragma unroll
+    for (int i = 0; i < kXLocalPer; ++i) {
+        const int g = warp + i * nwarps;
+        v[i] = g < op.KB ? load_act4<kF32>(op.a, static_cast<size_t>(op.K), 0, g * kGroup + lane * 4)
+                         : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < kXLocalPer; ++i) {
+        const int g = warp + i * nwarps;
+        if (g < op.KB) {   // warp-uniform
+            float sc;
+            float4 dec;
+            quant_group_warp(v[i], &sc, &dec);
+            *reinterpret_cast<float4*>(sm.act[0] + g * kGroup + act_pos(lane * 4)) = dec;
+            if (lane == 0) sm.act_s[0][g] = sc;
+        }
     }
 }
 
@@ -1346,6 +1360,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tc_fence_before();
     }
+    if (a.fused_route && warp < kCW) {
+        // the logits (and one token's x) are read right after the barrier
+        // below: start their lines towards L2 now
+        const int lg_lines = (a.M * a.E_routed * 4 + 127) / 128;
+        if (tid < lg_lines) prefetch_l2(reinterpret_cast<const char*>(a.logits) + 128 * tid);
+        const int x_lines = a.xloc ? (a.op[kKindGU].K * (a.op[kKindGU].a_f32 ? 4 : 2) + 127) / 128 : 0;
+        if (tid < x_lines) prefetch_l2(static_cast<const char*>(a.op[kKindGU].a) + 128 * tid);
+    }
     const int epoch = ld_relaxed(a.epoch) + 1;
     // every launch adds one per CTA to dc_cnt (keeping it at epoch * grid);
     // down by K group counts in its combine
@@ -1386,7 +1408,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     } else if (cw >= kCW / 2 && a.xloc) {
         // half the consumers quantise all of one token's x into this CTA's
         // first activation slot (the count keeps a_cnt at epoch * grid) ...
-        quantise_x_local<kGuF32>(a, sm, cw - kCW / 2, kCW / 2, lane);
+        quantise_x_local<kGuF32>(a, sm, cw - kCW / 2, lane);
         named_sync(3, kConsumers / 2);
         if (cw == kCW / 2 && lane == 0) {
             mbar_arrive(&sm.xq_bar);
