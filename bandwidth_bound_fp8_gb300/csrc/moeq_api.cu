@@ -558,6 +558,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     const bool one_block = dp_blocks_per_cta_host(static_cast<long long>(mu) * (I / 128), dev.sms) == 1;
     a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block;
     a.hloc = a.dc && one_block;
+    a.swb = a.xloc && aligned16(s_gu) && (H / 128) % 4 == 0;
     if (M == 1 || M >= mma_min_tokens()) {
         // one token, or the tcgen05 path (where a stage costs the same for 1
         // or 16 tokens): the routed experts' blocks and the shared expert's

@@ -94,6 +94,9 @@ struct StreamArgs {
     // all of x itself into its first activation slot (xloc), and hands the
     // h group it finishes to its own down by K group in shared memory (hloc)
     int xloc, hloc;
+    // with xloc: the CTA's first stage also brings its gate_up chunk's two
+    // rows of weight scales (bulk copies, 16-byte aligned rows)
+    int swb;
 };
 
 // Whole row blocks per CTA for n_rb blocks on G CTAs, or 0 for stream-K: the

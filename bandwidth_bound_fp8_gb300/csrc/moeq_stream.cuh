@@ -161,6 +161,8 @@ struct SmemTail {
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(SmemTail);
 static_assert(kActSlot >= kDcCombineFloats, "the down-by-K-group combine works in one activation slot");
 static_assert(kActSlot >= kXLocalMaxK, "one token's x fits one activation slot");
+static_assert(offsetof(SmemTail, sw) % 16 == 0 && (kChunkGroups * 4) % 16 == 0,
+              "weight-scale rows are bulk-copy destinations");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumers); }
@@ -390,9 +392,21 @@ __device__ __forceinline__ void producer(const StreamArgs& a, SmemTail& sm, uint
             if (sm.abort_flag) break;
             uint8_t* dst = stages + static_cast<size_t>(s) * kStageBytes;
             if (L.kind == kKindGU) {
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                // one token, one block per CTA: the first stage also brings
+                // the gate and up weight-scale rows of the block (the first
+                // chunk's, all K groups) into the first chunk's scale slots,
+                // so they land with the first tiles rather than behind them
+                const bool swb = a.swb && issued == 0;
+                const uint32_t sw_bytes = static_cast<uint32_t>(op.KB) * 4u;
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + (swb ? 2u * sw_bytes : 0u));
                 bulk_load(dst, tile_ptr(op, expert, rb, ku), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, tile_ptr(op, expert, L.RB + rb, ku), kTile, &sm.full[s], pol);
+                if (swb) {
+                    bulk_load(sm.sw[0][0], op.sw + (static_cast<size_t>(expert) * op.NB + rb) * op.KB, sw_bytes,
+                              &sm.full[s], pol);
+                    bulk_load(sm.sw[0][1], op.sw + (static_cast<size_t>(expert) * op.NB + L.RB + rb) * op.KB,
+                              sw_bytes, &sm.full[s], pol);
+                }
             } else if (L.kind == kKindDC) {
                 // row blocks 2ku and 2ku+1 of down at K group rb
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
@@ -461,7 +475,7 @@ __device__ __forceinline__ void prep_chunk(const StreamArgs& a, const Operand& o
     const bool xl = !kMma && a.xloc && m.kind == kKindGU && c == 0;
     // scales: activation (ntok x ng) then weight (1 or 2 tiles x ng), all
     // loads first; only as many 32-wide passes as there are values
-    const int n_as = xl ? 0 : m.ntok * ng, n_all = n_as + ng * (m.kind == kKindGU ? 2 : 1);
+    const int n_as = xl ? 0 : m.ntok * ng, n_all = n_as + (xl && a.swb ? 0 : ng * (m.kind == kKindGU ? 2 : 1));
     const float* sw0 = op.sw + (static_cast<size_t>(m.expert) * op.NB + m.rb) * op.KB + g0;
     const size_t sw_up = static_cast<size_t>(L.RB) * op.KB;   // the up tile's row block
     constexpr int kPer = (kActScales + 2 * kChunkGroups + 31) / 32;
