@@ -11,12 +11,16 @@
 //
 // Work.  A unit is one stage: for gate_up the gate tile and the up tile of
 // one 128-row block at one 128-wide K group (32 KiB), for down two
-// consecutive K tiles of one 128-row block (32 KiB).  Work comes in lists
-// (for the layer: gate_up, then down, each over the shared expert first and
-// then the routed experts of the plan).  When the row blocks of a list
-// nearly fill the grid in whole numbers per CTA (one token: 144 gate_up
-// blocks on 152 SMs, 3 down blocks per CTA), each CTA takes whole row blocks
-// and nothing is split.  Otherwise every CTA takes a contiguous, equal share
+// consecutive K tiles of one 128-row block (32 KiB), for down by K group
+// (one token) two row blocks' tiles of one K group (32 KiB).  Work comes in
+// lists (for the layer: gate_up, then down, each over the shared expert
+// first and then the routed experts of the plan).  When the row blocks of a
+// list nearly fill the grid in whole numbers per CTA (one token: 144 gate_up
+// blocks on 152 SMs), each CTA takes whole row blocks and nothing is split.
+// One token goes on with down by K group: the CTA that finished gate_up
+// block kb of a pair streams down's tiles (nb, kb) for every nb (its own h
+// group against all of down's rows) and stores fp32 sums per (pair, kb,
+// row); a combine over K groups ends the launch.  Otherwise every CTA takes a contiguous, equal share
 // of the list's units (stream-K); a share splits into segments (runs of one
 // row block) of which only the first and last can be partial in K, so each
 // CTA leaves at most two fp32 partials per list; the last CTA to finish a

@@ -151,14 +151,29 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_device.cuh", "moeq_route.cuh",
+                  "moeq_internal.h")
+
+
+def code_hash(texts):
+    """Hash of C/CUDA sources with comments and whitespace removed: the
+    traffic record follows changes of the code, not of its comments."""
     import hashlib
+    import re
     h = hashlib.sha256()
-    for f in ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_device.cuh", "moeq_route.cuh",
-              "moeq_internal.h"):
-        with open(os.path.join(ROOT, "bandwidth_bound_fp8_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for src in texts:
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    texts = []
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "bandwidth_bound_fp8_gb300", "csrc", f), encoding="utf-8") as fh:
+            texts.append(fh.read())
+    return code_hash(texts)
 
 
 def ncu_traffic(kernel: str, M: int):
