@@ -122,7 +122,8 @@ moeq_status moeq_route_plan_carve(void* base, size_t bytes, int M, int E_routed,
 /* Bytes needed by moeq_moe_layer for M tokens, hidden H, expert
  * intermediate I, n_experts_incl_shared = E_routed + 1, top_k.  Depends on
  * the current device's SM count; returns 0 on invalid arguments or when no
- * device is present. */
+ * device is present.  At M == 1 it includes the fp32 sums of down by K group
+ * (max_pairs * I/128 * H floats: 3.5 MB for H 6144, I 2048, top-8). */
 size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int top_k);
 /* Bytes needed by one standalone GEMM call.  gate_up (is_gate_up = 1):
  * rows_out = I, K = H, rows_in = M; down (is_gate_up = 0): rows_out = N,
