@@ -16,7 +16,8 @@ M = 1, 2, 4, 8, 16.  `roofline` reports the one kernel of the step (the fused
 layer kernel) against the measured HBM copy bandwidth; `e2e` is the same metric
 with the per-step host->device copy of x and logits and the device->host
 copy of the output inside the timed region (the copies run on their own
-streams, double-buffered, overlapping the neighbouring steps' compute); `cpu_baseline` is the oracle
+streams, double-buffered, overlapping the neighbouring steps' compute; 16
+steps at a time replayed from one CUDA graph); `cpu_baseline` is the oracle
 (test infrastructure, single-threaded C) on one M = 1 layer.
 
 --impl reference runs the oracle as the reference arm on the host cores
@@ -307,7 +308,10 @@ def bench_e2e(stack, M, steps, seed):
     each step copies its x and logits from pinned host memory and reads its
     output back.  The copies run on their own streams, double-buffered, so that
     step j+1's inputs and step j-1's output move while step j computes; the
-    timed region still holds every step's copies."""
+    timed region holds every step's copies.  Sixteen steps (one per input set,
+    two rounds of the 8 layers) are captured once in a CUDA graph and replayed,
+    so the host's per-step stream, event and copy calls leave the timed
+    region; if capture fails the same steps run eagerly and `mode` says so."""
     from bandwidth_bound_fp8_gb300 import moeq
     pool = 16
     xs, lg = make_inputs(pool, M, seed)
@@ -319,46 +323,78 @@ def bench_e2e(stack, M, steps, seed):
     dl = [torch.empty((M, E), dtype=torch.float32, device="cuda") for _ in range(2)]
     dout = [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, E + 1, TOPK))
-    comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot b landed
     ev_done = [torch.cuda.Event() for _ in range(2)]   # the layer that used slot b finished
     ev_out = [torch.cuda.Event() for _ in range(2)]    # slot b's output read back
 
-    def step(j):
-        b, s, l = j % 2, j % pool, j % stack.L
-        with torch.cuda.stream(up):
+    def sequence(comp):
+        """Steps 0 .. pool-1 on stream comp; the copy streams fork from and
+        join back into comp, so the sequence is one unit of stream order."""
+        up.wait_stream(comp)
+        down.wait_stream(comp)
+        for j in range(pool):
+            b, l = j % 2, j % stack.L
+            with torch.cuda.stream(up):
+                if j >= 2:
+                    up.wait_event(ev_done[b])          # slot b's previous inputs are consumed
+                dx[b].copy_(hx[j], non_blocking=True)
+                dl[b].copy_(hl[j], non_blocking=True)
+                ev_in[b].record(up)
+            comp.wait_event(ev_in[b])
             if j >= 2:
-                up.wait_event(ev_done[b])              # slot b's previous inputs are consumed
-            dx[b].copy_(hx[s], non_blocking=True)
-            dl[b].copy_(hl[s], non_blocking=True)
-            ev_in[b].record(up)
-        comp.wait_event(ev_in[b])
-        if j >= 2:
-            comp.wait_event(ev_out[b])                 # slot b's previous output is read back
-        moeq.moeq_moe_layer(dx[b], dl[b], H, I, E, TOPK, stack.gu_q[l], stack.gu_s[l], stack.dn_q[l],
-                            stack.dn_s[l], dout[b], ws, stream=comp)
-        ev_done[b].record(comp)
-        with torch.cuda.stream(down):
-            down.wait_event(ev_done[b])
-            hout[b].copy_(dout[b], non_blocking=True)
-            ev_out[b].record(down)
+                comp.wait_event(ev_out[b])             # slot b's previous output is read back
+            moeq.moeq_moe_layer(dx[b], dl[b], H, I, E, TOPK, stack.gu_q[l], stack.gu_s[l], stack.dn_q[l],
+                                stack.dn_s[l], dout[b], ws, stream=comp)
+            ev_done[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_done[b])
+                hout[b].copy_(dout[b], non_blocking=True)
+                ev_out[b].record(down)
+        comp.wait_stream(up)
+        comp.wait_stream(down)                         # the last output is on the host
 
-    for j in range(5):
-        step(j)
+    # the first calls on the capture's stream happen outside the capture
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        sequence(side)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
+    graph, mode = None, "cuda_graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sequence(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        graph = g
+    except Exception as ex:   # noqa: BLE001 -- reported, the eager steps are timed instead
+        torch.cuda.synchronize()
+        mode = f"eager (graph capture failed: {type(ex).__name__})"
+    comp = torch.cuda.current_stream()
+
+    def run_once():
+        if graph is not None:
+            graph.replay()
+        else:
+            sequence(comp)
+
+    for _ in range(3):
+        run_once()
+    torch.cuda.synchronize()
+    reps = max(1, steps // pool)
     a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
-    for j in range(steps):
-        step(5 + j)
-    comp.wait_stream(down)                             # the last output is on the host
+    for _ in range(reps):
+        run_once()
     e.record(comp)
     torch.cuda.synchronize()
     ms = a.elapsed_time(e)
-    byts = sum(U[(5 + j) % pool] * EXPERT_BYTES for j in range(steps))
+    n = reps * pool
+    byts = reps * sum(U[j] * EXPERT_BYTES for j in range(pool))
     h2d = M * H * 2 + M * E * 4
     d2h = M * H * 2
-    return dict(value=byts / (ms * 1e-3) / 1e9, h2d=h2d, d2h=d2h, ms_per_step=ms / steps)
+    return dict(value=byts / (ms * 1e-3) / 1e9, h2d=h2d, d2h=d2h, ms_per_step=ms / n, mode=mode)
 
 
 def cpu_baseline(stack, M, seed, budget_s=10.0):
@@ -536,7 +572,7 @@ def main():
     if rank == 0:
         e = bench_e2e(stack, args.M, min(args.e2e_steps, args.steps), seed=9000)
         e2e = {"value": round(e["value"], 1), "unit": "GB/s", "h2d_bytes_per_step": e["h2d"],
-               "d2h_bytes_per_step": e["d2h"], "ms_per_step": round(e["ms_per_step"], 5)}
+               "d2h_bytes_per_step": e["d2h"], "ms_per_step": round(e["ms_per_step"], 5), "mode": e["mode"]}
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(stack, 1, seed=9500)
