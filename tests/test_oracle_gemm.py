@@ -1,9 +1,10 @@
 """Pins of the oracle's block-scaled FP8 GEMM.
 
 Pinned to a hand-derived cancelling case (tests/golden/gemm_hand.json), the
-all-ones closed form, single-block isolation, zero-scale blocks, and brute
-force: numpy's float64 matmul over the dequantised operands (a library
-routine) on tiny shapes that span several blocks.
+all-ones closed form, single-block isolation, zero-scale blocks, additivity
+over K groups (catches transposed block scales and a transposed weight
+operand), and brute force: numpy's float64 matmul over the dequantised
+operands (a library routine) on tiny shapes that span several blocks.
 """
 import json
 import os
@@ -80,3 +81,27 @@ def test_gemm_brute_force_numpy(orc):
         y, T = orc.gemm(qa, sa, qw, sw)
         assert np.allclose(y, ref, rtol=0, atol=1e-12 * Tref.max())
         assert np.allclose(T, Tref, rtol=1e-13)
+
+
+def test_gemm_is_the_sum_of_its_k_groups(orc):
+    """y over all of K equals the sum, in group order, of the GEMMs limited to
+    one 128-wide K group each (with that group's activation and block
+    scales), the way a split over K decomposes it.  A scale taken from the
+    wrong group or row block breaks the equality."""
+    rng = np.random.default_rng(7)
+    M, N, K = 2, 384, 640
+    qa = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    qw = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    qa[(qa & 0x7F) == 0x7F] = 0
+    qw[(qw & 0x7F) == 0x7F] = 0
+    sa = rng.uniform(0.01, 2, (M, K // 128)).astype(np.float32)
+    sw = rng.uniform(0.01, 2, (N // 128, K // 128)).astype(np.float32)
+    y, T = orc.gemm(qa, sa, qw, sw)
+    acc, acc_T = np.zeros_like(y), np.zeros_like(T)
+    for g in range(K // 128):
+        k = slice(g * 128, (g + 1) * 128)
+        y_g, T_g = orc.gemm(qa[:, k], sa[:, g:g + 1], qw[:, k], sw[:, g:g + 1])
+        acc += y_g
+        acc_T += T_g
+    assert np.allclose(acc, y, rtol=0, atol=1e-14 * T.max())
+    assert np.allclose(acc_T, T, rtol=1e-14)

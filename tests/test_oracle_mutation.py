@@ -12,6 +12,7 @@ PINS = [
     tc.test_decode_matches_torch_all_codes, tc.test_midpoints_round_to_even,
     tc.test_encode_matches_torch_in_range, tq.test_quant_hand_cases,
     tg.test_gemm_hand_case, tg.test_gemm_brute_force_numpy, tg.test_gemm_single_block_isolation,
+    tg.test_gemm_is_the_sum_of_its_k_groups,
     tr.test_route_hand_cases, tr.test_swiglu_closed_forms, tl.test_layer_brute_force,
 ]
 
