@@ -2,6 +2,7 @@
 // layout and the launches.  Every check
 // runs on the host before anything is launched.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <mutex>
 #include <vector>
@@ -12,7 +13,7 @@ using namespace moeq;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 struct DeviceInfo {
     int ok = 0;
@@ -55,6 +56,33 @@ int mma_min_tokens() {
     }();
     return v;
 }
+
+// The one-token layer kernel serves M = 1 layers on the CUDA cores unless
+// MOEQ_TOKEN_KERNEL=0 (then the persistent engine does, as it does for every
+// other M); MOEQ_PDL=0 launches it without programmatic dependent launch.
+// Both read once.
+bool env_flag(const char* name, bool dflt) {
+    const char* e = std::getenv(name);
+    if (!e || !*e) return dflt;
+    return std::atoi(e) != 0;
+}
+bool token_kernel_enabled() {
+    static const bool v = env_flag("MOEQ_TOKEN_KERNEL", true);
+    return v;
+}
+bool pdl_enabled() {
+    static const bool v = env_flag("MOEQ_PDL", true);
+    return v;
+}
+
+// The one-token kernel reads weights before it waits for the kernel ahead of
+// it on the stream (programmatic dependent launch).  This library's own
+// weight writers (moeq_quant_weight, moeq_pack_weight) note their stream
+// here; a layer call that directly follows one on the same stream launches
+// without programmatic dependence, so it reads the weights only after the
+// writer has finished.
+std::atomic<uintptr_t> g_weight_write_stream{0};
+inline uintptr_t stream_key(void* s) { return s ? reinterpret_cast<uintptr_t>(s) : uintptr_t(1); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -103,7 +131,7 @@ StreamWs stream_ws_layout(size_t base, const int* aq_rows, const int* aq_k, int 
 }
 
 struct LayerWs {
-    size_t plan, h, y, dc;
+    size_t plan, h, y, dc, tok_tickets;
     StreamWs s;
 };
 
@@ -115,7 +143,11 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.y = align_up(l.h + sizeof(float) * static_cast<size_t>(mp) * I, 256);
     // one token: down by K group's sums per (pair, K group of down, column)
     l.dc = align_up(l.y + sizeof(float) * static_cast<size_t>(mp) * H, 256);
-    const size_t after = l.dc + (M == 1 ? sizeof(float) * static_cast<size_t>(mp) * (I / 128) * H : 0);
+    // one token: the token kernel's partials share that area; its arrival
+    // counts (one per 256 output rows) and completion count follow
+    l.tok_tickets = align_up(l.dc + (M == 1 ? sizeof(float) * static_cast<size_t>(mp) * (I / 128) * H : 0), 256);
+    const size_t after =
+        l.tok_tickets + (M == 1 ? sizeof(int) * (static_cast<size_t>((H + 255) / 256) + kGqUnits) : 0);
     // tickets of the layer's lists: M == 1 uses the first two (whole lists),
     // M > 1 all six (shared, half A, half B of each kind)
     const int rbmax = mu * ((H > I ? H : I) / 128);
@@ -273,6 +305,7 @@ moeq_status moeq_quant_weight(const float* w, int E, int N, int K, uint8_t* q, f
     if (N <= 0 || K <= 0 || N % 128 || K % 128 || N / 128 > 65535 || K / 128 > 65535)
         return MOEQ_ERR_UNSUPPORTED_SHAPE;
     if (!current_device().ok) return MOEQ_ERR_DEVICE;
+    g_weight_write_stream.store(stream_key(stream));
     return cuda_status(launch_quant_weight(w, E, N, K, q, s, as_stream(stream)));
 }
 
@@ -282,6 +315,7 @@ moeq_status moeq_pack_weight(const uint8_t* q_rows, int E, int N, int K, uint8_t
     if (N <= 0 || K <= 0 || N % 128 || K % 128 || N / 128 > 65535 || K / 128 > 65535)
         return MOEQ_ERR_UNSUPPORTED_SHAPE;
     if (!current_device().ok) return MOEQ_ERR_DEVICE;
+    g_weight_write_stream.store(stream_key(stream));
     return cuda_status(launch_pack_weight(q_rows, E, N, K, q_tiles, as_stream(stream)));
 }
 
@@ -495,12 +529,17 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
 
 moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int I, int E_routed, int top_k,
                            const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d, const float* s_d, void* out,
-                           const moeq_route_plan* plan_opt, float* h_opt, float* y_opt, void* const* events_opt,
-                           void* ws, size_t ws_bytes, void* stream) {
+                           const moeq_route_plan* plan_opt, float* h_opt, float* y_opt, uint8_t* q_x_opt,
+                           float* s_x_opt, uint8_t* q_h_opt, float* s_h_opt, void* const* events_opt, void* ws,
+                           size_t ws_bytes, void* stream) {
     if (!x || !logits || !w_gu || !s_gu || !w_d || !s_d || !out) return MOEQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w_gu) || !aligned16(w_d) || !aligned16(out) || !aligned4(s_gu) || !aligned4(s_d))
         return MOEQ_ERR_INVALID_ARG;
     if ((h_opt && !aligned16(h_opt)) || (y_opt && !aligned16(y_opt))) return MOEQ_ERR_INVALID_ARG;
+    if ((q_x_opt == nullptr) != (s_x_opt == nullptr) || (q_h_opt == nullptr) != (s_h_opt == nullptr))
+        return MOEQ_ERR_INVALID_ARG;
+    if ((q_x_opt && (!aligned16(q_x_opt) || !aligned4(s_x_opt))) || (q_h_opt && (!aligned16(q_h_opt) || !aligned4(s_h_opt))))
+        return MOEQ_ERR_INVALID_ARG;
     if (plan_opt && !plan_ok(plan_opt)) return MOEQ_ERR_INVALID_ARG;
     if (!route_args_ok(M, E_routed, top_k)) return MOEQ_ERR_INVALID_ARG;
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K || I > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
@@ -518,6 +557,46 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     float* h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
     float* y = y_opt ? y_opt : reinterpret_cast<float*>(base + l.y);
     const int mu = moeq_max_uniq(M, E_routed, top_k), mp = moeq_max_pairs(M, top_k);
+    cudaStream_t st = as_stream(stream);
+
+    // One token on the CUDA cores (no per-pair y asked for): the one-token
+    // kernel, which needs no co-resident grid and no cross-CTA wait.
+    if (M == 1 && M < mma_min_tokens() && !y_opt && token_kernel_enabled() && top_k <= kTokenMaxTopK &&
+        H <= kTokenMaxH && H % 256 == 0 && (top_k + 1) * (I / 128) <= kTokenMaxCols) {
+        TokenArgs t = {};
+        t.x = static_cast<const __nv_bfloat16*>(x);
+        t.logits = logits;
+        t.H = H;
+        t.I = I;
+        t.KB = H / 128;
+        t.RB = I / 128;
+        t.E_routed = E_routed;
+        t.top_k = top_k;
+        t.ncols = (top_k + 1) * (I / 128);
+        t.w_gu = w_gu;
+        t.s_gu = s_gu;
+        t.w_d = w_d;
+        t.s_d = s_d;
+        t.out = static_cast<__nv_bfloat16*>(out);
+        t.plan = plan;
+        t.h = h;
+        t.q_x = q_x_opt;
+        t.s_x = s_x_opt;
+        t.q_h = q_h_opt;
+        t.s_h = s_h_opt;
+        t.status = reinterpret_cast<int*>(base + kOffStatus);
+        t.tickets = reinterpret_cast<int*>(base + l.tok_tickets);
+        t.gq = t.tickets + H / 256;
+        t.part = reinterpret_cast<float*>(base + l.dc);
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        uintptr_t key = stream_key(stream);
+        const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+        if (launch_token(t, dev.sms, pdl_enabled() && !after_weight_write, st) != cudaSuccess) return MOEQ_ERR_CUDA;
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        return MOEQ_OK;
+    }
 
     StreamArgs a = {};
     Operand& g = a.op[kKindGU];
@@ -533,6 +612,8 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     g.out = h;
     g.out_ld = I;
     g.quant_input = 1;
+    g.qdump = q_x_opt;
+    g.sdump = s_x_opt;
     Operand& d = a.op[kKindDN];
     d.w = w_d;
     d.sw = s_d;
@@ -556,7 +637,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     // each CTA quantises all of x for itself, and down by K group takes the
     // h group the CTA finished itself from shared memory.
     const bool one_block = dp_blocks_per_cta_host(static_cast<long long>(mu) * (I / 128), dev.sms) == 1;
-    a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block;
+    a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block && !q_x_opt;
     a.hloc = a.dc && one_block;
     a.swb = a.xloc && aligned16(s_gu) && (H / 128) % 4 == 0;
     if (M == 1 || M >= mma_min_tokens()) {
@@ -603,10 +684,11 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     a.fused_combine = 1;
     a.out_bf16 = static_cast<__nv_bfloat16*>(out);
     a.h_to_dn = 1;
+    a.qh_dump = q_h_opt;
+    a.sh_dump = s_h_opt;
     fill_ws(a, ws, l.s, dev.sms);
     a.dc_part = reinterpret_cast<float*>(base + l.dc);
 
-    cudaStream_t st = as_stream(stream);
     if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
         return MOEQ_ERR_CUDA;
     if (launch_stream(a, dev.sms, true, st) != cudaSuccess) return MOEQ_ERR_CUDA;

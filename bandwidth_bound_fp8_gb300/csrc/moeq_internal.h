@@ -77,6 +77,8 @@ struct StreamArgs {
     int* done;
     int* a_cnt;               // CTAs done with the input quantisation phase (epoch * grid when all are)
     int h_to_dn;              // layer: the gate_up finish also quantises h into op[down].aq/as
+    uint8_t* qh_dump;         // layer, optional: h's codes [max_pairs, I] ...
+    float* sh_dump;           // ... and scales [max_pairs, I/128]
     int mma;                  // 1: tcgen05 path (activation codes kept as E4M3 bytes in aq)
     int* tickets[kMaxLists];
     float* partials;          // per list: 2 * grid slots of kMaxTokens * 256 floats
@@ -108,6 +110,39 @@ inline int dp_blocks_per_cta_host(long long n_rb, long long G) {
 }
 // x fits one activation slot (decoded fp32 codes of one token)
 constexpr int kXLocalMaxK = 6144;
+
+// The one-token layer kernel (moeq_token.cu): x fits its shared memory, the
+// routed picks plus the shared expert fit its per-slot sums.
+constexpr int kTokenMaxH = 6144;
+constexpr int kTokenMaxTopK = 8;
+constexpr int kTokenMaxCols = 152;   // (top_k + 1) * I/128 columns at most
+
+struct TokenArgs {
+    const __nv_bfloat16* x;      // [H]
+    const float* logits;         // [E_routed]
+    int H, I, KB, RB;            // KB = H/128 (gate_up K groups, down row blocks), RB = I/128
+    int E_routed, top_k;
+    int ncols;                   // (top_k + 1) * RB columns (expert slot, down K group)
+    const uint8_t* w_gu;         // tile-major [E_routed + 1, 2I, H]
+    const float* s_gu;           // [E_routed + 1, 2I/128, H/128]
+    const uint8_t* w_d;          // tile-major [E_routed + 1, H, I]
+    const float* s_d;            // [E_routed + 1, H/128, I/128]
+    __nv_bfloat16* out;          // [H]
+    moeq_route_plan plan;        // written by CTA 0
+    float* h;                    // [top_k + 1, I]
+    uint8_t* q_x;                // optional [H] and [H/128]: x's codes and scales
+    float* s_x;
+    uint8_t* q_h;                // optional [top_k + 1, I] and [top_k + 1, I/128]: h's codes and scales
+    float* s_h;
+    int* status;
+    int* tickets;                // [H/256] arrivals per output unit, zero between launches
+    int* gq;                     // kGqUnits ints, zero between launches
+    float* part;                 // [H/256][16][ncols][16] down partials
+};
+// Completion state of the one-token kernel (ints): CTAs finished.
+constexpr int kGqCtas = 0, kGqUnits = 4;
+
+cudaError_t launch_token(const TokenArgs& args, int grid, bool pdl, cudaStream_t stream);
 
 size_t stream_partials_floats(int grid);
 cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);

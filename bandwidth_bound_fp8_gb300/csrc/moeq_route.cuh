@@ -44,14 +44,18 @@ __device__ __forceinline__ float route_key_value(uint32_t k) {
 // each round takes the warp maximum of the key, then the smallest expert id
 // holding it (ties to the lower id), with two warp reductions.
 template <int NPER>
-__device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int E, int k, int lane, int* ids,
-                                                float* vals) {
-    uint32_t key[NPER];
+__device__ __forceinline__ void route_load_keys(const float* __restrict__ l, int E, int lane, uint32_t (&key)[NPER]) {
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
         key[i] = e < E ? route_key(__ldcg(l + e)) : 0u;
     }
+}
+
+// The selection itself, on keys already loaded by route_load_keys.
+template <int NPER>
+__device__ __forceinline__ void route_topk_keys(const uint32_t (&key)[NPER], int E, int k, int lane, int* ids,
+                                                float* vals) {
     uint32_t taken = 0;
     for (int j = 0; j < k; ++j) {
         uint32_t bk = 0;
@@ -74,6 +78,14 @@ __device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int
         }
     }
     __syncwarp();
+}
+
+template <int NPER>
+__device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int E, int k, int lane, int* ids,
+                                                float* vals) {
+    uint32_t key[NPER];
+    route_load_keys<NPER>(l, E, lane, key);
+    route_topk_keys<NPER>(key, E, k, lane, ids, vals);
 }
 
 // Computes the plan with NT threads (tid in [0, NT)); `sync` is a barrier

@@ -657,6 +657,10 @@ static __device__ __noinline__ void helper_epilogue(const StreamArgs& a, SmemTai
                 else
                     *reinterpret_cast<float4*>(dn.aq + (p * dn.KB + m.rb) * kGroup + act_pos(4 * lane)) = dec;
                 if (lane == 0) dn.as[p * dn.KB + m.rb] = sc;
+                if (a.qh_dump) {
+                    *reinterpret_cast<uint32_t*>(a.qh_dump + p * dn.K + m.rb * kGroup + 4 * lane) = hc;
+                    if (lane == 0) a.sh_dump[p * dn.KB + m.rb] = sc;
+                }
             }
         }
     } else if (m.valid) {

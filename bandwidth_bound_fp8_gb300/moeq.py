@@ -86,7 +86,8 @@ def load(path: str = LIB_PATH):
         "moeq_expert_gemm_down_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _i,
                                                _vp, _vp, _vp, _vp, _vp]),
         "moeq_moe_layer": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
-                                ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _sz, _vp]),
+                                ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                _sz, _vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -264,7 +265,8 @@ def moeq_combine(y, N, plan: RoutePlan, M, top_k, out, stream=None) -> None:
 
 
 def moeq_moe_layer(x, logits, H, I, E_routed, top_k, w_gu, s_gu, w_d, s_d, out, ws: Workspace,
-                   plan: RoutePlan | None = None, h=None, y=None, events=None, stream=None) -> None:
+                   plan: RoutePlan | None = None, h=None, y=None, q_x=None, s_x=None, q_h=None, s_h=None,
+                   events=None, stream=None) -> None:
     M = x.shape[0]
     ev = None
     if events is not None:
@@ -276,5 +278,5 @@ def moeq_moe_layer(x, logits, H, I, E_routed, top_k, w_gu, s_gu, w_d, s_d, out, 
         ev = (ctypes.c_void_p * 2)(*handles)
     _check("moeq_moe_layer", load().moeq_moe_layer(
         _p(x), _p(logits), M, H, I, E_routed, top_k, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(out),
-        ctypes.byref(plan.c) if plan is not None else None, _p(h), _p(y), ev, ws.ptr, ws.nbytes,
-        _stream(stream)))
+        ctypes.byref(plan.c) if plan is not None else None, _p(h), _p(y), _p(q_x), _p(s_x), _p(q_h), _p(s_h),
+        ev, ws.ptr, ws.nbytes, _stream(stream)))

@@ -105,7 +105,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -117,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
         except Exception:
@@ -152,8 +152,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-KERNEL_SOURCES = ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_device.cuh", "moeq_route.cuh",
-                  "moeq_internal.h")
+KERNEL_SOURCES = ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_token.cu", "moeq_device.cuh",
+                  "moeq_route.cuh", "moeq_internal.h")
 
 
 def code_hash(texts):
@@ -258,7 +258,8 @@ def make_events(steps, events_every):
 
 def run_steps(stack, xs, lg, M, ws, outs, steps, start, events_every=0, recs=()):
     """Launch `steps` layer forwards, passing recs[i // events_every] to every
-    events_every-th step for per-stage timing."""
+    events_every-th step for per-launch timing (events_every = 0: none, so
+    consecutive launches stay back to back)."""
     from bandwidth_bound_fp8_gb300 import moeq
     n = xs.shape[0]
     for i in range(steps):
@@ -269,7 +270,14 @@ def run_steps(stack, xs, lg, M, ws, outs, steps, start, events_every=0, recs=())
                             stack.dn_s[l], outs[j % 2], ws, events=ev)
 
 
-def bench_M(stack, M, steps, warmup, ws_world, seed, events_every=8):
+def bench_M(stack, M, steps, warmup, ws_world, seed, isolated=64):
+    """Timed region: `steps` layer calls back to back on one stream, events
+    only at its two ends.  A step is exactly one launch of the layer kernel,
+    so the kernel's average launch duration is the region's time / steps
+    (consecutive launches overlap by programmatic dependent launch: the next
+    layer streams its shared expert while this one finishes).  After the
+    region, `isolated` more launches are timed one by one with events on
+    their own stream, which breaks that overlap: the single-launch figure."""
     from bandwidth_bound_fp8_gb300 import moeq
     pool = max(16, min(256, steps + warmup))
     xs, lg = make_inputs(pool, M, seed)
@@ -277,14 +285,13 @@ def bench_M(stack, M, steps, warmup, ws_world, seed, events_every=8):
     ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, E + 1, TOPK))
     outs = [torch.empty((M, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     run_steps(stack, xs, lg, M, ws, outs, warmup, 0)
-    recs = make_events(steps, events_every)
     torch.cuda.synchronize()
     barrier(ws_world)
     torch.cuda.synchronize()
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0e.record()
-    run_steps(stack, xs, lg, M, ws, outs, steps, warmup, events_every, recs)
+    run_steps(stack, xs, lg, M, ws, outs, steps, warmup)
     t1e.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -293,13 +300,15 @@ def bench_M(stack, M, steps, warmup, ws_world, seed, events_every=8):
     if moeq.moeq_read_device_status(ws.t, ws.nbytes) != 0:
         raise RuntimeError("device status word set during the bench")
     byts = sum(U[(warmup + i) % pool] * EXPERT_BYTES for i in range(steps))
-    k_ms, k_bytes = [], []
-    for k, ev in enumerate(recs):
-        k_ms.append(ev[0].elapsed_time(ev[1]))
-        k_bytes.append(U[(warmup + k * events_every) % pool] * EXPERT_BYTES)
+    recs = make_events(isolated, 1)
+    run_steps(stack, xs, lg, M, ws, outs, isolated, warmup + steps, 1, recs)
+    torch.cuda.synchronize()
+    iso = [ev[0].elapsed_time(ev[1]) for ev in recs]
+    iso_bytes = [U[(warmup + steps + k) % pool] * EXPERT_BYTES for k in range(isolated)]
     return dict(ms=ms, bytes=byts, steps=steps, U_mean=float(np.mean([U[(warmup + i) % pool] for i in range(steps)])),
-                kernel_ms=float(np.mean(k_ms)) if k_ms else None,
-                kernel_bytes=float(np.mean(k_bytes)) if k_bytes else None, wall=(wall0, wall1),
+                kernel_ms=ms / steps, kernel_bytes=byts / steps,
+                isolated_ms=float(np.median(iso)) if iso else None,
+                isolated_bytes=float(np.mean(iso_bytes)) if iso else None, wall=(wall0, wall1),
                 xs=xs, lg=lg, U=U, ws=ws)
 
 
@@ -464,12 +473,18 @@ def reference_arm(args, ws, rank):
         byts += r.route.n_uniq * ebytes
     dt = time.perf_counter() - t0
     v = byts / dt / 1e9
-    sample = (f"oracle MoE layer at M={M}, 256 experts top-{TOPK} + shared, shape reduced to hidden {Hs}, "
-              f"intermediate {Is} so that {total} steps fit ~{budget:.0f} s")
+    full = (Hs, Is) == (H, I)
+    if full:
+        sample = (f"oracle MoE layer at M={M}, 256 experts top-{TOPK} + shared, the full layer shape (hidden {Hs}, "
+                  f"intermediate {Is}); {total} steps fit ~{budget:.0f} s")
+    else:
+        sample = (f"oracle MoE layer at M={M}, 256 experts top-{TOPK} + shared, shape reduced to hidden {Hs}, "
+                  f"intermediate {Is} so that {total} steps fit ~{budget:.0f} s")
+    workload = f"moe_layer_m{M}_h6144_i2048_e256_top8_shared1" + ("" if full else f" (sample: h{Hs}_i{Is})")
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"moe_layer_m{M}_h6144_i2048_e256_top8_shared1 (sample: h{Hs}_i{Is})", "M": M},
+            "config": {"workload": workload, "M": M},
             "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -552,10 +567,15 @@ def main():
 
     k_ms = r["kernel_ms"]
     achieved = r["kernel_bytes"] / (k_ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": "stream_kernel (whole MoE layer: route, gate_up+SwiGLU, down, combine)",
+    kname = ("token_kernel (one-token MoE layer: route, gate_up+SwiGLU, down, combine)" if args.M == 1 else
+             "stream_kernel (whole MoE layer: route, gate_up+SwiGLU, down, combine)")
+    roof = {"bound": "hbm", "kernel": kname,
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy), of {peak_kind}",
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": ncu_traffic("layer", args.M),
-            "algorithmic_bytes_per_launch": r["kernel_bytes"], "ms_per_launch": round(k_ms, 5)}
+            "algorithmic_bytes_per_launch": r["kernel_bytes"], "ms_per_launch": round(k_ms, 5),
+            "launch_duration": "timed region / launches (one launch per step, launches back to back)",
+            "isolated_launch_ms": round(r["isolated_ms"], 5),
+            "isolated_frac": round(r["isolated_bytes"] / (r["isolated_ms"] * 1e-3) / 1e9 / peak, 4)}
 
     sweep = {}
     if not args.no_sweep and rank == 0:
@@ -566,7 +586,7 @@ def main():
             sweep[f"M{M}"] = {"us_per_layer": round(us, 2), "weight_GBps": round(gbs, 1),
                               "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8TBps": round(gbs / 8000, 4),
                               "U_mean": rr["U_mean"],
-                              "kernel_us": round(rr["kernel_ms"] * 1e3, 2)}
+                              "isolated_launch_us": round(rr["isolated_ms"] * 1e3, 2)}
             del rr
     e2e = None
     if rank == 0:
@@ -591,6 +611,7 @@ def main():
             "us_per_layer": round(ms * 1e3 / args.steps, 3),
             "frac_of_8TBps": round(value / world / 8000, 4),
             "kernel_us": round(r["kernel_ms"] * 1e3, 3),
+            "isolated_launch_us": round(r["isolated_ms"] * 1e3, 3),
             "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
             "gpu_launches": args.steps, "sweep": sweep,
         }

@@ -263,16 +263,28 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
 /* ------------------------------------------------------------------------ */
 /* moeq_moe_layer -- one MoE FFN layer for M tokens, in ONE kernel:         */
 /*   route -> [quant x + gate_up + SwiGLU] -> [quant h + down] -> combine   */
-/*   One persistent CTA per SM (cooperative launch): every CTA routes for   */
-/*   itself while CTAs whose first blocks are the shared expert's already   */
-/*   stream them, and gate_up and down stream back to back.  M > 1, or a   */
-/*   call that asks for y: down waits per expert for its h, and the         */
-/*   combine runs in the down epilogue.  M == 1 without y (CUDA-core path,  */
-/*   H/128 even): the CTA that finished gate_up row block kb of a pair      */
-/*   streams down's K group kb for every output row block ("down by K       */
-/*   group", no wait on other CTAs' h), and the launch ends with a combine  */
-/*   over the K groups' fp32 sums in a fixed order.  Both give out within   */
-/*   the same bound; their fp32 rounding orders differ.                     */
+/*   (GLM-5.2 x10: bandwidth model -- a decode layer reads its top-8        */
+/*   experts plus the shared one; §1 and §8c -- live FP8 quantisation of    */
+/*   the activations in front of each GEMM; §4 -- fused into it; §1 --      */
+/*   split-K so that every SM streams; §5-§6 -- tokens verified together     */
+/*   read each expert once.)                                                */
+/*   M == 1 on the CUDA cores, y not asked for, top_k <= 8, H <= 6144 and   */
+/*   H % 256 == 0: the one-token kernel.  One CTA per (expert, 128-wide K   */
+/*   group of down): it streams that h group's gate and up rows, forms and  */
+/*   quantises the group itself, and streams down's K group against every  */
+/*   output row; the fp32 partials of each 256 output rows are summed, and  */
+/*   the bf16 output formed, by the CTA whose contribution arrives last     */
+/*   (atomic ticket), so no CTA waits for another.  It is launched with     */
+/*   programmatic dependent launch: the next kernel on the stream may start */
+/*   as its CTAs finish, and waits (griddepcontrol.wait) before it reads    */
+/*   anything this one writes.                                              */
+/*   Otherwise: one persistent CTA per SM (cooperative launch).  Every CTA  */
+/*   routes for itself while CTAs whose first blocks are the shared         */
+/*   expert's already stream them; down waits per expert for its h, and the */
+/*   combine runs in the down epilogue (M == 1 without y on the persistent  */
+/*   engine streams down by K group instead).                               */
+/*   All paths give out within the same bound; their fp32 rounding orders   */
+/*   differ.                                                                */
 /*   x      [M, H] bf16; logits [M, E_routed] fp32                          */
 /*   w_gu/s_gu, w_d/s_d: E_routed + 1 experts (tile-major codes), the       */
 /*           shared expert last                                             */
@@ -281,6 +293,12 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
 /*           caller buffers that receive the plan and the intermediates     */
 /*           (NULL: kept in the workspace; a non-NULL y_opt selects the     */
 /*           row-block down path, which is the one that forms y)            */
+/*   q_x_opt [M, H] u8 + s_x_opt [M, H/128] f32: optional, both or neither: */
+/*           the codes and scales of x's live quantisation (a2)             */
+/*   q_h_opt [max_pairs, I] u8 + s_h_opt [max_pairs, I/128] f32: optional,  */
+/*           both or neither: the codes and scales of h's live quantisation */
+/*           (a5), the ones the down GEMM multiplies, h being the layer's   */
+/*           own fp32 h (h_opt)                                             */
 /*   events_opt: NULL, or 2 cudaEvent_t recorded on `stream` right before   */
 /*           and right after the layer's kernel, for the caller's timing    */
 /* A workspace serves one layer call at a time: consecutive calls on one    */
@@ -291,7 +309,10 @@ moeq_status moeq_moe_layer(const void* x, const float* logits,
                            const uint8_t* w_gu, const float* s_gu,
                            const uint8_t* w_d, const float* s_d,
                            void* out, const moeq_route_plan* plan_opt,
-                           float* h_opt, float* y_opt, void* const* events_opt,
+                           float* h_opt, float* y_opt,
+                           uint8_t* q_x_opt, float* s_x_opt,
+                           uint8_t* q_h_opt, float* s_h_opt,
+                           void* const* events_opt,
                            void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     from bandwidth_bound_fp8_gb300 import moeq
-    assert moeq.moeq_abi_version() == 1
+    assert moeq.moeq_abi_version() == 2
     for s in range(7):
         assert moeq.status_string(s)
     assert moeq.status_string(99) == "unknown status"
@@ -98,8 +98,10 @@ def test_argument_validation_without_device(lib):
     # down: N not a multiple of 128
     assert lib.moeq_expert_gemm_down(p, 0, 256, 100, p, p, 1, p, p, p, 1, 1, p, None, None, p, 1 << 16, None) == 2
     # layer: k > E, then M = 0
-    assert lib.moeq_moe_layer(p, p, 1, 256, 128, 4, 8, p, p, p, p, p, None, None, None, None, p, 1 << 16, None) == 1
-    assert lib.moeq_moe_layer(p, p, 0, 256, 128, 8, 2, p, p, p, p, p, None, None, None, None, p, 1 << 16, None) == 1
+    assert lib.moeq_moe_layer(p, p, 1, 256, 128, 4, 8, p, p, p, p, p, None, None, None, None, None, None, None,
+                              None, p, 1 << 16, None) == 1
+    assert lib.moeq_moe_layer(p, p, 0, 256, 128, 8, 2, p, p, p, p, p, None, None, None, None, None, None, None,
+                              None, p, 1 << 16, None) == 1
     # combine with top_k > 0 but no weights
     plan = __import__("bandwidth_bound_fp8_gb300.moeq", fromlist=["x"]).moeq_route_plan()
     plan.pair_of = p

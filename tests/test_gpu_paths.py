@@ -8,6 +8,10 @@ in child processes:
     experts, ragged K tails, split-K at every size);
   * with it at 17, every launch runs on the CUDA cores (16-token experts on
     the shared-memory accumulation mode).
+One token on the CUDA cores runs the one-token kernel unless
+MOEQ_TOKEN_KERNEL=0, which hands it to the persistent engine (down by K
+group, or row-block down when y is asked for); a third child re-runs the
+one-token layer tests, the full-size one included, on that path.
 The children use the same oracle comparisons and tolerances as the default
 run."""
 import os
@@ -29,3 +33,11 @@ def test_parity_with_forced_path(crossover):
            "-k", "not full_size and not full_m1 and not multi_token_sampled"]
     r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, f"crossover {crossover}:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"
+
+
+def test_parity_one_token_on_the_persistent_engine():
+    env = dict(os.environ, MOEQ_TOKEN_KERNEL="0")
+    cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+           os.path.join(HERE, "test_gpu_layer.py"), "-k", "m1 or reduced"]
+    r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, f"engine one-token path:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"

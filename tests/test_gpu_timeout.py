@@ -7,8 +7,14 @@ in the workspace header (byte offset 16) is set far below anything the
 launch can reach, so the chunk-preparing warps of every CTA give up after
 the limit.  It then checks the status, re-initialises the workspace and
 checks that a normal call on the same context still matches the oracle.
-A second case does the same to the count that the one-token layer's final
-combine waits for."""
+A second case does the same to the count that the persistent engine's
+one-token layer waits for before its final combine (the engine serves one
+token when MOEQ_TOKEN_KERNEL=0; by default the one-token kernel does, which
+has no wait on another CTA at all), in a child process with that setting."""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -50,9 +56,18 @@ DC_CNT_INT_OFFSET = 20 // 4  # int32 index of the down-by-K-group count
 
 
 def test_layer_combine_wait_reports_timeout_and_the_context_survives(orc):
-    """One token without y: the combine after down by K group waits for every
-    CTA's count.  With the count set out of reach that wait gives up, the
-    status says so, and after a re-initialisation the layer is correct."""
+    """One token without y on the persistent engine: the combine after down by
+    K group waits for every CTA's count.  With the count set out of reach that
+    wait gives up, the status says so, and after a re-initialisation the layer
+    is correct."""
+    if os.environ.get("MOEQ_TOKEN_KERNEL") != "0":
+        env = dict(os.environ, MOEQ_TOKEN_KERNEL="0")
+        here = os.path.dirname(os.path.abspath(__file__))
+        cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+               os.path.abspath(__file__), "-k", "combine_wait"]
+        r = subprocess.run(cmd, env=env, cwd=os.path.dirname(here), capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, f"{r.stdout[-3000:]}\n{r.stderr[-2000:]}"
+        return
     from test_gpu_layer import Layer, check_layer
     from bandwidth_bound_fp8_gb300 import moeq
     E, H, I, k = 8, 512, 256, 2
