@@ -562,7 +562,7 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     // One token on the CUDA cores (no per-pair y asked for): the one-token
     // kernel, which needs no co-resident grid and no cross-CTA wait.
     if (M == 1 && M < mma_min_tokens() && !y_opt && token_kernel_enabled() && top_k <= kTokenMaxTopK &&
-        H <= kTokenMaxH && H % 256 == 0 && (top_k + 1) * (I / 128) <= kTokenMaxCols) {
+        H <= kTokenMaxH && H % 256 == 0) {
         TokenArgs t = {};
         t.x = static_cast<const __nv_bfloat16*>(x);
         t.logits = logits;

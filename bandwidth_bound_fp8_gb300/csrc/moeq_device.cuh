@@ -56,6 +56,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete sleeps (up to
+// kSleepHintNs, woken early when the phase completes) instead of returning at
+// once: a waiting warp takes no issue slots from the warps that work.
+constexpr uint32_t kSleepHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepHintNs)
+        : "memory");
+    return done != 0;
+}
+
+// Sleeping wait for the phase with the given parity; gives up (returns
+// false) when *abort becomes non-zero or after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {

@@ -115,7 +115,6 @@ constexpr int kXLocalMaxK = 6144;
 // routed picks plus the shared expert fit its per-slot sums.
 constexpr int kTokenMaxH = 6144;
 constexpr int kTokenMaxTopK = 8;
-constexpr int kTokenMaxCols = 152;   // (top_k + 1) * I/128 columns at most
 
 struct TokenArgs {
     const __nv_bfloat16* x;      // [H]

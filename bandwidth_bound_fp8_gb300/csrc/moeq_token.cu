@@ -53,9 +53,7 @@ constexpr int kStageBytes = 2 * kTile;
 constexpr int kStages = 4;
 constexpr int kMaxKB = kTokenMaxH / 128;       // K groups of x
 constexpr int kMaxUnits = kTokenMaxH / 256;    // 256-row output units of down
-constexpr int kMaxSlots = kTokenMaxTopK + 1;   // routed picks + the shared expert
 constexpr int kParts = kCW;                    // a unit's rows split by consumer warp (16 rows each)
-constexpr int kCombineWarps = kCW;             // warps of a CTA that sum parts (one buffer each)
 
 struct Smem {
     alignas(16) float xdec[kTokenMaxH];   // decoded x codes, each group in the consumer layout
@@ -65,27 +63,22 @@ struct Smem {
     float gsum[256];                   // the column's gate (0..127) and up (128..255) sums
     alignas(16) float hdec[128];       // decoded h codes (consumer layout) ...
     float hs;                          // ... and their scale
-    alignas(16) float comb[kCombineWarps][kMaxSlots][16];   // per summing warp: per-slot sums of one part's rows
     int topk_id[kTokenMaxTopK];
     float topk_w[kTokenMaxTopK];
     int uniq[kTokenMaxTopK];           // routed experts, ascending
     int pick_rank[kTokenMaxTopK];      // position of pick j in uniq
+    int slot_pick[kTokenMaxTopK];      // the pick at position s of uniq
     float rvals[kTokenMaxTopK];        // picked logits (routing scratch)
     int wdone[kCW];                    // down partials stored, per consumer warp (monotonic)
     int abort_flag;
     uint64_t full[kStages], empty[kStages];
     uint64_t plan_bar;
-    uint64_t comb_bar[kCombineWarps];   // one per summing warp: its part's bulk copy landed
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(offsetof(Smem, xdec) % 16 == 0 && offsetof(Smem, hdec) % 16 == 0 && offsetof(Smem, comb) % 16 == 0,
-              "float4 accesses");
+static_assert(offsetof(Smem, xdec) % 16 == 0 && offsetof(Smem, hdec) % 16 == 0, "float4 accesses");
 static_assert((static_cast<size_t>(kStages) * kStageBytes) % 1024 == 0, "the tail starts 1024-aligned");
-static_assert(offsetof(Smem, xdec) == 0, "the x buffer follows the stage ring");
-static_assert(kCombineWarps * kTokenMaxCols * 64 <= kStages * kStageBytes + sizeof(float) * kTokenMaxH,
-              "the sums' buffers fit the stage ring and the x buffer");
 
 __device__ __forceinline__ void consumer_sync() { named_sync(1, kConsumers); }
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
@@ -93,7 +86,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Smem& sm, int* status) {
-    if (mbar_wait_bounded(bar, parity, &sm.abort_flag)) return true;
+    if (mbar_wait_sleep_bounded(bar, parity, &sm.abort_flag)) return true;
     record_error(status, MOEQ_ERR_TIMEOUT);
     sm.abort_flag = 1;
     return false;
@@ -212,6 +205,7 @@ __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int
         sm.topk_w[lane] = w;
         sm.uniq[rank] = id;
         sm.pick_rank[lane] = rank;
+        sm.slot_pick[rank] = lane;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.plan_bar);
@@ -398,7 +392,9 @@ __device__ bool consume_column(const TokenArgs& a, Smem& sm, const uint8_t* stag
     consumer_sync();
     float2 hv[8];
     load_act(sm.hdec, l8, hv);
-    const float sa = sm.hs;
+    // the routing weight of this column's expert (1 for the shared one) goes
+    // into its partials, so that a unit's output is the plain sum of them
+    const float sa = sm.hs * (col.g == 0 ? 1.0f : sm.topk_w[sm.slot_pick[col.g - 1]]);
     const uint64_t keep = l2_evict_last_policy();
     const int nu = a.KB / 2;
     for (int i = 0; i < nu; ++i, ++it) {
@@ -430,83 +426,66 @@ __device__ bool consume_column(const TokenArgs& a, Smem& sm, const uint8_t* stag
 
 // ------------------------------------------------------------------ combine
 // One part of a completed unit: rows (2u + w/8)*128 + (w%8)*16 .. +15 of the
-// output.  One bulk copy brings the part's ncols x 16 partials (9 KiB at the
-// layer's shapes) into this warp's buffer; the slots' (column groups') sums
-// over their RB columns are formed in a fixed order (each lane one row and
-// every other K group, then the two halves), and lanes 0..15 form out =
-// y_shared + sum_j w_j * y_pick(j) in pick order, rounded once to bf16.
-__device__ void combine_part(const TokenArgs& a, Smem& sm, uint8_t* buf, uint64_t* bar, uint32_t parity, int u, int w,
-                             int warp, int lane) {
-    const uint32_t bytes = static_cast<uint32_t>(a.ncols) * 64u;
-    if (lane == 0) {
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(buf, a.part + (static_cast<size_t>(u) * kParts + w) * a.ncols * 16, bytes, bar, l2_evict_first_policy());
-    }
-    const bool ok = wait_or_abort(bar, parity, sm, a.status);
-    if (!__all_sync(0xffffffffu, ok)) return;
-    // lane (row r, half h) sums row r of every slot over kb = h, h + 2, ...;
-    // the two halves are then added (xor-16 shuffle): a fixed order
-    const float* pt = reinterpret_cast<const float*>(buf);
-    const int U = a.top_k + 1, r = lane & 15, h = lane >> 4;
-    float(*cs)[16] = sm.comb[warp];
-    float acc[kMaxSlots];
+// output.  Every column's partial already carries its expert's routing
+// weight, so the output is their plain sum: lane (row quad q = lane % 4,
+// column class c8 = lane / 4) adds the columns c8, c8 + 8, ... in order (all
+// its loads in flight at once, from L2), a fixed butterfly over the eight
+// column classes adds those, and lanes 0..3 round their four rows to bf16.
+__device__ void combine_part(const TokenArgs& a, int u, int w, int lane) {
+    const float4* src = reinterpret_cast<const float4*>(a.part + (static_cast<size_t>(u) * kParts + w) * a.ncols * 16);
+    const int n4 = a.ncols * 4;
+    constexpr int kBatch = 19;   // up to 152 columns in one batch
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int f0 = lane; f0 < n4; f0 += 32 * kBatch) {
+        float4 v[kBatch];
 #pragma unroll
-    for (int g = 0; g < kMaxSlots; ++g) {
-        float s0 = 0.0f, s1 = 0.0f;
-        if (g < U) {
-            const float* col = pt + (static_cast<size_t>(g) * a.RB + h) * 16 + r;
-            int kb = h;
-            for (; kb + 2 < a.RB; kb += 4, col += 64) {
-                s0 += col[0];
-                s1 += col[32];
-            }
-            if (kb < a.RB) s0 += col[0];
+        for (int b = 0; b < kBatch; ++b) {
+            const int f = f0 + 32 * b;
+            v[b] = f < n4 ? __ldcg(src + f) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
-        acc[g] = s0 + s1;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            acc.x += v[b].x;
+            acc.y += v[b].y;
+            acc.z += v[b].z;
+            acc.w += v[b].w;
+        }
     }
 #pragma unroll
-    for (int g = 0; g < kMaxSlots; ++g) acc[g] += __shfl_xor_sync(0xffffffffu, acc[g], 16);
-    if (lane < 16) {
-#pragma unroll
-        for (int g = 0; g < kMaxSlots; ++g) cs[g][lane] = acc[g];
+    for (int o = 4; o < 32; o <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
     }
-    __syncwarp();
-    if (lane < 16) {
-        float y = cs[0][lane];
-        for (int jj = 0; jj < a.top_k; ++jj) y = fmaf(sm.topk_w[jj], cs[1 + sm.pick_rank[jj]][lane], y);
-        const int n = (2 * u + (w >> 3)) * 128 + (w & 7) * 16 + lane;
-        a.out[n] = __float2bfloat16_rn(y);
+    if (lane < 4) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+        const int n = (2 * u + (w >> 3)) * 128 + (w & 7) * 16 + 4 * lane;
+        *reinterpret_cast<uint2*>(a.out + n) = packed;
     }
-    __syncwarp();
 }
 
-// The parts this warp sums, in unit order (kCombineWarps warps of a CTA
-// take parts, each into its own buffer in the stage ring and the x buffer
-// after it, both idle by then).  With CTAs to spare (grid > columns) those CTAs take every part:
-// part p = 16u + w goes to spare CTA p % n_spare and there to warp
-// (p / n_spare) % kCombineWarps, so a unit's 16 parts land on 16 different
-// warps; otherwise every CTA takes parts p = c + G * (warp + kCombineWarps * i)
-// once its own stream is done.  A part waits (bounded) for its unit's count
-// to reach ncols.
-__device__ void combine_worker(const TokenArgs& a, Smem& sm, uint8_t* stages, int cw, int lane) {
-    if (cw >= kCombineWarps) return;
+// The parts this warp sums, in unit order.  With CTAs to spare (grid >
+// columns) those CTAs take every part: part p = 16u + w goes to spare CTA
+// p % n_spare and there to warp (p / n_spare) % 16, so a unit's 16 parts land
+// on 16 different warps; otherwise every CTA takes parts p = c + G * (warp +
+// 16 i) once its own stream is done.  A part waits (bounded) for its unit's
+// count to reach ncols.
+__device__ void combine_worker(const TokenArgs& a, Smem& sm, int cw, int lane) {
     const int G = gridDim.x, c = blockIdx.x, total = (a.KB / 2) * kParts, n_spare = G - a.ncols;
     int first, stride;
     if (n_spare > 0) {
         if (c < a.ncols) return;
         first = (c - a.ncols) + n_spare * cw;
-        stride = n_spare * kCombineWarps;
+        stride = n_spare * kCW;
     } else {
         first = c + G * cw;
-        stride = G * kCombineWarps;
+        stride = G * kCW;
     }
-    if (first >= total) return;
-    // the routing weights and slots the sums read
-    if (lane == 0) wait_or_abort(&sm.plan_bar, 0, sm, a.status);
-    __syncwarp();
-    uint8_t* buf = stages + static_cast<size_t>(cw) * a.ncols * 64;
-    uint32_t parity = 0;
-    for (int p = first; p < total; p += stride, parity ^= 1u) {
+    for (int p = first; p < total; p += stride) {
         const int u = p / kParts;
         int ok = 0;
         if (lane == 0) {
@@ -525,12 +504,11 @@ __device__ void combine_worker(const TokenArgs& a, Smem& sm, uint8_t* stages, in
                         break;
                     }
                 }
-                __nanosleep(128);
+                __nanosleep(64);
             }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-        fence_proxy_async();   // the bulk copy reads what generic-proxy stores wrote
-        combine_part(a, sm, buf, &sm.comb_bar[cw], parity, u, p % kParts, cw, lane);
+        combine_part(a, u, p % kParts, lane);
     }
 }
 
@@ -591,11 +569,10 @@ __device__ void consumer_warp(const TokenArgs& a, Smem& sm, const uint8_t* stage
             const Column col = column(a, sm, j);
             if (!consume_column(a, sm, stages, col, j, cw, lane, it, stored)) return;
         }
-        consumer_sync();   // every stage has been read: the ring is free for the sums' buffers
     } else {
         pdl_wait();
     }
-    combine_worker(a, sm, const_cast<uint8_t*>(stages), cw, lane);
+    combine_worker(a, sm, cw, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) token_kernel(const __grid_constant__ TokenArgs a) {
@@ -610,7 +587,6 @@ __global__ void __launch_bounds__(kThreads, 1) token_kernel(const __grid_constan
             mbar_init(&sm.empty[s], kCW);
         }
         mbar_init(&sm.plan_bar, 1);
-        for (int w = 0; w < kCombineWarps; ++w) mbar_init(&sm.comb_bar[w], 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
