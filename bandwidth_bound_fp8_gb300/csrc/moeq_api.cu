@@ -480,9 +480,12 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
     const moeq_status st = noalloc_scratch(&ws);
     if (st != MOEQ_OK) return st;
     cudaStream_t cs = as_stream(stream);
-    // The counters (status word, epoch, input-quantisation count, tickets)
-    // must be zero when a launch starts: zero them on the stream first.
-    if (cudaMemsetAsync(ws, 0, wl.partials, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
+    // The counters (header: status word, epoch, input-quantisation count;
+    // the split-K tickets) must be zero when a launch starts: zero them on
+    // the stream first.  The activation buffers between them need no zeroing.
+    if (cudaMemsetAsync(ws, 0, kHeader, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
+    if (cudaMemsetAsync(static_cast<char*>(ws) + wl.tickets[0], 0, wl.partials - wl.tickets[0], cs) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
     StreamArgs a = {};
     Operand& o = a.op[kKindDN];
     o.quant_input = 1;
@@ -509,6 +512,7 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
+    a.mma = a.max_ntok >= mma_min_tokens();   // the path moeq_expert_gemm_down takes
     fill_ws(a, ws, wl, dev.sms);
     if (launch_stream(a, dev.sms, true, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
     if (device_status_opt &&

@@ -50,11 +50,15 @@ __device__ __noinline__ void mma_issue_loop(const StreamArgs& a, SmemTail& sm, c
         }
         ++c;
     }
-    // every MMA issued must have completed before TMEM is freed (bounded)
+    // every MMA issued must have completed before TMEM is freed (bounded; a
+    // wait that runs out is an error of the launch: its results are void)
     if (last >= 0) {
         const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(&sm.mma_done[last % kTmemBufs], static_cast<uint32_t>((last / kTmemBufs) & 1)) &&
-               global_timer_ns() - t0 < 100ull * 1000ull * 1000ull) {
+        while (!mbar_try_wait(&sm.mma_done[last % kTmemBufs], static_cast<uint32_t>((last / kTmemBufs) & 1))) {
+            if (global_timer_ns() - t0 > 100ull * 1000ull * 1000ull) {
+                if (lane == 0) record_error(a.status, MOEQ_ERR_TIMEOUT);
+                break;
+            }
         }
     }
 }

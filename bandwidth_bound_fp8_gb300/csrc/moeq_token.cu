@@ -416,9 +416,11 @@ __device__ bool consume_column(const TokenArgs& a, Smem& sm, const uint8_t* stag
             st_global_hint(a.part + ((static_cast<size_t>(u) * kParts + cw) * a.ncols + j) * 16 + 4 * (l8 >> 1) + rsub,
                            v, keep);
         __syncwarp();
-        if (lane == 0) {
+        // the ticket warp learns of the stored partials four units at a time
+        ++stored;
+        if (lane == 0 && ((i & 3) == 3 || i == nu - 1)) {
             __threadfence_block();
-            *reinterpret_cast<volatile int*>(&sm.wdone[cw]) = ++stored;
+            *reinterpret_cast<volatile int*>(&sm.wdone[cw]) = stored;
         }
     }
     return true;

@@ -39,10 +39,13 @@
  *     `stream` is a cudaStream_t passed as void*;
  *   - calls are asynchronous on `stream` and never synchronise the host
  *     (except moeq_read_device_status, which says so);
- *   - the library allocates no device memory: the caller passes a
- *     workspace sized by moeq_workspace_size / moeq_gemm_workspace_size,
- *     zeroed once with moeq_workspace_init; kernels leave it reusable; one
- *     workspace must not be used by two calls that may run concurrently;
+ *   - the library makes no device allocation at run time: the caller
+ *     passes a workspace sized by moeq_workspace_size /
+ *     moeq_gemm_workspace_size, zeroed once with moeq_workspace_init; kernels
+ *     leave it reusable; one workspace must not be used by two calls that may
+ *     run concurrently.  The one exception, moeq_expert_gemm_down_noalloc,
+ *     uses a fixed 8 MiB static device array that the library holds on every
+ *     device it is loaded on;
  *   - arguments are validated on the host first; on any error nothing is
  *     launched and the status says why;
  *   - inputs must be finite (NaN/Inf inputs give unspecified results).

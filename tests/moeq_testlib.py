@@ -91,6 +91,18 @@ class Experts:
         return orc.quant_weight(self.f32(e))
 
 
+def half_ulp_bf16(*vals) -> np.ndarray:
+    """Half a bf16 ulp at the larger magnitude of the given values (arrays of
+    the same shape), from the exponent: a value in [2^e, 2^(e+1)) has ulp
+    2^(e-7) in bf16 (8 significant bits), so half of it is 2^(e-8); zero and
+    subnormal magnitudes take the subnormal spacing's half, 2^-134.  This
+    bounds the final rounding of a result to bf16: |RN(g) - g| is at most
+    half an ulp at |RN(g)|."""
+    m = np.max(np.abs(np.stack([np.asarray(v, np.float64) for v in vals])), axis=0)
+    e = np.floor(np.log2(np.maximum(m, 2.0 ** -126)))
+    return np.where(m >= 2.0 ** -126, 2.0 ** (e - 8), 2.0 ** -134)
+
+
 def assert_close(gpu, ref, T, rel, absl=0.0, what=""):
     gpu = np.asarray(gpu, np.float64)
     err = np.abs(gpu - ref)
