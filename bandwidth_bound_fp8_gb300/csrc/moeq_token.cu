@@ -54,6 +54,7 @@ constexpr int kStages = 4;
 constexpr int kMaxKB = kTokenMaxH / 128;       // K groups of x
 constexpr int kMaxUnits = kTokenMaxH / 256;    // 256-row output units of down
 constexpr int kParts = kCW;                    // a unit's rows split by consumer warp (16 rows each)
+constexpr int kTailUnits = 4;                  // the last down units, summed by the column CTAs
 
 struct Smem {
     alignas(16) float xdec[kTokenMaxH];   // decoded x codes, each group in the consumer layout
@@ -167,6 +168,15 @@ __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int
     const int stages_per_col = a.KB + a.KB / 2;
     const uint64_t pol = l2_evict_first_policy();
     long long issued = 0;
+    // The logits and x are the previous kernel's to write until
+    // griddepcontrol.wait; their lines can still be brought into L2 now (L2
+    // is where every SM's writes meet), so the reads after the wait are hits.
+    {
+        const int lg_lines = (a.E_routed * 4 + 127) / 128, x_lines = (a.H * 2 + 127) / 128;
+        for (int i = lane; i < lg_lines + x_lines; i += 32)
+            prefetch_l2(i < lg_lines ? reinterpret_cast<const char*>(a.logits) + 128 * i
+                                     : reinterpret_cast<const char*>(a.x) + 128 * (i - lg_lines));
+    }
     prefetch_shared_expert(a, lane);
     // The shared expert's columns (the first RB) need no plan: start them now.
     int pre = 0;
@@ -416,9 +426,10 @@ __device__ bool consume_column(const TokenArgs& a, Smem& sm, const uint8_t* stag
             st_global_hint(a.part + ((static_cast<size_t>(u) * kParts + cw) * a.ncols + j) * 16 + 4 * (l8 >> 1) + rsub,
                            v, keep);
         __syncwarp();
-        // the ticket warp learns of the stored partials four units at a time
+        // the ticket warp learns of the stored partials four units at a time,
+        // and of each of the last kTailUnits at once
         ++stored;
-        if (lane == 0 && ((i & 3) == 3 || i == nu - 1)) {
+        if (lane == 0 && ((i & 3) == 3 || i >= nu - kTailUnits)) {
             __threadfence_block();
             *reinterpret_cast<volatile int*>(&sm.wdone[cw]) = stored;
         }
@@ -470,48 +481,55 @@ __device__ void combine_part(const TokenArgs& a, int u, int w, int lane) {
     }
 }
 
-// The parts this warp sums, in unit order.  With CTAs to spare (grid >
-// columns) those CTAs take every part: part p = 16u + w goes to spare CTA
-// p % n_spare and there to warp (p / n_spare) % 16, so a unit's 16 parts land
-// on 16 different warps; otherwise every CTA takes parts p = c + G * (warp +
-// 16 i) once its own stream is done.  A part waits (bounded) for its unit's
-// count to reach ncols.
-__device__ void combine_worker(const TokenArgs& a, Smem& sm, int cw, int lane) {
-    const int G = gridDim.x, c = blockIdx.x, total = (a.KB / 2) * kParts, n_spare = G - a.ncols;
-    int first, stride;
-    if (n_spare > 0) {
-        if (c < a.ncols) return;
-        first = (c - a.ncols) + n_spare * cw;
-        stride = n_spare * kCW;
-    } else {
-        first = c + G * cw;
-        stride = G * kCW;
-    }
-    for (int p = first; p < total; p += stride) {
-        const int u = p / kParts;
-        int ok = 0;
-        if (lane == 0) {
-            const int* cnt = a.tickets + u;
-            const unsigned long long t0 = global_timer_ns();
-            for (uint32_t i = 0;; ++i) {
-                if (ld_relaxed(cnt) >= a.ncols) {
-                    ok = ld_acquire(cnt) >= a.ncols;   // acquires the unit's partials
+// The parts this warp sums, in unit order.  The units complete one after
+// another as the slowest stream passes them.  All but the last kTailUnits
+// are summed while the streams go on, by the CTAs without a column when there
+// are some (part p = 16u + w to spare CTA p % n_spare, warp (p / n_spare) %
+// 16, so a unit's 16 parts land on 16 different warps), else by every CTA
+// once its stream is done (part p to CTA p % G).  The last units complete at
+// the very end, when every column CTA is free: their parts are spread one per
+// CTA over the column CTAs.  A part waits (bounded) for its unit's count to
+// reach ncols.
+__device__ void sum_part_when_complete(const TokenArgs& a, Smem& sm, int p, int lane, bool& ok_out) {
+    const int u = p / kParts;
+    int ok = 0;
+    if (lane == 0) {
+        const int* cnt = a.tickets + u;
+        const unsigned long long t0 = global_timer_ns();
+        for (uint32_t i = 0;; ++i) {
+            if (ld_relaxed(cnt) >= a.ncols) {
+                ok = ld_acquire(cnt) >= a.ncols;   // acquires the unit's partials
+                break;
+            }
+            if ((i & 7u) == 7u) {
+                if (sm.abort_flag) break;
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    record_error(a.status, MOEQ_ERR_TIMEOUT);
+                    sm.abort_flag = 1;
                     break;
                 }
-                if ((i & 7u) == 7u) {
-                    if (sm.abort_flag) break;
-                    if (global_timer_ns() - t0 > kWaitLimitNs) {
-                        record_error(a.status, MOEQ_ERR_TIMEOUT);
-                        sm.abort_flag = 1;
-                        break;
-                    }
-                }
-                __nanosleep(64);
             }
+            __nanosleep(64);
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-        combine_part(a, u, p % kParts, lane);
     }
+    ok_out = __shfl_sync(0xffffffffu, ok, 0) != 0;
+    if (ok_out) combine_part(a, u, p % kParts, lane);
+}
+
+__device__ void combine_worker(const TokenArgs& a, Smem& sm, int cw, int lane) {
+    const int G = gridDim.x, c = blockIdx.x, nu = a.KB / 2, n_spare = G - a.ncols;
+    const int tail = min(kTailUnits, nu), early = (nu - tail) * kParts;
+    bool ok = true;
+    if (n_spare > 0) {
+        if (c >= a.ncols)
+            for (int p = (c - a.ncols) + n_spare * cw; p < early && ok; p += n_spare * kCW)
+                sum_part_when_complete(a, sm, p, lane, ok);
+    } else {
+        for (int p = c + G * cw; p < early && ok; p += G * kCW) sum_part_when_complete(a, sm, p, lane, ok);
+    }
+    const int nc = min(a.ncols, G);
+    if (c < nc)
+        for (int q = c + nc * cw; q < tail * kParts && ok; q += nc * kCW) sum_part_when_complete(a, sm, early + q, lane, ok);
 }
 
 // The ticket warp: as the consumer warps store down partials, count each
