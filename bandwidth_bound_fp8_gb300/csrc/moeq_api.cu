@@ -74,6 +74,16 @@ bool pdl_enabled() {
     static const bool v = env_flag("MOEQ_PDL", true);
     return v;
 }
+// The standalone GEMM calls spread over every SM; MOEQ_GRID_LIMIT=n (read
+// once) caps them at n CTAs, for experiments that compare split widths.
+int gemm_grid(int sms) {
+    static const int lim = [] {
+        const char* e = std::getenv("MOEQ_GRID_LIMIT");
+        const int x = e ? std::atoi(e) : 0;
+        return x >= 1 ? x : 0;
+    }();
+    return lim ? std::min(lim, sms) : sms;
+}
 
 // The one-token kernel reads weights before it waits for the kernel ahead of
 // it on the stream (programmatic dependent launch).  This library's own
@@ -374,7 +384,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.mma = a.max_ntok >= mma_min_tokens();
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
-    return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
+    return cuda_status(launch_stream(a, gemm_grid(dev.sms), true, as_stream(stream)));
 }
 
 moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, int N, const uint8_t* w_d,
@@ -420,7 +430,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
     a.mma = a.max_ntok >= mma_min_tokens();
     fill_ws(a, ws, wl, dev.sms);
-    return cuda_status(launch_stream(a, dev.sms, true, as_stream(stream)));
+    return cuda_status(launch_stream(a, gemm_grid(dev.sms), true, as_stream(stream)));
 }
 
 // ------------------------------------------------------------------ no-alloc down
@@ -520,6 +530,80 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
                         cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
         return MOEQ_ERR_CUDA;
     return MOEQ_OK;
+}
+
+// ------------------------------------------------------------------ dense FFN
+// One token through one dense FFN: the one-token kernel with no routing (the
+// one expert is its "shared" expert).  Workspace: header, h [I], the down
+// partials [I/128, H], the arrival counts and the completion count.
+struct DenseWs {
+    size_t h, part, tickets, end;
+};
+
+DenseWs dense_ws_layout(int H, int I) {
+    DenseWs l;
+    l.h = kHeader;
+    l.part = align_up(l.h + sizeof(float) * static_cast<size_t>(I), 256);
+    l.tickets = align_up(l.part + sizeof(float) * static_cast<size_t>(I / 128) * H, 256);
+    l.end = align_up(l.tickets + sizeof(int) * (static_cast<size_t>(H / 256) + kGqUnits), 256);
+    return l;
+}
+
+bool dense_shape_ok(int M, int H, int I) {
+    return M == 1 && H > 0 && I > 0 && H % 256 == 0 && I % 128 == 0 && H <= kTokenMaxH && I <= MOEQ_MAX_K;
+}
+
+size_t moeq_dense_ffn_workspace_size(int M, int H, int I) {
+    if (!dense_shape_ok(M, H, I)) return 0;
+    return dense_ws_layout(H, I).end;
+}
+
+moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_gu, const float* s_gu,
+                           const uint8_t* w_d, const float* s_d, void* out, float* h_opt, uint8_t* q_x_opt,
+                           float* s_x_opt, uint8_t* q_h_opt, float* s_h_opt, void* ws, size_t ws_bytes,
+                           void* stream) {
+    if (!x || !w_gu || !s_gu || !w_d || !s_d || !out) return MOEQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gu) || !aligned16(w_d) || !aligned16(out) || !aligned4(s_gu) || !aligned4(s_d))
+        return MOEQ_ERR_INVALID_ARG;
+    if (h_opt && !aligned16(h_opt)) return MOEQ_ERR_INVALID_ARG;
+    if ((q_x_opt == nullptr) != (s_x_opt == nullptr) || (q_h_opt == nullptr) != (s_h_opt == nullptr))
+        return MOEQ_ERR_INVALID_ARG;
+    if ((q_x_opt && (!aligned16(q_x_opt) || !aligned4(s_x_opt))) || (q_h_opt && (!aligned16(q_h_opt) || !aligned4(s_h_opt))))
+        return MOEQ_ERR_INVALID_ARG;
+    if (M < 1 || M > MOEQ_MAX_TOKENS) return MOEQ_ERR_INVALID_ARG;
+    if (!dense_shape_ok(M, H, I)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    const DeviceInfo dev = current_device();
+    if (!dev.ok) return MOEQ_ERR_DEVICE;
+    const DenseWs l = dense_ws_layout(H, I);
+    if (!ws || !aligned16(ws) || ws_bytes < l.end) return MOEQ_ERR_WORKSPACE;
+    char* base = static_cast<char*>(ws);
+    TokenArgs t = {};
+    t.x = static_cast<const __nv_bfloat16*>(x);
+    t.logits = nullptr;
+    t.H = H;
+    t.I = I;
+    t.KB = H / 128;
+    t.RB = I / 128;
+    t.E_routed = 0;   // expert 0 is the one expert
+    t.top_k = 0;
+    t.ncols = I / 128;
+    t.w_gu = w_gu;
+    t.s_gu = s_gu;
+    t.w_d = w_d;
+    t.s_d = s_d;
+    t.out = static_cast<__nv_bfloat16*>(out);
+    t.h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
+    t.q_x = q_x_opt;
+    t.s_x = s_x_opt;
+    t.q_h = q_h_opt;
+    t.s_h = s_h_opt;
+    t.status = reinterpret_cast<int*>(base + kOffStatus);
+    t.tickets = reinterpret_cast<int*>(base + l.tickets);
+    t.gq = t.tickets + H / 256;
+    t.part = reinterpret_cast<float*>(base + l.part);
+    uintptr_t key = stream_key(stream);
+    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+    return cuda_status(launch_token(t, dev.sms, pdl_enabled() && !after_weight_write, as_stream(stream)));
 }
 
 moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k, void* out_bf16,

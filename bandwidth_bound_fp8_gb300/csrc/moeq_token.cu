@@ -163,6 +163,59 @@ __device__ __forceinline__ void route_one_token(const TokenArgs& a, Smem& sm, in
     route_topk_keys<NPER>(key, a.E_routed, a.top_k, lane, sm.topk_id, sm.rvals);
 }
 
+// Routing of the token by the producer warp: top-k with ties to the lower
+// id, softmax over the picks, picks sorted by id into the slots; CTA 0 also
+// writes the plan out.
+__device__ void producer_route(const TokenArgs& a, Smem& sm, int lane) {
+    const int k = a.top_k;
+    if (a.E_routed <= 256)
+        route_one_token<8>(a, sm, lane);
+    else
+        route_one_token<kRouteMaxE / 32>(a, sm, lane);
+    __syncwarp();
+    float ex = 0.0f;
+    int id = 0x7fffffff;
+    if (lane < k) {
+        ex = expf(sm.rvals[lane] - sm.rvals[0]);
+        id = sm.topk_id[lane];
+    }
+    float den = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    int rank = 0;
+    for (int i = 0; i < k; ++i) rank += __shfl_sync(0xffffffffu, id, i) < id;
+    const float w = lane < k ? __fdiv_rn(ex, den) : 0.0f;
+    if (lane < k) {
+        sm.topk_w[lane] = w;
+        sm.uniq[rank] = id;
+        sm.pick_rank[lane] = rank;
+        sm.slot_pick[rank] = lane;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.plan_bar);
+    if (blockIdx.x == 0) {
+        // CTA 0 hands the plan to the caller (one token: every routed expert
+        // has one pair, in uniq order; the shared expert's pair is last)
+        const moeq_route_plan& p = a.plan;
+        if (lane < k) {
+            p.topk_id[lane] = id;
+            p.topk_w[lane] = w;
+            p.uniq[rank] = id;
+            p.offs[lane] = lane;
+            p.pair_tok[lane] = 0;
+            p.pair_of[lane] = rank;
+        }
+        if (lane == 0) {
+            p.uniq[k] = a.E_routed;
+            p.offs[k] = k;
+            p.offs[k + 1] = k + 1;
+            p.pair_tok[k] = 0;
+            p.pair_of[k] = k;
+            *p.n_uniq = k + 1;
+        }
+    }
+}
+
 __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int lane) {
     const int G = gridDim.x, c = blockIdx.x, k = a.top_k;
     const int stages_per_col = a.KB + a.KB / 2;
@@ -192,53 +245,10 @@ __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int
     }
     issued = pre;
     pdl_wait();
-    // top-k with ties to the lower id, softmax over the picks, picks sorted
-    // by id into the slots
-    if (a.E_routed <= 256)
-        route_one_token<8>(a, sm, lane);
-    else
-        route_one_token<kRouteMaxE / 32>(a, sm, lane);
-    __syncwarp();
-    float ex = 0.0f;
-    int id = 0x7fffffff;
-    if (lane < k) {
-        ex = expf(sm.rvals[lane] - sm.rvals[0]);
-        id = sm.topk_id[lane];
-    }
-    float den = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    int rank = 0;
-    for (int i = 0; i < k; ++i) rank += __shfl_sync(0xffffffffu, id, i) < id;
-    const float w = lane < k ? __fdiv_rn(ex, den) : 0.0f;
-    if (lane < k) {
-        sm.topk_w[lane] = w;
-        sm.uniq[rank] = id;
-        sm.pick_rank[lane] = rank;
-        sm.slot_pick[rank] = lane;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.plan_bar);
-    if (c == 0) {
-        // CTA 0 hands the plan to the caller (one token: every routed expert
-        // has one pair, in uniq order; the shared expert's pair is last)
-        const moeq_route_plan& p = a.plan;
-        if (lane < k) {
-            p.topk_id[lane] = id;
-            p.topk_w[lane] = w;
-            p.uniq[rank] = id;
-            p.offs[lane] = lane;
-            p.pair_tok[lane] = 0;
-            p.pair_of[lane] = rank;
-        }
-        if (lane == 0) {
-            p.uniq[k] = a.E_routed;
-            p.offs[k] = k;
-            p.offs[k + 1] = k + 1;
-            p.pair_tok[k] = 0;
-            p.pair_of[k] = k;
-            *p.n_uniq = k + 1;
-        }
+    if (k == 0) {   // a dense FFN: the one expert, no routing
+        if (lane == 0) mbar_arrive(&sm.plan_bar);
+    } else {
+        producer_route(a, sm, lane);
     }
     if (lane != 0) return;
     for (int j = c; j < a.ncols && !sm.abort_flag; j += G) {

@@ -35,6 +35,7 @@ EXPORTS = [
     "moeq_gemm_workspace_size", "moeq_workspace_init", "moeq_read_device_status",
     "moeq_quant_act", "moeq_quant_weight", "moeq_pack_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
     "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer", "moeq_expert_gemm_down_noalloc",
+    "moeq_dense_ffn_workspace_size", "moeq_dense_ffn",
 ]
 
 
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
         "moeq_combine": (_i, [_vp, _i, ctypes.POINTER(moeq_route_plan), _i, _i, _vp, _vp]),
         "moeq_expert_gemm_down_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _i,
                                                _vp, _vp, _vp, _vp, _vp]),
+        "moeq_dense_ffn_workspace_size": (_sz, [_i, _i, _i]),
+        "moeq_dense_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
         "moeq_moe_layer": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                                 ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                 _sz, _vp]),
@@ -257,6 +260,18 @@ def moeq_expert_gemm_down(a, K, N, w_d, s_d, n_experts, uniq, offs, n_uniq, max_
     _check("moeq_expert_gemm_down", load().moeq_expert_gemm_down(
         _p(a), _dtype(a), K, N, _p(w_d), _p(s_d), n_experts, _p(uniq), _p(offs), _p(n_uniq),
         max_uniq, max_pairs, _p(y), _p(q_a), _p(s_a), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def moeq_dense_ffn_workspace_size(M, H, I) -> int:
+    return int(load().moeq_dense_ffn_workspace_size(M, H, I))
+
+
+def moeq_dense_ffn(x, H, I, w_gu, s_gu, w_d, s_d, out, ws: Workspace, h=None, q_x=None, s_x=None, q_h=None,
+                   s_h=None, stream=None) -> None:
+    M = x.shape[0]
+    _check("moeq_dense_ffn", load().moeq_dense_ffn(
+        _p(x), M, H, I, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(out), _p(h), _p(q_x), _p(s_x), _p(q_h), _p(s_h),
+        ws.ptr, ws.nbytes, _stream(stream)))
 
 
 def moeq_combine(y, N, plan: RoutePlan, M, top_k, out, stream=None) -> None:

@@ -433,6 +433,174 @@ def cpu_baseline(stack, M, seed, budget_s=10.0):
             "seconds": round(t_total, 2)}
 
 
+# ------------------------------------------------------------------ dense configs and the gate_up ladder
+L2_BYTES = 129 * 1024 * 1024
+
+
+def time_scrubbed(fn, reps: int, warmup: int):
+    """Median / p10 / p90 ms of fn() over `reps` CUDA-event timings, each
+    after a write of more than twice L2 (outside the timed region), so the
+    weights come from HBM every time."""
+    scrub = torch.empty(2 * L2_BYTES // 4 + 1024, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(reps):
+        scrub.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    return ts[len(ts) // 2], ts[len(ts) // 10], ts[(len(ts) * 9) // 10]
+
+
+def _line(name, byts, t, peak, oracle_s=None):
+    med, p10, p90 = t
+    d = {"workload": name, "us": round(med * 1e3, 2), "us_p10": round(p10 * 1e3, 2), "us_p90": round(p90 * 1e3, 2),
+         "weight_bytes": byts, "weight_GBps": round(byts / (med * 1e-3) / 1e9, 1),
+         "frac_of_measured_hbm": round(byts / (med * 1e-3) / 1e9 / peak, 4),
+         "frac_of_8TBps": round(byts / (med * 1e-3) / 1e9 / 8000, 4), "l2": "scrubbed (> 2x L2 written) before each rep"}
+    if oracle_s is not None:
+        d["oracle_ms_1core"] = round(oracle_s * 1e3, 2)
+    return d
+
+
+def bench_dense(peak, reps=50, with_oracle=True):
+    """The two dense configurations at M = 1, each call timed alone:
+    C0 the projection K 2048 -> N 4096 (one moeq_expert_gemm_down call, x bf16
+    in, y fp32 out); C1 the FFN hidden 6144 / intermediate 12288 through
+    moeq_dense_ffn (one kernel), and through the three separate calls (gate_up
+    + SwiGLU, down, the bf16 cast through moeq_combine).  Beside each, the
+    oracle (one core) on the same inputs."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    out = {}
+    # C0
+    c = synth.DENSE_PROJ
+    K, N = c["K"], c["N"]
+    wq = torch.empty((1, N, K), dtype=torch.uint8, device="cuda")
+    ws_ = torch.empty((1, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    w32 = synth.weight_f32(N, K, synth.expert_seed(c["seed"], 0, 0, 1), device="cuda")
+    moeq.moeq_quant_weight(w32[None], wq, ws_)
+    x = synth.activations_bf16(1, K, c["seed"], c["n_outlier"], c["outlier_scale"], device="cuda")
+    one = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    uq, of, nu = one([0]), one([0, 1]), one([1])
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    wsp = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, 1, 1, 0))
+    torch.cuda.synchronize()
+    t = time_scrubbed(lambda: moeq.moeq_expert_gemm_down(x, K, N, wq, ws_, 1, uq, of, nu, 1, 1, y, wsp), reps, 5)
+    osec = None
+    if with_oracle:
+        import oracle
+        qw, sw = oracle.quant_weight(w32.cpu().numpy())
+        xb = x.view(torch.uint16).cpu().numpy()
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(xb)
+        oracle.gemm(qa, sa, qw, sw)
+        osec = time.perf_counter() - t0
+    out["C0"] = _line(c["name"], N * K + (N // 128) * (K // 128) * 4, t, peak, osec)
+    del wq, ws_, w32
+    # C1
+    c = synth.DENSE_FFN
+    Hh, Ii = c["H"], c["I"]
+    gq = torch.empty((1, 2 * Ii, Hh), dtype=torch.uint8, device="cuda")
+    gs = torch.empty((1, 2 * Ii // 128, Hh // 128), dtype=torch.float32, device="cuda")
+    dq = torch.empty((1, Hh, Ii), dtype=torch.uint8, device="cuda")
+    dsc = torch.empty((1, Hh // 128, Ii // 128), dtype=torch.float32, device="cuda")
+    g32 = synth.weight_f32(2 * Ii, Hh, synth.expert_seed(c["seed"], 0, 0, 0), device="cuda")
+    moeq.moeq_quant_weight(g32[None], gq, gs)
+    d32 = synth.weight_f32(Hh, Ii, synth.expert_seed(c["seed"], 0, 0, 1), device="cuda")
+    moeq.moeq_quant_weight(d32[None], dq, dsc)
+    x = synth.activations_bf16(1, Hh, c["seed"], c["n_outlier"], c["outlier_scale"], device="cuda")
+    pt = one([0])
+    h = torch.empty((1, Ii), dtype=torch.float32, device="cuda")
+    y = torch.empty((1, Hh), dtype=torch.float32, device="cuda")
+    o16 = torch.empty((1, Hh), dtype=torch.bfloat16, device="cuda")
+    wgu = moeq.Workspace(moeq.moeq_gemm_workspace_size(2 * Ii, Hh, 1, 1, 1))
+    wdn = moeq.Workspace(moeq.moeq_gemm_workspace_size(Hh, Ii, 1, 1, 0))
+    plan = moeq.RoutePlan(1, 1, 1)
+    plan.pair_of.view(-1)[0] = 0
+    torch.cuda.synchronize()
+
+    def ffn():
+        moeq.moeq_expert_gemm_gateup_swiglu(x, Hh, Ii, gq, gs, 1, uq, of, pt, nu, 1, 1, h, wgu)
+        moeq.moeq_expert_gemm_down(h, Ii, Hh, dq, dsc, 1, uq, of, nu, 1, 1, y, wdn)
+        moeq.moeq_combine(y, Hh, plan, 1, 0, o16)
+
+    t_calls = time_scrubbed(ffn, reps, 5)
+    wff = moeq.Workspace(moeq.moeq_dense_ffn_workspace_size(1, Hh, Ii))
+    torch.cuda.synchronize()
+    t = time_scrubbed(lambda: moeq.moeq_dense_ffn(x, Hh, Ii, gq, gs, dq, dsc, o16, wff), reps, 5)
+    osec = None
+    if with_oracle:
+        import oracle
+        qg, sg = oracle.quant_weight(g32.cpu().numpy())
+        qd, sd = oracle.quant_weight(d32.cpu().numpy())
+        xb = x.view(torch.uint16).cpu().numpy()
+        t0 = time.perf_counter()
+        qa, sa = oracle.quant_act(xb)
+        gy = oracle.gemm(qa, sa, qg, sg, with_T=False)
+        hh = oracle.swiglu_vec(gy[:, :Ii], gy[:, Ii:])
+        qh, sh = oracle.quant_act(hh)
+        yy = oracle.gemm(qh, sh, qd, sd, with_T=False)
+        [oracle.f64_to_bf16_bits(v) for v in yy[0]]
+        osec = time.perf_counter() - t0
+    byts = 2 * Ii * Hh + (2 * Ii // 128) * (Hh // 128) * 4 + Hh * Ii + (Hh // 128) * (Ii // 128) * 4
+    out["C1"] = _line(c["name"], byts, t, peak, osec)
+    out["C1"]["call"] = "moeq_dense_ffn (one kernel)"
+    out["C1_gemm_calls"] = _line(c["name"], byts, t_calls, peak)
+    out["C1_gemm_calls"]["call"] = "moeq_expert_gemm_gateup_swiglu + moeq_expert_gemm_down + moeq_combine"
+    out["C0"]["call"] = "moeq_expert_gemm_down"
+    return out
+
+
+def gate_up_ladder(peak, variants=("split_all_sms", "quant_launch_first"), reps=30):
+    """The one-token gate_up of a layer (the shared expert and 8 routed
+    experts: 226.5 MB) in the variants the GLM-5.2 x10 page measured (§1):
+    split over every SM (this library's call); the activations' quantisation
+    as a launch of its own ahead of the GEMM (which still quantises its input
+    itself); and, in a child process with MOEQ_GRID_LIMIT=4, four CTAs."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    n_exp = 9
+    gq = torch.empty((n_exp, 2 * I, H), dtype=torch.uint8, device="cuda")
+    gs = torch.empty((n_exp, 2 * I // 128, H // 128), dtype=torch.float32, device="cuda")
+    for e in range(n_exp):
+        w = synth.weight_f32(2 * I, H, synth.expert_seed(CFG["seed"], 9, e, 0), device="cuda")
+        moeq.moeq_quant_weight(w[None], gq[e:e + 1], gs[e:e + 1])
+    del w
+    x = synth.activations_bf16(1, H, 3, CFG["n_outlier"], CFG["outlier_scale"], device="cuda")
+    t = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    uq, of, pt, nu = t(list(range(n_exp))), t(list(range(n_exp + 1))), t([0] * n_exp), t([n_exp])
+    h = torch.empty((n_exp, I), dtype=torch.float32, device="cuda")
+    qx = torch.empty((1, H), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((1, H // 128), dtype=torch.float32, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(2 * I, H, 1, n_exp, 1))
+    torch.cuda.synchronize()
+    gemm = lambda: moeq.moeq_expert_gemm_gateup_swiglu(x, H, I, gq, gs, n_exp, uq, of, pt, nu, n_exp, n_exp, h, ws)
+    byts = n_exp * GU_BYTES
+    out = {}
+    for v in variants:
+        if v == "quant_launch_first":
+            fn = lambda: (moeq.moeq_quant_act(x, qx, sx), gemm())
+        else:
+            fn = gemm
+        out[v] = _line(f"gate_up_m1_9experts_h{H}_i{I} ({v})", byts, time_scrubbed(fn, reps, 3), peak)
+    return out
+
+
+def gate_up_ladder_child(peak):
+    """The ladder's four-CTA leg, in a child process (the grid limit is read
+    once per process)."""
+    env = dict(os.environ, MOEQ_GRID_LIMIT="4")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--ladder-child"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 # ------------------------------------------------------------------ reference arm
 def reference_arm(args, ws, rank):
     """The oracle as the reference arm, on a shape-reduced sample of the layer:
@@ -537,9 +705,17 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="run a few launches of the small ncu case (8 routed experts, top-8) and exit")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense configurations and the gate_up ladder")
+    ap.add_argument("--ladder-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.profile_case:
         profile_case(args.M, args.reps)
+        return
+    if args.ladder_child:
+        from bandwidth_bound_fp8_gb300 import build as b
+        b.build()
+        peak, _ = load_peaks()
+        print(json.dumps(gate_up_ladder(peak, variants=("four_ctas",), reps=5)["four_ctas"]))
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -588,6 +764,12 @@ def main():
                               "U_mean": rr["U_mean"],
                               "isolated_launch_us": round(rr["isolated_ms"] * 1e3, 2)}
             del rr
+    dense = None
+    if rank == 0 and not args.no_dense:
+        dense = bench_dense(peak, with_oracle=not args.no_cpu)
+        ladder = gate_up_ladder(peak)
+        ladder["four_ctas"] = gate_up_ladder_child(peak)
+        dense["gate_up_ladder"] = ladder
     e2e = None
     if rank == 0:
         e = bench_e2e(stack, args.M, min(args.e2e_steps, args.steps), seed=9000)
@@ -613,7 +795,7 @@ def main():
             "kernel_us": round(r["kernel_ms"] * 1e3, 3),
             "isolated_launch_us": round(r["isolated_ms"] * 1e3, 3),
             "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-            "gpu_launches": args.steps, "sweep": sweep,
+            "gpu_launches": args.steps, "sweep": sweep, "dense": dense,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
