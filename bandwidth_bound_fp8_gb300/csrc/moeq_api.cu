@@ -221,6 +221,259 @@ void fill_ws(StreamArgs& a, void* ws, const StreamWs& l, int grid) {
     a.comb = reinterpret_cast<int*>(base + l.comb);
 }
 
+// ------------------------------------------------------------------ layer
+// One moeq_moe_layer call's arguments.
+struct LayerCall {
+    const void* x;
+    const float* logits;
+    int M, H, I, E_routed, top_k;
+    const uint8_t* w_gu;
+    const float* s_gu;
+    const uint8_t* w_d;
+    const float* s_d;
+    void* out;
+    const moeq_route_plan* plan_opt;
+    float* h_opt;
+    float* y_opt;
+    uint8_t* q_x_opt;
+    float* s_x_opt;
+    uint8_t* q_h_opt;
+    float* s_h_opt;
+    void* const* events_opt;
+    void* ws;
+    size_t ws_bytes;
+};
+
+// Host-side checks of one layer call (nothing is launched).
+moeq_status layer_check(const LayerCall& c, const DeviceInfo& dev) {
+    if (!c.x || !c.logits || !c.w_gu || !c.s_gu || !c.w_d || !c.s_d || !c.out) return MOEQ_ERR_INVALID_ARG;
+    if (!aligned16(c.x) || !aligned16(c.w_gu) || !aligned16(c.w_d) || !aligned16(c.out) || !aligned4(c.s_gu) ||
+        !aligned4(c.s_d))
+        return MOEQ_ERR_INVALID_ARG;
+    if ((c.h_opt && !aligned16(c.h_opt)) || (c.y_opt && !aligned16(c.y_opt))) return MOEQ_ERR_INVALID_ARG;
+    if ((c.q_x_opt == nullptr) != (c.s_x_opt == nullptr) || (c.q_h_opt == nullptr) != (c.s_h_opt == nullptr))
+        return MOEQ_ERR_INVALID_ARG;
+    if ((c.q_x_opt && (!aligned16(c.q_x_opt) || !aligned4(c.s_x_opt))) ||
+        (c.q_h_opt && (!aligned16(c.q_h_opt) || !aligned4(c.s_h_opt))))
+        return MOEQ_ERR_INVALID_ARG;
+    if (c.plan_opt && !plan_ok(c.plan_opt)) return MOEQ_ERR_INVALID_ARG;
+    if (!route_args_ok(c.M, c.E_routed, c.top_k)) return MOEQ_ERR_INVALID_ARG;
+    const int H = c.H, I = c.I;
+    if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K || I > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    if (!dev.ok) return MOEQ_ERR_DEVICE;
+    const LayerWs l = layer_ws_layout(c.M, H, I, c.E_routed, c.top_k, dev.sms);
+    if (!c.ws || !aligned16(c.ws) || c.ws_bytes < l.s.end) return MOEQ_ERR_WORKSPACE;
+    return MOEQ_OK;
+}
+
+// The launch of one checked layer call.  route_early: the logits are not
+// written by the kernel ahead on the stream (the one-token kernel may then
+// route before it waits for that kernel); allow_pdl: the weights are not
+// either.
+moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_early, bool allow_pdl,
+                         cudaStream_t st) {
+    const void* x = c.x;
+    const float* logits = c.logits;
+    const int M = c.M, H = c.H, I = c.I, E_routed = c.E_routed, top_k = c.top_k;
+    const uint8_t *w_gu = c.w_gu, *w_d = c.w_d;
+    const float *s_gu = c.s_gu, *s_d = c.s_d;
+    void* out = c.out;
+    const moeq_route_plan* plan_opt = c.plan_opt;
+    float *h_opt = c.h_opt, *y_opt = c.y_opt, *s_x_opt = c.s_x_opt, *s_h_opt = c.s_h_opt;
+    uint8_t *q_x_opt = c.q_x_opt, *q_h_opt = c.q_h_opt;
+    void* const* events_opt = c.events_opt;
+    void* ws = c.ws;
+    const LayerWs l = layer_ws_layout(M, H, I, E_routed, top_k, dev.sms);
+    char* base = static_cast<char*>(ws);
+    moeq_route_plan plan;
+    if (plan_opt)
+        plan = *plan_opt;
+    else
+        moeq_route_plan_carve(base + l.plan, l.h - l.plan, M, E_routed, top_k, &plan);
+    float* h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
+    float* y = y_opt ? y_opt : reinterpret_cast<float*>(base + l.y);
+    const int mu = moeq_max_uniq(M, E_routed, top_k), mp = moeq_max_pairs(M, top_k);
+
+    // One token on the CUDA cores (no per-pair y asked for): the one-token
+    // kernel, which needs no co-resident grid and no cross-CTA wait.
+    if (M == 1 && M < mma_min_tokens() && !y_opt && token_kernel_enabled() && top_k <= kTokenMaxTopK &&
+        H <= kTokenMaxH && H % 256 == 0) {
+        TokenArgs t = {};
+        t.x = static_cast<const __nv_bfloat16*>(x);
+        t.logits = logits;
+        t.H = H;
+        t.I = I;
+        t.KB = H / 128;
+        t.RB = I / 128;
+        t.E_routed = E_routed;
+        t.top_k = top_k;
+        t.ncols = (top_k + 1) * (I / 128);
+        t.w_gu = w_gu;
+        t.s_gu = s_gu;
+        t.w_d = w_d;
+        t.s_d = s_d;
+        t.out = static_cast<__nv_bfloat16*>(out);
+        t.plan = plan;
+        t.h = h;
+        t.q_x = q_x_opt;
+        t.s_x = s_x_opt;
+        t.q_h = q_h_opt;
+        t.s_h = s_h_opt;
+        t.status = reinterpret_cast<int*>(base + kOffStatus);
+        t.tickets = reinterpret_cast<int*>(base + l.tok_tickets);
+        t.gq = t.tickets + H / 256;
+        t.part = reinterpret_cast<float*>(base + l.dc);
+        t.route_early = route_early ? 1 : 0;
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        if (launch_token(t, dev.sms, pdl_enabled() && allow_pdl, st) != cudaSuccess) return MOEQ_ERR_CUDA;
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        return MOEQ_OK;
+    }
+
+    StreamArgs a = {};
+    Operand& g = a.op[kKindGU];
+    g.w = w_gu;
+    g.sw = s_gu;
+    g.K = H;
+    g.KB = H / 128;
+    g.NB = 2 * I / 128;
+    g.RB = I / 128;
+    g.a = x;
+    g.a_f32 = 0;
+    g.rows_a = M;
+    g.out = h;
+    g.out_ld = I;
+    g.quant_input = 1;
+    g.qdump = q_x_opt;
+    g.sdump = s_x_opt;
+    Operand& d = a.op[kKindDN];
+    d.w = w_d;
+    d.sw = s_d;
+    d.K = I;
+    d.KB = I / 128;
+    d.NB = H / 128;
+    d.RB = H / 128;
+    d.a = h;
+    d.a_f32 = 1;
+    d.rows_a = mp;
+    d.out = y;
+    d.out_ld = H;
+    a.mma = M >= mma_min_tokens();
+    // One token on the CUDA cores (unless y is asked for): down by K group.
+    // The CTA that finished gate_up row block kb of a pair goes on with
+    // down's tiles (nb, kb) for every nb, so no CTA waits for another's h;
+    // a combine over the K groups' sums ends the launch.
+    const int dc_cols = (H + dev.sms - 1) / dev.sms;
+    a.dc = M == 1 && !a.mma && !y_opt && (H / 128) % 2 == 0 && mp * dc_cols <= kDcCombineFloats;
+    // One gate_up block per CTA (whole blocks, as the engine deals them):
+    // each CTA quantises all of x for itself, and down by K group takes the
+    // h group the CTA finished itself from shared memory.
+    const bool one_block = dp_blocks_per_cta_host(static_cast<long long>(mu) * (I / 128), dev.sms) == 1;
+    a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block && !q_x_opt;
+    a.hloc = a.dc && one_block;
+    a.swb = a.xloc && aligned16(s_gu) && (H / 128) % 4 == 0;
+    if (M == 1 || M >= mma_min_tokens()) {
+        // one token, or the tcgen05 path (where a stage costs the same for 1
+        // or 16 tokens): the routed experts' blocks and the shared expert's
+        // cost the same, so each kind is one list, dealt out in whole row
+        // blocks where they nearly fill the grid
+        a.n_lists = 2;
+        a.list_kind[0] = kKindGU;
+        a.list_src[0] = kSrcLayer;
+        a.list_kind[1] = a.dc ? kKindDC : kKindDN;
+        a.list_src[1] = kSrcLayer;
+    } else {
+        // the shared expert serves all M tokens (M times a routed block's
+        // arithmetic): its own lists spread it over every CTA; the routed
+        // experts come in two halves so that down of the first hides the
+        // finish of the second's h
+        a.n_lists = 6;
+        const int kinds[6] = {kKindGU, kKindGU, kKindGU, kKindDN, kKindDN, kKindDN};
+        const int srcs[6] = {kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB, kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB};
+        for (int i = 0; i < 6; ++i) {
+            a.list_kind[i] = kinds[i];
+            a.list_src[i] = srcs[i];
+        }
+    }
+    a.n_uniq = plan.n_uniq;
+    a.uniq = plan.uniq;
+    a.offs = plan.offs;
+    a.pair_tok = plan.pair_tok;
+    a.pair_of = plan.pair_of;
+    a.topk_w = plan.topk_w;
+    a.n_experts = E_routed + 1;
+    a.max_uniq = mu;
+    a.max_pairs = mp;
+    a.max_ntok = M;
+    a.shared_id = E_routed;
+    a.shared_p0 = M * top_k;
+    a.M = M;
+    a.fused_route = 1;
+    a.logits = logits;
+    a.E_routed = E_routed;
+    a.top_k = top_k;
+    a.plan = plan;
+    a.fused_combine = 1;
+    a.out_bf16 = static_cast<__nv_bfloat16*>(out);
+    a.h_to_dn = 1;
+    a.qh_dump = q_h_opt;
+    a.sh_dump = s_h_opt;
+    fill_ws(a, ws, l.s, dev.sms);
+    a.dc_part = reinterpret_cast<float*>(base + l.dc);
+
+    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
+    if (launch_stream(a, dev.sms, true, st) != cudaSuccess) return MOEQ_ERR_CUDA;
+    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
+    return MOEQ_OK;
+}
+
+// ------------------------------------------------------------------ stack
+// A stack's workspace: one layer workspace at offset 0 (its header holds the
+// status word, so moeq_read_device_status reads a stack's workspace as it
+// reads a layer's), then one route plan per layer.
+struct StackWs {
+    size_t layer_bytes, plan0, plan_stride, end;
+};
+
+StackWs stack_ws_layout(int L, size_t layer_bytes, int M, int E_routed, int top_k) {
+    StackWs w;
+    w.layer_bytes = layer_bytes;
+    w.plan0 = align_up(layer_bytes, 256);
+    w.plan_stride = align_up(moeq_route_plan_bytes(M, E_routed, top_k), 256);
+    w.end = w.plan0 + static_cast<size_t>(L) * w.plan_stride;
+    return w;
+}
+
+// Instantiated stack graphs, keyed by the device and every argument of the
+// call that captured them; the least recently used is dropped beyond
+// kStackGraphs (a graph that is still running is freed when it completes).
+struct StackGraph {
+    std::vector<uintptr_t> key;
+    cudaGraphExec_t exec;
+    unsigned long long used;
+};
+constexpr size_t kStackGraphs = 16;
+std::mutex g_stack_mu;
+std::vector<StackGraph> g_stack_graphs;
+unsigned long long g_stack_clock = 0;
+
+// A non-blocking stream per device on which the library captures (capture
+// issues no work, so the caller's stream, which may be the legacy default
+// stream, never needs to be put into capture mode).
+cudaStream_t capture_stream(int dev) {
+    static std::vector<cudaStream_t> streams;
+    if (static_cast<int>(streams.size()) <= dev) streams.resize(dev + 1, nullptr);
+    if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        streams[dev] = nullptr;
+    }
+    return streams[dev];
+}
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -620,168 +873,151 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
                            const moeq_route_plan* plan_opt, float* h_opt, float* y_opt, uint8_t* q_x_opt,
                            float* s_x_opt, uint8_t* q_h_opt, float* s_h_opt, void* const* events_opt, void* ws,
                            size_t ws_bytes, void* stream) {
-    if (!x || !logits || !w_gu || !s_gu || !w_d || !s_d || !out) return MOEQ_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_gu) || !aligned16(w_d) || !aligned16(out) || !aligned4(s_gu) || !aligned4(s_d))
+    const LayerCall c{x,     logits, M,       H,       I,       E_routed, top_k,      w_gu,       s_gu, w_d, s_d,
+                      out,   plan_opt, h_opt, y_opt,   q_x_opt, s_x_opt,  q_h_opt,    s_h_opt,    events_opt,
+                      ws,    ws_bytes};
+    const DeviceInfo dev = current_device();
+    const moeq_status st = layer_check(c, dev);
+    if (st != MOEQ_OK) return st;
+    uintptr_t key = stream_key(stream);
+    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+    return layer_launch(c, dev, false, !after_weight_write, as_stream(stream));
+}
+
+size_t moeq_stack_workspace_size(int L, int M, int H, int I, int n_experts_incl_shared, int top_k) {
+    if (L < 1 || L > MOEQ_MAX_LAYERS) return 0;
+    const size_t lb = moeq_workspace_size(M, H, I, n_experts_incl_shared, top_k);
+    if (!lb) return 0;
+    return stack_ws_layout(L, lb, M, n_experts_incl_shared - 1, top_k).end;
+}
+
+moeq_status moeq_stack_plan(void* ws, size_t ws_bytes, int L, int M, int H, int I, int E_routed, int top_k, int layer,
+                            moeq_route_plan* plan) {
+    if (!ws || !plan || layer < 0 || layer >= L) return MOEQ_ERR_INVALID_ARG;
+    const size_t need = moeq_stack_workspace_size(L, M, H, I, E_routed + 1, top_k);
+    if (!need) return MOEQ_ERR_INVALID_ARG;
+    if (ws_bytes < need) return MOEQ_ERR_WORKSPACE;
+    const StackWs w = stack_ws_layout(L, moeq_workspace_size(M, H, I, E_routed + 1, top_k), M, E_routed, top_k);
+    return moeq_route_plan_carve(static_cast<char*>(ws) + w.plan0 + static_cast<size_t>(layer) * w.plan_stride,
+                                 w.plan_stride, M, E_routed, top_k, plan);
+}
+
+moeq_status moeq_moe_stack(int L, const void* x, const float* logits, int M, int H, int I, int E_routed, int top_k,
+                           const uint8_t* const* w_gu, const float* const* s_gu, const uint8_t* const* w_d,
+                           const float* const* s_d, void* out, int flags, void* ws, size_t ws_bytes, void* stream) {
+    if (L < 1 || L > MOEQ_MAX_LAYERS || !w_gu || !s_gu || !w_d || !s_d || !x || !logits || !out)
         return MOEQ_ERR_INVALID_ARG;
-    if ((h_opt && !aligned16(h_opt)) || (y_opt && !aligned16(y_opt))) return MOEQ_ERR_INVALID_ARG;
-    if ((q_x_opt == nullptr) != (s_x_opt == nullptr) || (q_h_opt == nullptr) != (s_h_opt == nullptr))
-        return MOEQ_ERR_INVALID_ARG;
-    if ((q_x_opt && (!aligned16(q_x_opt) || !aligned4(s_x_opt))) || (q_h_opt && (!aligned16(q_h_opt) || !aligned4(s_h_opt))))
-        return MOEQ_ERR_INVALID_ARG;
-    if (plan_opt && !plan_ok(plan_opt)) return MOEQ_ERR_INVALID_ARG;
+    if (flags & ~MOEQ_STACK_EAGER) return MOEQ_ERR_INVALID_ARG;
     if (!route_args_ok(M, E_routed, top_k)) return MOEQ_ERR_INVALID_ARG;
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K || I > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const LayerWs l = layer_ws_layout(M, H, I, E_routed, top_k, dev.sms);
-    if (!ws || !aligned16(ws) || ws_bytes < l.s.end) return MOEQ_ERR_WORKSPACE;
+    const size_t need = moeq_stack_workspace_size(L, M, H, I, E_routed + 1, top_k);
+    if (!ws || !aligned16(ws) || ws_bytes < need) return MOEQ_ERR_WORKSPACE;
+    const StackWs w = stack_ws_layout(L, moeq_workspace_size(M, H, I, E_routed + 1, top_k), M, E_routed, top_k);
 
-    char* base = static_cast<char*>(ws);
-    moeq_route_plan plan;
-    if (plan_opt)
-        plan = *plan_opt;
-    else
-        moeq_route_plan_carve(base + l.plan, l.h - l.plan, M, E_routed, top_k, &plan);
-    float* h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
-    float* y = y_opt ? y_opt : reinterpret_cast<float*>(base + l.y);
-    const int mu = moeq_max_uniq(M, E_routed, top_k), mp = moeq_max_pairs(M, top_k);
+    // every layer's call, checked before anything is launched or captured
+    std::vector<LayerCall> calls(L);
+    std::vector<moeq_route_plan> plans(L);
+    const size_t x_bytes = static_cast<size_t>(M) * H * 2;
+    for (int l = 0; l < L; ++l) {
+        moeq_stack_plan(ws, ws_bytes, L, M, H, I, E_routed, top_k, l, &plans[l]);
+        LayerCall& c = calls[l];
+        c = LayerCall{};
+        c.x = l == 0 ? x : static_cast<const char*>(out) + (l - 1) * x_bytes;
+        c.logits = logits + static_cast<size_t>(l) * M * E_routed;
+        c.M = M;
+        c.H = H;
+        c.I = I;
+        c.E_routed = E_routed;
+        c.top_k = top_k;
+        c.w_gu = w_gu[l];
+        c.s_gu = s_gu[l];
+        c.w_d = w_d[l];
+        c.s_d = s_d[l];
+        c.out = static_cast<char*>(out) + l * x_bytes;
+        c.plan_opt = &plans[l];
+        c.ws = ws;
+        c.ws_bytes = w.layer_bytes;
+        const moeq_status st = layer_check(c, dev);
+        if (st != MOEQ_OK) return st;
+    }
     cudaStream_t st = as_stream(stream);
+    uintptr_t skey = stream_key(stream);
+    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(skey, 0);
 
-    // One token on the CUDA cores (no per-pair y asked for): the one-token
-    // kernel, which needs no co-resident grid and no cross-CTA wait.
-    if (M == 1 && M < mma_min_tokens() && !y_opt && token_kernel_enabled() && top_k <= kTokenMaxTopK &&
-        H <= kTokenMaxH && H % 256 == 0) {
-        TokenArgs t = {};
-        t.x = static_cast<const __nv_bfloat16*>(x);
-        t.logits = logits;
-        t.H = H;
-        t.I = I;
-        t.KB = H / 128;
-        t.RB = I / 128;
-        t.E_routed = E_routed;
-        t.top_k = top_k;
-        t.ncols = (top_k + 1) * (I / 128);
-        t.w_gu = w_gu;
-        t.s_gu = s_gu;
-        t.w_d = w_d;
-        t.s_d = s_d;
-        t.out = static_cast<__nv_bfloat16*>(out);
-        t.plan = plan;
-        t.h = h;
-        t.q_x = q_x_opt;
-        t.s_x = s_x_opt;
-        t.q_h = q_h_opt;
-        t.s_h = s_h_opt;
-        t.status = reinterpret_cast<int*>(base + kOffStatus);
-        t.tickets = reinterpret_cast<int*>(base + l.tok_tickets);
-        t.gq = t.tickets + H / 256;
-        t.part = reinterpret_cast<float*>(base + l.dc);
-        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
-            return MOEQ_ERR_CUDA;
-        uintptr_t key = stream_key(stream);
-        const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
-        if (launch_token(t, dev.sms, pdl_enabled() && !after_weight_write, st) != cudaSuccess) return MOEQ_ERR_CUDA;
-        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
-            return MOEQ_ERR_CUDA;
-        return MOEQ_OK;
-    }
-
-    StreamArgs a = {};
-    Operand& g = a.op[kKindGU];
-    g.w = w_gu;
-    g.sw = s_gu;
-    g.K = H;
-    g.KB = H / 128;
-    g.NB = 2 * I / 128;
-    g.RB = I / 128;
-    g.a = x;
-    g.a_f32 = 0;
-    g.rows_a = M;
-    g.out = h;
-    g.out_ld = I;
-    g.quant_input = 1;
-    g.qdump = q_x_opt;
-    g.sdump = s_x_opt;
-    Operand& d = a.op[kKindDN];
-    d.w = w_d;
-    d.sw = s_d;
-    d.K = I;
-    d.KB = I / 128;
-    d.NB = H / 128;
-    d.RB = H / 128;
-    d.a = h;
-    d.a_f32 = 1;
-    d.rows_a = mp;
-    d.out = y;
-    d.out_ld = H;
-    a.mma = M >= mma_min_tokens();
-    // One token on the CUDA cores (unless y is asked for): down by K group.
-    // The CTA that finished gate_up row block kb of a pair goes on with
-    // down's tiles (nb, kb) for every nb, so no CTA waits for another's h;
-    // a combine over the K groups' sums ends the launch.
-    const int dc_cols = (H + dev.sms - 1) / dev.sms;
-    a.dc = M == 1 && !a.mma && !y_opt && (H / 128) % 2 == 0 && mp * dc_cols <= kDcCombineFloats;
-    // One gate_up block per CTA (whole blocks, as the engine deals them):
-    // each CTA quantises all of x for itself, and down by K group takes the
-    // h group the CTA finished itself from shared memory.
-    const bool one_block = dp_blocks_per_cta_host(static_cast<long long>(mu) * (I / 128), dev.sms) == 1;
-    a.xloc = M == 1 && !a.mma && H <= kXLocalMaxK && one_block && !q_x_opt;
-    a.hloc = a.dc && one_block;
-    a.swb = a.xloc && aligned16(s_gu) && (H / 128) % 4 == 0;
-    if (M == 1 || M >= mma_min_tokens()) {
-        // one token, or the tcgen05 path (where a stage costs the same for 1
-        // or 16 tokens): the routed experts' blocks and the shared expert's
-        // cost the same, so each kind is one list, dealt out in whole row
-        // blocks where they nearly fill the grid
-        a.n_lists = 2;
-        a.list_kind[0] = kKindGU;
-        a.list_src[0] = kSrcLayer;
-        a.list_kind[1] = a.dc ? kKindDC : kKindDN;
-        a.list_src[1] = kSrcLayer;
-    } else {
-        // the shared expert serves all M tokens (M times a routed block's
-        // arithmetic): its own lists spread it over every CTA; the routed
-        // experts come in two halves so that down of the first hides the
-        // finish of the second's h
-        a.n_lists = 6;
-        const int kinds[6] = {kKindGU, kKindGU, kKindGU, kKindDN, kKindDN, kKindDN};
-        const int srcs[6] = {kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB, kSrcShared, kSrcPlanRoutedA, kSrcPlanRoutedB};
-        for (int i = 0; i < 6; ++i) {
-            a.list_kind[i] = kinds[i];
-            a.list_src[i] = srcs[i];
+    // Layer l > 0 reads logits that no layer of the stack writes, so it may
+    // route before it waits for layer l - 1; layer 0 follows whatever came
+    // before it on the stream.
+    auto launch_all = [&](cudaStream_t s, bool first_pdl) -> moeq_status {
+        for (int l = 0; l < L; ++l) {
+            const moeq_status r = layer_launch(calls[l], dev, l > 0, l > 0 || first_pdl, s);
+            if (r != MOEQ_OK) return r;
         }
+        return MOEQ_OK;
+    };
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return MOEQ_ERR_CUDA;
     }
-    a.n_uniq = plan.n_uniq;
-    a.uniq = plan.uniq;
-    a.offs = plan.offs;
-    a.pair_tok = plan.pair_tok;
-    a.pair_of = plan.pair_of;
-    a.topk_w = plan.topk_w;
-    a.n_experts = E_routed + 1;
-    a.max_uniq = mu;
-    a.max_pairs = mp;
-    a.max_ntok = M;
-    a.shared_id = E_routed;
-    a.shared_p0 = M * top_k;
-    a.M = M;
-    a.fused_route = 1;
-    a.logits = logits;
-    a.E_routed = E_routed;
-    a.top_k = top_k;
-    a.plan = plan;
-    a.fused_combine = 1;
-    a.out_bf16 = static_cast<__nv_bfloat16*>(out);
-    a.h_to_dn = 1;
-    a.qh_dump = q_h_opt;
-    a.sh_dump = s_h_opt;
-    fill_ws(a, ws, l.s, dev.sms);
-    a.dc_part = reinterpret_cast<float*>(base + l.dc);
+    // Eager on request, and inside the caller's own capture (the launches
+    // become part of the caller's graph).
+    if ((flags & MOEQ_STACK_EAGER) || cap != cudaStreamCaptureStatusNone) return launch_all(st, !after_weight_write);
 
-    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
-        return MOEQ_ERR_CUDA;
-    if (launch_stream(a, dev.sms, true, st) != cudaSuccess) return MOEQ_ERR_CUDA;
-    if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
-        return MOEQ_ERR_CUDA;
+    int devid = 0;
+    if (cudaGetDevice(&devid) != cudaSuccess) return MOEQ_ERR_CUDA;
+    std::vector<uintptr_t> key = {static_cast<uintptr_t>(devid), static_cast<uintptr_t>(L), static_cast<uintptr_t>(M),
+                                  static_cast<uintptr_t>(H), static_cast<uintptr_t>(I),
+                                  static_cast<uintptr_t>(E_routed), static_cast<uintptr_t>(top_k),
+                                  reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(logits),
+                                  reinterpret_cast<uintptr_t>(out), reinterpret_cast<uintptr_t>(ws), ws_bytes};
+    for (int l = 0; l < L; ++l) {
+        key.push_back(reinterpret_cast<uintptr_t>(w_gu[l]));
+        key.push_back(reinterpret_cast<uintptr_t>(s_gu[l]));
+        key.push_back(reinterpret_cast<uintptr_t>(w_d[l]));
+        key.push_back(reinterpret_cast<uintptr_t>(s_d[l]));
+    }
+    std::lock_guard<std::mutex> lock(g_stack_mu);
+    StackGraph* hit = nullptr;
+    for (StackGraph& g : g_stack_graphs)
+        if (g.key == key) hit = &g;
+    if (!hit) {
+        // capture on first use
+        cudaStream_t cs = capture_stream(devid);
+        if (!cs) return MOEQ_ERR_CUDA;
+        if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+            cudaGetLastError();
+            return MOEQ_ERR_CUDA;
+        }
+        const moeq_status r = launch_all(cs, false);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+        cudaGraphExec_t exec = nullptr;
+        const bool ok = r == MOEQ_OK && e == cudaSuccess && graph &&
+                        cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+        if (graph) cudaGraphDestroy(graph);
+        if (!ok) {
+            cudaGetLastError();
+            return r != MOEQ_OK ? r : MOEQ_ERR_CUDA;
+        }
+        if (g_stack_graphs.size() >= kStackGraphs) {
+            auto lru = std::min_element(g_stack_graphs.begin(), g_stack_graphs.end(),
+                                        [](const StackGraph& a, const StackGraph& b) { return a.used < b.used; });
+            cudaGraphExecDestroy(lru->exec);
+            g_stack_graphs.erase(lru);
+        }
+        g_stack_graphs.push_back(StackGraph{std::move(key), exec, 0});
+        hit = &g_stack_graphs.back();
+    }
+    hit->used = ++g_stack_clock;
+    return cuda_status(cudaGraphLaunch(hit->exec, st));
+}
+
+moeq_status moeq_stack_release_graphs(void) {
+    std::lock_guard<std::mutex> lock(g_stack_mu);
+    for (StackGraph& g : g_stack_graphs) cudaGraphExecDestroy(g.exec);
+    g_stack_graphs.clear();
     return MOEQ_OK;
 }
 

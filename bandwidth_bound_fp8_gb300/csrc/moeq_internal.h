@@ -137,6 +137,9 @@ struct TokenArgs {
     int* tickets;                // [H/256] arrivals per output unit, zero between launches
     int* gq;                     // kGqUnits ints, zero between launches
     float* part;                 // [H/256][16][ncols][16] down partials
+    int route_early;             // 1: the logits are not written by the kernel ahead on the stream,
+                                 // so the token is routed (and its first column started) before
+                                 // griddepcontrol.wait
 };
 // Completion state of the one-token kernel (ints): CTAs finished.
 constexpr int kGqCtas = 0, kGqUnits = 4;

@@ -232,13 +232,13 @@ __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int
     }
     prefetch_shared_expert(a, lane);
     // The shared expert's columns (the first RB) need no plan: start them now.
+    // When the logits are known not to come from the kernel ahead, the token
+    // is routed now too, and a routed first column starts as well.
+    const bool routed_now = a.route_early && k > 0;
+    if (routed_now) producer_route(a, sm, lane);
     int pre = 0;
-    if (c < a.ncols && c < a.RB) {
-        Column col;
-        col.g = 0;
-        col.kb = c;
-        col.expert = a.E_routed;
-        col.pair = k;
+    if (c < a.ncols && (c < a.RB || routed_now)) {
+        const Column col = column(a, sm, c);
         pre = min(kStages, stages_per_col);
         if (lane == 0)
             for (int t = 0; t < pre; ++t) issue_stage(a, sm, stages, col, t, issued++, pol);
@@ -247,7 +247,7 @@ __device__ void producer_warp(const TokenArgs& a, Smem& sm, uint8_t* stages, int
     pdl_wait();
     if (k == 0) {   // a dense FFN: the one expert, no routing
         if (lane == 0) mbar_arrive(&sm.plan_bar);
-    } else {
+    } else if (!routed_now) {
         producer_route(a, sm, lane);
     }
     if (lane != 0) return;
@@ -574,21 +574,22 @@ __device__ void ticket_warp(const TokenArgs& a, Smem& sm, int lane) {
 __device__ void consumer_warp(const TokenArgs& a, Smem& sm, const uint8_t* stages, int cw, int lane) {
     const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x;
     if (c < a.ncols) {
-        const bool shared_first = c < a.RB;   // the first column is the shared expert's: known before routing
-        if (shared_first) {
-            Column col;
-            col.g = 0;
-            col.kb = c;
-            col.expert = a.E_routed;
-            col.pair = a.top_k;
-            load_column_scales(a, sm, col, tid);
+        // the first column is known before griddepcontrol.wait when it is the
+        // shared expert's, or when the token is routed ahead of the wait
+        const bool first_early = c < a.RB || (a.route_early && a.top_k > 0);
+        if (first_early) {
+            if (c >= a.RB) {
+                if (lane == 0) wait_or_abort(&sm.plan_bar, 0, sm, a.status);
+                __syncwarp();
+            }
+            load_column_scales(a, sm, column(a, sm, c), tid);
         }
         pdl_wait();
         quantise_x(a, sm, cw, lane);
         long long it = 0;
         int stored = 0;
         for (int j = c; j < a.ncols; j += G) {
-            if (j != c || !shared_first) {
+            if (j != c || !first_early) {
                 if (lane == 0) wait_or_abort(&sm.plan_bar, 0, sm, a.status);
                 __syncwarp();
                 consumer_sync();   // the previous column's scales are no longer read

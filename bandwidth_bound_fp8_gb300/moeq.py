@@ -27,6 +27,8 @@ MOEQ_BF16 = 0
 MOEQ_F32 = 1
 MOEQ_GROUP = 128
 MOEQ_MAX_TOKENS = 16
+MOEQ_MAX_LAYERS = 256
+MOEQ_STACK_EAGER = 1
 
 # Every symbol include/moeq.h declares (checked by the tests against the header).
 EXPORTS = [
@@ -35,7 +37,8 @@ EXPORTS = [
     "moeq_gemm_workspace_size", "moeq_workspace_init", "moeq_read_device_status",
     "moeq_quant_act", "moeq_quant_weight", "moeq_pack_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
     "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer", "moeq_expert_gemm_down_noalloc",
-    "moeq_dense_ffn_workspace_size", "moeq_dense_ffn",
+    "moeq_dense_ffn_workspace_size", "moeq_dense_ffn", "moeq_stack_workspace_size", "moeq_moe_stack",
+    "moeq_stack_plan", "moeq_stack_release_graphs",
 ]
 
 
@@ -88,6 +91,10 @@ def load(path: str = LIB_PATH):
                                                _vp, _vp, _vp, _vp, _vp]),
         "moeq_dense_ffn_workspace_size": (_sz, [_i, _i, _i]),
         "moeq_dense_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+        "moeq_stack_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+        "moeq_moe_stack": (_i, [_i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp]),
+        "moeq_stack_plan": (_i, [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(moeq_route_plan)]),
+        "moeq_stack_release_graphs": (_i, []),
         "moeq_moe_layer": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                                 ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                 _sz, _vp]),
@@ -160,24 +167,30 @@ def moeq_gemm_workspace_size(rows_out, K, rows_in, max_uniq, is_gate_up) -> int:
 
 
 class RoutePlan:
-    """A route plan in one device buffer, with torch views of its members."""
+    """A route plan in one device buffer, with torch views of its members.
+    `within` = (uint8 tensor, moeq_route_plan) views a plan already carved
+    inside that buffer (e.g. a stack workspace's) instead of allocating one."""
 
-    def __init__(self, M: int, E_routed: int, top_k: int, device="cuda"):
+    def __init__(self, M: int, E_routed: int, top_k: int, device="cuda", within=None):
         L = load()
         self.M, self.E, self.k = M, E_routed, top_k
-        nbytes = L.moeq_route_plan_bytes(M, E_routed, top_k)
-        if not nbytes:
-            raise MoeqError("moeq_route_plan_bytes", MOEQ_ERR_INVALID_ARG)
-        self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
-        self.c = moeq_route_plan()
-        _check("moeq_route_plan_carve",
-               L.moeq_route_plan_carve(self.buf.data_ptr(), nbytes, M, E_routed, top_k, ctypes.byref(self.c)))
+        if within is None:
+            nbytes = L.moeq_route_plan_bytes(M, E_routed, top_k)
+            if not nbytes:
+                raise MoeqError("moeq_route_plan_bytes", MOEQ_ERR_INVALID_ARG)
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+            self.c = moeq_route_plan()
+            _check("moeq_route_plan_carve",
+                   L.moeq_route_plan_carve(self.buf.data_ptr(), nbytes, M, E_routed, top_k, ctypes.byref(self.c)))
+        else:
+            self.buf, self.c = within
         self.max_uniq = L.moeq_max_uniq(M, E_routed, top_k)
         self.max_pairs = L.moeq_max_pairs(M, top_k)
         base = self.buf.data_ptr()
 
         def view(field, n, dt):
             off = getattr(self.c, field) - base
+            assert 0 <= off and off + 4 * n <= self.buf.numel(), "plan outside its buffer"
             return self.buf[off:off + 4 * n].view(dt)
 
         self.topk_id = view("topk_id", M * top_k, torch.int32).view(M, top_k)
@@ -295,3 +308,32 @@ def moeq_moe_layer(x, logits, H, I, E_routed, top_k, w_gu, s_gu, w_d, s_d, out, 
         _p(x), _p(logits), M, H, I, E_routed, top_k, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(out),
         ctypes.byref(plan.c) if plan is not None else None, _p(h), _p(y), _p(q_x), _p(s_x), _p(q_h), _p(s_h),
         ev, ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def moeq_stack_workspace_size(L, M, H, I, n_experts_incl_shared, top_k) -> int:
+    return int(load().moeq_stack_workspace_size(L, M, H, I, n_experts_incl_shared, top_k))
+
+
+def moeq_moe_stack(x, logits, H, I, E_routed, top_k, w_gu, s_gu, w_d, s_d, out, ws: Workspace, flags=0,
+                   stream=None) -> None:
+    """L layers in sequence (L = len(w_gu)); logits [L, M, E_routed], out
+    [L, M, H]; w_gu .. s_d: sequences of L tensors (or device pointers)."""
+    Ln, M = len(w_gu), x.shape[0]
+    if not (len(s_gu) == len(w_d) == len(s_d) == Ln):
+        raise ValueError("moeq_moe_stack: one weight set per layer")
+    arr = lambda ts: (ctypes.c_void_p * Ln)(*[_p(t) for t in ts])
+    _check("moeq_moe_stack", load().moeq_moe_stack(
+        Ln, _p(x), _p(logits), M, H, I, E_routed, top_k, arr(w_gu), arr(s_gu), arr(w_d), arr(s_d), _p(out),
+        int(flags), ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def moeq_stack_plan(ws: Workspace, L, M, H, I, E_routed, top_k, layer) -> RoutePlan:
+    """Layer `layer`'s route plan inside a stack workspace, as a RoutePlan view."""
+    c = moeq_route_plan()
+    _check("moeq_stack_plan", load().moeq_stack_plan(ws.ptr, ws.nbytes, L, M, H, I, E_routed, top_k, layer,
+                                                     ctypes.byref(c)))
+    return RoutePlan(M, E_routed, top_k, within=(ws.t, c))
+
+
+def moeq_stack_release_graphs() -> None:
+    _check("moeq_stack_release_graphs", load().moeq_stack_release_graphs())

@@ -312,6 +312,42 @@ def bench_M(stack, M, steps, warmup, ws_world, seed, isolated=64):
                 xs=xs, lg=lg, U=U, ws=ws)
 
 
+def bench_stack(stack, M, calls, seed, peak):
+    """The L-layer stack through moeq_moe_stack: one call = one decode step
+    through every layer (one CUDA graph launch; the first call captures it).
+    Layer l routes its own seeded logits; x is the previous layer's output.
+    Timed: `calls` calls back to back, events at the region's two ends.
+    Every call reads each layer's experts cold (the stack's weights are far
+    larger than L2)."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    L = stack.L
+    x = synth.activations_bf16(M, H, seed, CFG["n_outlier"], CFG["outlier_scale"], device="cuda")
+    logits = torch.stack([synth.logits_f32(M, E, seed + 1 + l, device="cuda") for l in range(L)])
+    out = torch.empty((L, M, H), dtype=torch.bfloat16, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_stack_workspace_size(L, M, H, I, E + 1, TOPK))
+    w = ([stack.gu_q[l] for l in range(L)], [stack.gu_s[l] for l in range(L)],
+         [stack.dn_q[l] for l in range(L)], [stack.dn_s[l] for l in range(L)])
+    for _ in range(3):
+        moeq.moeq_moe_stack(x, logits, H, I, E, TOPK, *w, out, ws)
+    torch.cuda.synchronize()
+    U = [int(moeq.moeq_stack_plan(ws, L, M, H, I, E, TOPK, l).n_uniq.item()) for l in range(L)]
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(calls):
+        moeq.moeq_moe_stack(x, logits, H, I, E, TOPK, *w, out, ws)
+    e.record()
+    torch.cuda.synchronize()
+    if moeq.moeq_read_device_status(ws.t, ws.nbytes) != 0:
+        raise RuntimeError("device status word set during the stack bench")
+    ms = a.elapsed_time(e)
+    byts = calls * sum(U) * EXPERT_BYTES
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"layers": L, "calls": calls, "us_per_layer": round(ms * 1e3 / (calls * L), 2),
+            "us_per_step": round(ms * 1e3 / calls, 1), "weight_GBps": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "frac_of_8TBps": round(gbs / 8000, 4),
+            "U_per_layer": U}
+
+
 def bench_e2e(stack, M, steps, seed):
     """Same metric through the public call, with host<->device copies per step:
     each step copies its x and logits from pinned host memory and reads its
@@ -706,6 +742,8 @@ def main():
                     help="run a few launches of the small ncu case (8 routed experts, top-8) and exit")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--no-dense", action="store_true", help="skip the dense configurations and the gate_up ladder")
+    ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack sweep")
+    ap.add_argument("--stack-calls", type=int, default=40)
     ap.add_argument("--ladder-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.profile_case:
@@ -764,6 +802,11 @@ def main():
                               "U_mean": rr["U_mean"],
                               "isolated_launch_us": round(rr["isolated_ms"] * 1e3, 2)}
             del rr
+    stack_sweep = {}
+    if not args.no_stack and rank == 0:
+        for M in (1, 2, 4, 8, 16):
+            stack_sweep[f"M{M}"] = bench_stack(stack, M, args.stack_calls, seed=8000 + 37 * M, peak=peak)
+        stack_sweep["call"] = "moeq_moe_stack (one CUDA graph per step through all layers)"
     dense = None
     if rank == 0 and not args.no_dense:
         dense = bench_dense(peak, with_oracle=not args.no_cpu)
@@ -795,7 +838,7 @@ def main():
             "kernel_us": round(r["kernel_ms"] * 1e3, 3),
             "isolated_launch_us": round(r["isolated_ms"] * 1e3, 3),
             "roofline": roof, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-            "gpu_launches": args.steps, "sweep": sweep, "dense": dense,
+            "gpu_launches": args.steps, "sweep": sweep, "stack": stack_sweep, "dense": dense,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -77,6 +77,8 @@ typedef enum moeq_dtype { MOEQ_BF16 = 0, MOEQ_F32 = 1 } moeq_dtype;
 #define MOEQ_MAX_EXPERTS 1024   /* routed experts limit of moeq_route */
 #define MOEQ_MAX_TOPK 16
 #define MOEQ_MAX_K 32768        /* K (H or I) limit of the GEMM calls */
+#define MOEQ_MAX_LAYERS 256     /* L limit of moeq_moe_stack */
+#define MOEQ_STACK_EAGER 1      /* moeq_moe_stack flag: launch the layers directly, no graph */
 
 /* Human-readable text of a status (static storage, never NULL). */
 const char* moeq_status_string(moeq_status s);
@@ -309,9 +311,11 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I,
 /*   H % 256 == 0: the one-token kernel.  One CTA per (expert, 128-wide K   */
 /*   group of down): it streams that h group's gate and up rows, forms and  */
 /*   quantises the group itself, and streams down's K group against every  */
-/*   output row; the fp32 partials of each 256 output rows are summed, and  */
-/*   the bf16 output formed, by the CTA whose contribution arrives last     */
-/*   (atomic ticket), so no CTA waits for another.  It is launched with     */
+/*   output row; each column's fp32 partials already carry its routing     */
+/*   weight, and each 256 output rows' partials are summed in a fixed order */
+/*   (and the bf16 output formed) by warps with no stream of their own once */
+/*   the unit's arrival count is full; no stream waits for another CTA.     */
+/*   It is launched with                                                   */
 /*   programmatic dependent launch: the next kernel on the stream may start */
 /*   as its CTAs finish, and waits (griddepcontrol.wait) before it reads    */
 /*   anything this one writes.                                              */
@@ -351,6 +355,52 @@ moeq_status moeq_moe_layer(const void* x, const float* logits,
                            uint8_t* q_h_opt, float* s_h_opt,
                            void* const* events_opt,
                            void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moeq_moe_stack -- one decode step through L MoE layers in sequence, as   */
+/*   ONE CUDA graph (GLM-5.2 x10 §8b: graph replay takes the host's         */
+/*   per-kernel launch cost out of a decode step).  Layer l runs            */
+/*   moeq_moe_layer on x_l (x_0 = x, x_l = layer l-1's bf16 output) with     */
+/*   its own logits and weights.  The first call with a given set of        */
+/*   arguments captures the L launches and instantiates the graph; every    */
+/*   later call with the same arguments (pointers included) launches it on  */
+/*   `stream`, so new data in the same buffers needs no host work.  Up to   */
+/*   16 graphs are kept per process (least recently used dropped); a call   */
+/*   made while `stream` is being captured by the caller, or with           */
+/*   MOEQ_STACK_EAGER, launches the layers directly instead.                */
+/*   Layers after the first route before they wait for the layer ahead     */
+/*   (their logits are inputs, which no layer writes).                      */
+/*   L      1 .. MOEQ_MAX_LAYERS                                            */
+/*   x      [M, H] bf16                                                     */
+/*   logits [L, M, E_routed] fp32, contiguous                               */
+/*   w_gu, s_gu, w_d, s_d: HOST arrays of L device pointers, layer l's      */
+/*           weights as moeq_moe_layer takes them (read during the call;    */
+/*           the arrays may be freed after it)                              */
+/*   out    [L, M, H] bf16: every layer's output (layer L-1's is the        */
+/*           stack's); must not overlap x, logits or the weights            */
+/*   flags  0 or MOEQ_STACK_EAGER                                           */
+/*   ws     moeq_stack_workspace_size(L, M, H, I, E_routed + 1, top_k)      */
+/*           bytes, zeroed once with moeq_workspace_init; it holds one      */
+/*           layer workspace and every layer's route plan (moeq_stack_plan  */
+/*           gives layer l's).  A graph records the workspace's address: do */
+/*           not free a workspace while a call that used it may still run.  */
+/* Errors: every layer's arguments are checked before anything is launched  */
+/* or captured (the statuses of moeq_moe_layer); a failed capture or        */
+/* instantiation returns MOEQ_ERR_CUDA and keeps nothing.                   */
+/* ------------------------------------------------------------------------ */
+size_t moeq_stack_workspace_size(int L, int M, int H, int I, int n_experts_incl_shared, int top_k);
+moeq_status moeq_moe_stack(int L, const void* x, const float* logits,
+                           int M, int H, int I, int E_routed, int top_k,
+                           const uint8_t* const* w_gu, const float* const* s_gu,
+                           const uint8_t* const* w_d, const float* const* s_d,
+                           void* out, int flags, void* ws, size_t ws_bytes, void* stream);
+/* Layer `layer`'s route plan inside a stack workspace (pointers only; the  */
+/* plan is written by the stack's calls).                                   */
+moeq_status moeq_stack_plan(void* ws, size_t ws_bytes, int L, int M, int H, int I, int E_routed, int top_k,
+                            int layer, moeq_route_plan* plan);
+/* Destroy every graph moeq_moe_stack keeps (a graph still running is freed */
+/* when it completes).  The next stack call captures again.                 */
+moeq_status moeq_stack_release_graphs(void);
 
 #ifdef __cplusplus
 }

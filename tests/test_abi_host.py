@@ -120,3 +120,13 @@ def test_dense_ffn_workspace_size_rejects_shapes(lib):
     assert lib.moeq_dense_ffn_workspace_size(1, 8192, 256) == 0
     assert lib.moeq_dense_ffn_workspace_size(1, 512, 200) == 0
     assert lib.moeq_dense_ffn_workspace_size(1, 512, 256) > 0
+
+
+def test_stack_rejects_layer_count_before_the_device(lib):
+    """moeq_moe_stack checks L (1 .. MOEQ_MAX_LAYERS) before it looks for a
+    device; the workspace size is 0 outside that range."""
+    assert lib.moeq_stack_workspace_size(0, 1, 512, 256, 17, 4) == 0
+    assert lib.moeq_stack_workspace_size(257, 1, 512, 256, 17, 4) == 0
+    arr = (ctypes.c_void_p * 1)(16)
+    st = lib.moeq_moe_stack(0, 16, 16, 1, 512, 256, 16, 4, arr, arr, arr, arr, 16, 0, 16, 1 << 20, None)
+    assert st == 1   # MOEQ_ERR_INVALID_ARG
