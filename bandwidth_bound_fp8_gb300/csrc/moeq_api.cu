@@ -74,6 +74,12 @@ bool pdl_enabled() {
     static const bool v = env_flag("MOEQ_PDL", true);
     return v;
 }
+// Layers of 2..16 tokens run the multi-token kernel unless
+// MOEQ_MTOK_KERNEL=0 (then the persistent engine does).  Read once.
+bool mtok_kernel_enabled() {
+    static const bool v = env_flag("MOEQ_MTOK_KERNEL", true);
+    return v;
+}
 // The standalone GEMM calls spread over every SM; MOEQ_GRID_LIMIT=n (read
 // once) caps them at n CTAs, for experiments that compare split widths.
 int gemm_grid(int sms) {
@@ -142,6 +148,7 @@ StreamWs stream_ws_layout(size_t base, const int* aq_rows, const int* aq_k, int 
 
 struct LayerWs {
     size_t plan, h, y, dc, tok_tickets;
+    size_t mt_cnt, mt_slots, mt_xq, mt_xs, mt_part;   // multi-token kernel (M >= 2)
     StreamWs s;
 };
 
@@ -156,8 +163,18 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     // one token: the token kernel's partials share that area; its arrival
     // counts (one per 256 output rows) and completion count follow
     l.tok_tickets = align_up(l.dc + (M == 1 ? sizeof(float) * static_cast<size_t>(mp) * (I / 128) * H : 0), 256);
-    const size_t after =
+    const size_t tok_end =
         l.tok_tickets + (M == 1 ? sizeof(int) * (static_cast<size_t>((H + 255) / 256) + kGqUnits) : 0);
+    // M >= 2: the multi-token kernel's counts and flags, split-column slots,
+    // x's codes and scales, and the down partials
+    const bool mt = M >= 2;
+    l.mt_cnt = align_up(tok_end, 256);
+    l.mt_slots = align_up(l.mt_cnt + (mt ? sizeof(int) * (kMtokFlags + grid + 1) : 0), 256);
+    l.mt_xq = align_up(l.mt_slots + (mt ? static_cast<size_t>(grid + 1) * kMtokSlotBytes : 0), 256);
+    l.mt_xs = align_up(l.mt_xq + (mt ? static_cast<size_t>(H / 128) * kMtokXGroupBytes : 0), 256);
+    l.mt_part = align_up(l.mt_xs + (mt ? sizeof(float) * static_cast<size_t>(H / 128) * 16 : 0), 256);
+    const size_t after =
+        l.mt_part + (mt ? sizeof(float) * static_cast<size_t>(M) * H * (k + 1) * (I / 128) : 0);
     // tickets of the layer's lists: M == 1 uses the first two (whole lists),
     // M > 1 all six (shared, half A, half B of each kind)
     const int rbmax = mu * ((H > I ? H : I) / 128);
@@ -327,6 +344,44 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
             return MOEQ_ERR_CUDA;
         if (launch_token(t, dev.sms, pdl_enabled() && allow_pdl, st) != cudaSuccess) return MOEQ_ERR_CUDA;
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        return MOEQ_OK;
+    }
+
+    // 2..16 tokens (no per-pair y asked for): the multi-token kernel, on the
+    // tensor cores, with no cross-CTA wait inside its streams.
+    if (M >= 2 && !y_opt && mtok_kernel_enabled() && top_k <= kMtokMaxTopK && H <= kTokenMaxH && H % 256 == 0) {
+        MtokArgs t = {};
+        t.x = static_cast<const __nv_bfloat16*>(x);
+        t.logits = logits;
+        t.M = M;
+        t.H = H;
+        t.I = I;
+        t.KB = H / 128;
+        t.RB = I / 128;
+        t.E_routed = E_routed;
+        t.top_k = top_k;
+        t.w_gu = w_gu;
+        t.s_gu = s_gu;
+        t.w_d = w_d;
+        t.s_d = s_d;
+        t.out = static_cast<__nv_bfloat16*>(out);
+        t.plan = plan;
+        t.h = h;
+        t.q_x = q_x_opt;
+        t.s_x = s_x_opt;
+        t.q_h = q_h_opt;
+        t.s_h = s_h_opt;
+        t.status = reinterpret_cast<int*>(base + kOffStatus);
+        t.cnt = reinterpret_cast<int*>(base + l.mt_cnt);
+        t.slots = reinterpret_cast<uint8_t*>(base + l.mt_slots);
+        t.xq = reinterpret_cast<uint8_t*>(base + l.mt_xq);
+        t.xs = reinterpret_cast<float*>(base + l.mt_xs);
+        t.part = reinterpret_cast<float*>(base + l.mt_part);
+        if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        if (launch_mtok(t, dev.sms, pdl_enabled() && allow_pdl, st) != cudaSuccess) return MOEQ_ERR_CUDA;
         if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[1]), st) != cudaSuccess)
             return MOEQ_ERR_CUDA;
         return MOEQ_OK;

@@ -146,6 +146,40 @@ constexpr int kGqCtas = 0, kGqUnits = 4;
 
 cudaError_t launch_token(const TokenArgs& args, int grid, bool pdl, cudaStream_t stream);
 
+// The multi-token layer kernel (moeq_mtok.cu): 2..16 tokens on the tcgen05
+// tensor cores, H a multiple of 256 up to kTokenMaxH, top_k up to 16.
+struct MtokArgs {
+    const __nv_bfloat16* x;      // [M, H]
+    const float* logits;         // [M, E_routed]
+    int M, H, I, KB, RB;         // KB = H/128, RB = I/128
+    int E_routed, top_k;
+    const uint8_t* w_gu;         // tile-major [E_routed + 1, 2I, H]
+    const float* s_gu;           // [E_routed + 1, 2I/128, H/128]
+    const uint8_t* w_d;          // tile-major [E_routed + 1, H, I]
+    const float* s_d;            // [E_routed + 1, H/128, I/128]
+    __nv_bfloat16* out;          // [M, H]
+    moeq_route_plan plan;        // written by CTA 0
+    float* h;                    // [max_pairs, I]
+    uint8_t* q_x;                // optional [M, H] and [M, H/128]: x's codes and scales
+    float* s_x;
+    uint8_t* q_h;                // optional [max_pairs, I] and [max_pairs, I/128]: h's codes and scales
+    float* s_h;
+    int* status;
+    int* cnt;                    // kMtokFlags + grid + 1 ints, zero between launches
+    uint8_t* slots;              // [grid + 1][kMtokSlotBytes]: what a split column's head publishes
+    uint8_t* xq;                 // [KB][16 * 128]: x's codes, token n in row n (gate_up's B operand)
+    float* xs;                   // [KB][16]: x's scales
+    float* part;                 // [M][H/256][16][top_k + 1][RB][16] down partials
+};
+// counts (ints): CTAs done streaming, CTAs done summing, quantised groups
+// per K group of x, and the split columns' flags (one per CTA boundary)
+constexpr int kMtokDone = 0, kMtokFin = 1, kMtokX = 2, kMtokFlags = kMtokX + kTokenMaxH / 128;
+constexpr int kMtokSlotBytes = 18688;
+constexpr int kMtokXGroupBytes = 16 * 128;   // one K group of x's codes for up to 16 tokens
+constexpr int kMtokMaxTopK = 16;
+
+cudaError_t launch_mtok(const MtokArgs& args, int grid, bool pdl, cudaStream_t stream);
+
 size_t stream_partials_floats(int grid);
 cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t launch_stream_mma(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);

@@ -152,8 +152,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-KERNEL_SOURCES = ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_token.cu", "moeq_device.cuh",
-                  "moeq_route.cuh", "moeq_internal.h")
+# The sources each layer kernel is built from (a traffic record names its set).
+KERNEL_SOURCES = {
+    "token": ("moeq_token.cu", "moeq_device.cuh", "moeq_route.cuh", "moeq_internal.h"),
+    "mtok": ("moeq_mtok.cu", "moeq_device.cuh", "moeq_route.cuh", "moeq_internal.h"),
+    "stream": ("moeq_stream.cuh", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_device.cuh", "moeq_route.cuh",
+               "moeq_internal.h"),
+}
 
 
 def code_hash(texts):
@@ -169,9 +174,9 @@ def code_hash(texts):
     return h.hexdigest()[:16]
 
 
-def kernel_source_hash():
+def kernel_source_hash(which: str):
     texts = []
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[which]:
         with open(os.path.join(ROOT, "bandwidth_bound_fp8_gb300", "csrc", f), encoding="utf-8") as fh:
             texts.append(fh.read())
     return code_hash(texts)
@@ -185,7 +190,7 @@ def ncu_traffic(kernel: str, M: int):
         with open(p) as f:
             d = json.load(f)
         e = d[f"{kernel}_m{M}"]
-        if e["source_hash"] != kernel_source_hash():
+        if e["source_hash"] != kernel_source_hash(e["sources"]):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -695,14 +700,16 @@ def reference_arm(args, ws, rank):
 
 
 # ------------------------------------------------------------------ profiling case
-def profile_case(M: int, reps: int):
-    """A small launch for ncu captures: the layer kernel with 8 routed experts
-    and top-8, so that a one-token launch does exactly the full layer's work
-    (8 routed + the shared expert, ~340 MB) on ~350 MB of weights."""
+def profile_case(M: int, reps: int, Er: int = 8):
+    """A small launch for ncu captures: the layer kernel with Er routed experts
+    and top-8.  Er = 8: a one-token launch does exactly the full layer's work
+    (8 routed + the shared expert, ~340 MB) on ~350 MB of weights.  Er = 64
+    (2.45 GB of weights): several tokens' picks spread over the experts as in
+    the full layer (4 tokens ~27 unique routed experts, 16 tokens ~56), most
+    of them serving one or two tokens."""
     from bandwidth_bound_fp8_gb300 import build as b
     b.build()
     from bandwidth_bound_fp8_gb300 import moeq
-    Er = 8
     gq = torch.empty((Er + 1, 2 * I, H), dtype=torch.uint8, device="cuda")
     gs = torch.empty((Er + 1, 2 * I // 128, H // 128), dtype=torch.float32, device="cuda")
     dq = torch.empty((Er + 1, H, I), dtype=torch.uint8, device="cuda")
@@ -717,12 +724,15 @@ def profile_case(M: int, reps: int):
     lg = synth.logits_f32(M, Er, 4, device="cuda")
     out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
     ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, Er + 1, TOPK))
+    plan = moeq.RoutePlan(M, Er, TOPK)
     for _ in range(reps):
-        moeq.moeq_moe_layer(x, lg, H, I, Er, TOPK, gq, gs, dq, ds, out, ws)
+        moeq.moeq_moe_layer(x, lg, H, I, Er, TOPK, gq, gs, dq, ds, out, ws, plan=plan)
     torch.cuda.synchronize()
     if moeq.moeq_read_device_status(ws.t, ws.nbytes) != 0:
         raise RuntimeError("device status word set")
-    print(json.dumps({"profile_case": f"moe_layer_m{M}_h{H}_i{I}_e{Er}_top{TOPK}_shared1", "launches": reps}))
+    U = int(plan.n_uniq.item())
+    print(json.dumps({"profile_case": f"moe_layer_m{M}_h{H}_i{I}_e{Er}_top{TOPK}_shared1", "launches": reps,
+                      "unique_experts": U, "algorithmic_bytes": U * EXPERT_BYTES}))
 
 
 # ------------------------------------------------------------------ main
@@ -741,13 +751,14 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="run a few launches of the small ncu case (8 routed experts, top-8) and exit")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--profile-experts", type=int, default=8, help="routed experts of the --profile-case layer")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense configurations and the gate_up ladder")
     ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack sweep")
     ap.add_argument("--stack-calls", type=int, default=40)
     ap.add_argument("--ladder-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.profile_case:
-        profile_case(args.M, args.reps)
+        profile_case(args.M, args.reps, args.profile_experts)
         return
     if args.ladder_child:
         from bandwidth_bound_fp8_gb300 import build as b

@@ -43,18 +43,21 @@ def test_code_hash_follows_code():
 def test_traffic_reported_only_for_the_hash_it_was_taken_on(tmp_path, monkeypatch):
     b = _bench()
     (tmp_path / "profiles").mkdir()
-    rec = {"layer_m1": {"dram_read": 300, "dram_write": 7, "dram_bytes_per_launch": 307, "source_hash": "abc"}}
+    rec = {"layer_m1": {"dram_read": 300, "dram_write": 7, "dram_bytes_per_launch": 307, "source_hash": "abc",
+                        "sources": "token"}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(b, "ROOT", str(tmp_path))
-    monkeypatch.setattr(b, "kernel_source_hash", lambda: "abc")
+    monkeypatch.setattr(b, "kernel_source_hash", lambda which: "abc" if which == "token" else "zzz")
     assert b.ncu_traffic("layer", 1) == 307.0
     assert b.ncu_traffic("layer", 16) is None        # no record for that workload
-    monkeypatch.setattr(b, "kernel_source_hash", lambda: "def")
+    monkeypatch.setattr(b, "kernel_source_hash", lambda which: "def")
     assert b.ncu_traffic("layer", 1) is None          # the kernel changed since the capture
 
 
 def test_committed_traffic_record_is_consistent():
+    b = _bench()
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         for e in json.load(f).values():
             assert e["dram_bytes_per_launch"] == e["dram_read"] + e["dram_write"]
             assert len(e["source_hash"]) == 16 and "ncu" in e["command"]
+            assert e["sources"] in b.KERNEL_SOURCES

@@ -22,9 +22,10 @@ shared) runs at M = 1 (every output), and at M = 4 and 16 with the whole plan
 and every pair's h and codes checked and the outputs of sampled tokens (tokens
 are independent, a property pinned in the oracle).
 
-One token without the per-pair y output runs the one-token kernel; asking
-for y keeps the persistent engine's row-block down path, so both are checked
-(and test_gpu_paths re-runs the one-token cases on the engine).
+One token without the per-pair y output runs the one-token kernel, two to
+sixteen the multi-token kernel; asking for y keeps the persistent engine's
+row-block down path, so every path is checked (and test_gpu_paths re-runs
+the cases without y on the engine).
 """
 import concurrent.futures as cf
 
@@ -139,11 +140,18 @@ def check_layer(orc, lay, x, logits, k, rows=None, with_y=True):
                                               (1, 12, 1280, 384, 3, False), (1, 8, 640, 256, 2, False),
                                               (1, 16, 512, 2432, 7, False), (1, 16, 512, 2432, 7, True),
                                               (3, 16, 640, 384, 2, True), (16, 32, 512, 256, 8, True),
-                                              (5, 8, 768, 128, 8, True)])
+                                              (5, 8, 768, 128, 8, True),
+                                              (2, 16, 1024, 256, 4, False), (3, 16, 512, 384, 2, False),
+                                              (5, 8, 768, 128, 8, False), (16, 32, 512, 256, 8, False),
+                                              (8, 32, 512, 2560, 8, False), (13, 64, 256, 1280, 6, False)])
 def test_layer_reduced(orc, M, E, H, I, k, with_y):
     # (1, 8, 640, ...): an odd number of output row blocks keeps one token
     # on the persistent engine; (1, 16, 512, 2432, 7): 8 unique experts x 19
-    # K groups of down = 152 columns, one per CTA on 152 SMs
+    # K groups of down = 152 columns, one per CTA on 152 SMs.  Two or more
+    # tokens without y run the multi-token kernel: (8, 32, 512, 2560, 8) and
+    # (13, 64, 256, 1280, 6) have several hundred columns of 6 (3) stages, so
+    # the even split of the stages over the CTAs cuts columns inside gate_up
+    # and inside down
     lay = Layer(E, H, I, seed=50 + M + E)
     x = synth.activations_bf16(M, H, 51 + M, max(1, H // 100), 30.0, device="cuda")
     logits = synth.logits_f32(M, E, 52 + M, device="cuda")
@@ -168,12 +176,15 @@ def test_layer_full_m1(orc, full_layer, with_y):
         assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
-@pytest.mark.parametrize("M,rows", [(4, [0, 3]), (16, [5])])
-def test_layer_full_multi_token(orc, full_layer, M, rows):
+@pytest.mark.parametrize("M,rows,with_y", [(4, [0, 3], True), (16, [5], True), (2, [0, 1], False),
+                                           (4, [1, 2], False), (16, [0, 15], False)])
+def test_layer_full_multi_token(orc, full_layer, M, rows, with_y):
+    # with y: the persistent engine's row-block down; without: the
+    # multi-token kernel (the path of every bench layer with 2..16 tokens)
     c = synth.MOE_LAYER
     x = synth.activations_bf16(M, c["H"], c["seed"] + M, c["n_outlier"], c["outlier_scale"], device="cuda")
     logits = synth.logits_f32(M, c["E"], c["seed"] + 100 + M, device="cuda")
-    out = check_layer(orc, full_layer, x, logits, c["top_k"], rows=rows)
+    out = check_layer(orc, full_layer, x, logits, c["top_k"], rows=rows, with_y=with_y)
     # determinism: a second run is bit-identical
-    out2 = full_layer.run(x, logits, c["top_k"], dumps=False)[0]
+    out2 = full_layer.run(x, logits, c["top_k"], with_y=with_y, dumps=False)[0]
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))

@@ -8,10 +8,11 @@ in child processes:
     experts, ragged K tails, split-K at every size);
   * with it at 17, every launch runs on the CUDA cores (16-token experts on
     the shared-memory accumulation mode).
-One token on the CUDA cores runs the one-token kernel unless
-MOEQ_TOKEN_KERNEL=0, which hands it to the persistent engine (down by K
-group, or row-block down when y is asked for); a third child re-runs the
-one-token layer tests, the full-size one included, on that path.
+Layers without the per-pair y output run the one-token kernel (one token)
+and the multi-token kernel (2..16) unless MOEQ_TOKEN_KERNEL=0 and
+MOEQ_MTOK_KERNEL=0 hand them to the persistent engine; the crossover
+children set both, and a third child re-runs the one-token layer tests, the
+full-size one included, and the reduced ones on the engine.
 The children use the same oracle comparisons and tolerances as the default
 run."""
 import os
@@ -27,7 +28,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 @pytest.mark.parametrize("crossover", ["1", "17"])
 def test_parity_with_forced_path(crossover):
-    env = dict(os.environ, MOEQ_MMA_MIN_TOKENS=crossover)
+    env = dict(os.environ, MOEQ_MMA_MIN_TOKENS=crossover, MOEQ_TOKEN_KERNEL="0", MOEQ_MTOK_KERNEL="0")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            os.path.join(HERE, "test_gpu_gemm.py"), os.path.join(HERE, "test_gpu_layer.py"),
            "-k", "not full_size and not full_m1 and not multi_token"]
@@ -36,7 +37,7 @@ def test_parity_with_forced_path(crossover):
 
 
 def test_parity_one_token_on_the_persistent_engine():
-    env = dict(os.environ, MOEQ_TOKEN_KERNEL="0")
+    env = dict(os.environ, MOEQ_TOKEN_KERNEL="0", MOEQ_MTOK_KERNEL="0")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            os.path.join(HERE, "test_gpu_layer.py"), "-k", "m1 or reduced"]
     r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
