@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoeq.so")
-SOURCES = ["moeq_api.cu", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_token.cu", "moeq_mtok.cu", "moeq_quant.cu",
+SOURCES = ["moeq_api.cu", "moeq_stream.cu", "moeq_stream_mma.cu", "moeq_token.cu", "moeq_mtok.cu", "moeq_tp.cu", "moeq_quant.cu",
            "moeq_route.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

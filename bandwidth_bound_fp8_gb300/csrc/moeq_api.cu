@@ -249,6 +249,7 @@ struct LayerCall {
     const uint8_t* w_d;
     const float* s_d;
     void* out;
+    float* out_f32;   // a tensor-parallel shard's fp32 partial instead of out
     const moeq_route_plan* plan_opt;
     float* h_opt;
     float* y_opt;
@@ -261,10 +262,22 @@ struct LayerCall {
     size_t ws_bytes;
 };
 
+// The fused one-token and multi-token kernels serve a call (the persistent
+// engine serves the rest).
+bool token_path(const LayerCall& c) {
+    return c.M == 1 && (c.out_f32 || c.M < mma_min_tokens()) && !c.y_opt && token_kernel_enabled() &&
+           c.top_k <= kTokenMaxTopK && c.H <= kTokenMaxH && c.H % 256 == 0;
+}
+bool mtok_path(const LayerCall& c) {
+    return c.M >= 2 && !c.y_opt && mtok_kernel_enabled() && c.top_k <= kMtokMaxTopK && c.H <= kTokenMaxH &&
+           c.H % 256 == 0;
+}
+
 // Host-side checks of one layer call (nothing is launched).
 moeq_status layer_check(const LayerCall& c, const DeviceInfo& dev) {
-    if (!c.x || !c.logits || !c.w_gu || !c.s_gu || !c.w_d || !c.s_d || !c.out) return MOEQ_ERR_INVALID_ARG;
-    if (!aligned16(c.x) || !aligned16(c.w_gu) || !aligned16(c.w_d) || !aligned16(c.out) || !aligned4(c.s_gu) ||
+    void* const dst = c.out_f32 ? static_cast<void*>(c.out_f32) : c.out;
+    if (!c.x || !c.logits || !c.w_gu || !c.s_gu || !c.w_d || !c.s_d || !dst) return MOEQ_ERR_INVALID_ARG;
+    if (!aligned16(c.x) || !aligned16(c.w_gu) || !aligned16(c.w_d) || !aligned16(dst) || !aligned4(c.s_gu) ||
         !aligned4(c.s_d))
         return MOEQ_ERR_INVALID_ARG;
     if ((c.h_opt && !aligned16(c.h_opt)) || (c.y_opt && !aligned16(c.y_opt))) return MOEQ_ERR_INVALID_ARG;
@@ -277,6 +290,8 @@ moeq_status layer_check(const LayerCall& c, const DeviceInfo& dev) {
     if (!route_args_ok(c.M, c.E_routed, c.top_k)) return MOEQ_ERR_INVALID_ARG;
     const int H = c.H, I = c.I;
     if (H <= 0 || I <= 0 || H % 128 || I % 128 || H > MOEQ_MAX_K || I > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    // an fp32 partial comes from the fused kernels only
+    if (c.out_f32 && !token_path(c) && !mtok_path(c)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     if (!dev.ok) return MOEQ_ERR_DEVICE;
     const LayerWs l = layer_ws_layout(c.M, H, I, c.E_routed, c.top_k, dev.sms);
     if (!c.ws || !aligned16(c.ws) || c.ws_bytes < l.s.end) return MOEQ_ERR_WORKSPACE;
@@ -313,8 +328,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
 
     // One token on the CUDA cores (no per-pair y asked for): the one-token
     // kernel, which needs no co-resident grid and no cross-CTA wait.
-    if (M == 1 && M < mma_min_tokens() && !y_opt && token_kernel_enabled() && top_k <= kTokenMaxTopK &&
-        H <= kTokenMaxH && H % 256 == 0) {
+    if (token_path(c)) {
         TokenArgs t = {};
         t.x = static_cast<const __nv_bfloat16*>(x);
         t.logits = logits;
@@ -330,6 +344,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         t.w_d = w_d;
         t.s_d = s_d;
         t.out = static_cast<__nv_bfloat16*>(out);
+        t.out_f32 = c.out_f32;
         t.plan = plan;
         t.h = h;
         t.q_x = q_x_opt;
@@ -351,7 +366,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
 
     // 2..16 tokens (no per-pair y asked for): the multi-token kernel, on the
     // tensor cores, with no cross-CTA wait inside its streams.
-    if (M >= 2 && !y_opt && mtok_kernel_enabled() && top_k <= kMtokMaxTopK && H <= kTokenMaxH && H % 256 == 0) {
+    if (mtok_path(c)) {
         MtokArgs t = {};
         t.x = static_cast<const __nv_bfloat16*>(x);
         t.logits = logits;
@@ -367,6 +382,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         t.w_d = w_d;
         t.s_d = s_d;
         t.out = static_cast<__nv_bfloat16*>(out);
+        t.out_f32 = c.out_f32;
         t.plan = plan;
         t.h = h;
         t.q_x = q_x_opt;
@@ -928,8 +944,8 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
                            const moeq_route_plan* plan_opt, float* h_opt, float* y_opt, uint8_t* q_x_opt,
                            float* s_x_opt, uint8_t* q_h_opt, float* s_h_opt, void* const* events_opt, void* ws,
                            size_t ws_bytes, void* stream) {
-    const LayerCall c{x,     logits, M,       H,       I,       E_routed, top_k,      w_gu,       s_gu, w_d, s_d,
-                      out,   plan_opt, h_opt, y_opt,   q_x_opt, s_x_opt,  q_h_opt,    s_h_opt,    events_opt,
+    const LayerCall c{x,     logits,  M,        H,     I,       E_routed, top_k,   w_gu,    s_gu,      w_d, s_d,
+                      out,   nullptr, plan_opt, h_opt, y_opt,   q_x_opt,  s_x_opt, q_h_opt, s_h_opt,   events_opt,
                       ws,    ws_bytes};
     const DeviceInfo dev = current_device();
     const moeq_status st = layer_check(c, dev);
@@ -937,6 +953,86 @@ moeq_status moeq_moe_layer(const void* x, const float* logits, int M, int H, int
     uintptr_t key = stream_key(stream);
     const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
     return layer_launch(c, dev, false, !after_weight_write, as_stream(stream));
+}
+
+moeq_status moeq_moe_layer_shard(const void* x, const float* logits, int M, int H, int I_shard, int E_routed,
+                                 int top_k, const uint8_t* w_gu, const float* s_gu, const uint8_t* w_d,
+                                 const float* s_d, float* out_partial, const moeq_route_plan* plan_opt, float* h_opt,
+                                 uint8_t* q_x_opt, float* s_x_opt, uint8_t* q_h_opt, float* s_h_opt, void* ws,
+                                 size_t ws_bytes, void* stream) {
+    LayerCall c = {};
+    c.x = x;
+    c.logits = logits;
+    c.M = M;
+    c.H = H;
+    c.I = I_shard;
+    c.E_routed = E_routed;
+    c.top_k = top_k;
+    c.w_gu = w_gu;
+    c.s_gu = s_gu;
+    c.w_d = w_d;
+    c.s_d = s_d;
+    c.out_f32 = out_partial;
+    c.plan_opt = plan_opt;
+    c.h_opt = h_opt;
+    c.q_x_opt = q_x_opt;
+    c.s_x_opt = s_x_opt;
+    c.q_h_opt = q_h_opt;
+    c.s_h_opt = s_h_opt;
+    c.ws = ws;
+    c.ws_bytes = ws_bytes;
+    const DeviceInfo dev = current_device();
+    const moeq_status st = layer_check(c, dev);
+    if (st != MOEQ_OK) return st;
+    uintptr_t key = stream_key(stream);
+    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+    return layer_launch(c, dev, false, !after_weight_write, as_stream(stream));
+}
+
+moeq_status moeq_tp_shard_weights(int E, int H, int I, int R, int rank, const uint8_t* w_gu, const float* s_gu,
+                                  const uint8_t* w_d, const float* s_d, uint8_t* w_gu_shard, float* s_gu_shard,
+                                  uint8_t* w_d_shard, float* s_d_shard, void* stream) {
+    if (!w_gu || !s_gu || !w_d || !s_d || !w_gu_shard || !s_gu_shard || !w_d_shard || !s_d_shard)
+        return MOEQ_ERR_INVALID_ARG;
+    if (E < 1 || R < 1 || rank < 0 || rank >= R) return MOEQ_ERR_INVALID_ARG;
+    if (H <= 0 || I <= 0 || H % 128 || I % (128 * R) || H > MOEQ_MAX_K || I > MOEQ_MAX_K)
+        return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    if (!current_device().ok) return MOEQ_ERR_DEVICE;
+    const size_t tile = 16384, KB = H / 128, RB = I / 128, RBs = RB / R;
+    cudaStream_t st = as_stream(stream);
+    // gate_up, per expert: row blocks [r*RBs, (r+1)*RBs) (gate) and RB + that
+    // (up), each a contiguous run of RBs * KB tiles; its scales likewise
+    const size_t gu_run = RBs * KB * tile, gu_pitch = 2 * RB * KB * tile, gus_pitch = 2 * RBs * KB * tile;
+    const size_t sg_run = RBs * KB * 4, sg_pitch = 2 * RB * KB * 4, sgs_pitch = 2 * RBs * KB * 4;
+    const size_t E_ = static_cast<size_t>(E);
+    for (int half = 0; half < 2; ++half) {
+        const size_t rb0 = half * RB + rank * RBs;
+        if (cudaMemcpy2DAsync(w_gu_shard + half * gu_run, gus_pitch, w_gu + rb0 * KB * tile, gu_pitch, gu_run, E_,
+                              cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaMemcpy2DAsync(reinterpret_cast<char*>(s_gu_shard) + half * sg_run, sgs_pitch,
+                              reinterpret_cast<const char*>(s_gu) + rb0 * KB * 4, sg_pitch, sg_run, E_,
+                              cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+    }
+    // down, per (expert, row block): K groups [r*RBs, (r+1)*RBs), a
+    // contiguous run of RBs tiles; its scales likewise
+    if (cudaMemcpy2DAsync(w_d_shard, RBs * tile, w_d + rank * RBs * tile, RB * tile, RBs * tile, E_ * KB,
+                          cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+        cudaMemcpy2DAsync(s_d_shard, RBs * 4, s_d + rank * RBs, RB * 4, RBs * 4, E_ * KB, cudaMemcpyDeviceToDevice,
+                          st) != cudaSuccess)
+        return MOEQ_ERR_CUDA;
+    // the shards are weights the layer kernels read before they wait for the
+    // kernel ahead of them: note the writing stream (see moeq_quant_weight)
+    g_weight_write_stream.store(stream_key(stream));
+    return MOEQ_OK;
+}
+
+moeq_status moeq_tp_reduce(const float* partials, int R, int M, int H, void* out_bf16, void* stream) {
+    if (!partials || !out_bf16 || !aligned16(partials) || !aligned16(out_bf16)) return MOEQ_ERR_INVALID_ARG;
+    if (R < 1 || M < 1 || M > MOEQ_MAX_TOKENS) return MOEQ_ERR_INVALID_ARG;
+    if (H <= 0 || H % 128) return MOEQ_ERR_UNSUPPORTED_SHAPE;
+    if (!current_device().ok) return MOEQ_ERR_DEVICE;
+    return cuda_status(launch_tp_reduce(partials, R, M, H, out_bf16, as_stream(stream)));
 }
 
 size_t moeq_stack_workspace_size(int L, int M, int H, int I, int n_experts_incl_shared, int top_k) {

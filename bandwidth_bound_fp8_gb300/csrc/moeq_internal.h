@@ -127,6 +127,7 @@ struct TokenArgs {
     const uint8_t* w_d;          // tile-major [E_routed + 1, H, I]
     const float* s_d;            // [E_routed + 1, H/128, I/128]
     __nv_bfloat16* out;          // [H]
+    float* out_f32;              // or, when set, [H] fp32: the unrounded sum (a tensor-parallel shard's partial)
     moeq_route_plan plan;        // written by CTA 0
     float* h;                    // [top_k + 1, I]
     uint8_t* q_x;                // optional [H] and [H/128]: x's codes and scales
@@ -158,6 +159,7 @@ struct MtokArgs {
     const uint8_t* w_d;          // tile-major [E_routed + 1, H, I]
     const float* s_d;            // [E_routed + 1, H/128, I/128]
     __nv_bfloat16* out;          // [M, H]
+    float* out_f32;              // or, when set, [M, H] fp32: the unrounded sums (a tensor-parallel shard's partial)
     moeq_route_plan plan;        // written by CTA 0
     float* h;                    // [max_pairs, I]
     uint8_t* q_x;                // optional [M, H] and [M, H/128]: x's codes and scales
@@ -179,6 +181,9 @@ constexpr int kMtokXGroupBytes = 16 * 128;   // one K group of x's codes for up 
 constexpr int kMtokMaxTopK = 16;
 
 cudaError_t launch_mtok(const MtokArgs& args, int grid, bool pdl, cudaStream_t stream);
+
+// Tensor-parallel combine (moeq_tp.cu): out = bf16(sum over r in order of part[r]).
+cudaError_t launch_tp_reduce(const float* part, int R, int M, int H, void* out, cudaStream_t stream);
 
 size_t stream_partials_floats(int grid);
 cudaError_t launch_stream(const StreamArgs& args, int grid, bool cooperative, cudaStream_t stream);

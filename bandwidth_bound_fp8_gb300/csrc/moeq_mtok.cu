@@ -665,11 +665,16 @@ __device__ void combine_part(const MtokArgs& a, int n, int u, int w, int lane) {
         acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
     }
     if (lane < 4) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(a.out + static_cast<size_t>(n) * a.H + 256 * u + 16 * w + 4 * lane) = packed;
+        const size_t o = static_cast<size_t>(n) * a.H + 256 * u + 16 * w + 4 * lane;
+        if (a.out_f32) {
+            *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
+        } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(a.out + o) = packed;
+        }
     }
 }
 

@@ -482,12 +482,16 @@ __device__ void combine_part(const TokenArgs& a, int u, int w, int lane) {
         acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
     }
     if (lane < 4) {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
         const int n = (2 * u + (w >> 3)) * 128 + (w & 7) * 16 + 4 * lane;
-        *reinterpret_cast<uint2*>(a.out + n) = packed;
+        if (a.out_f32) {
+            *reinterpret_cast<float4*>(a.out_f32 + n) = acc;
+        } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(a.out + n) = packed;
+        }
     }
 }
 

@@ -38,7 +38,8 @@ EXPORTS = [
     "moeq_quant_act", "moeq_quant_weight", "moeq_pack_weight", "moeq_route", "moeq_expert_gemm_gateup_swiglu",
     "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer", "moeq_expert_gemm_down_noalloc",
     "moeq_dense_ffn_workspace_size", "moeq_dense_ffn", "moeq_stack_workspace_size", "moeq_moe_stack",
-    "moeq_stack_plan", "moeq_stack_release_graphs",
+    "moeq_stack_plan", "moeq_stack_release_graphs", "moeq_tp_shard_weights", "moeq_moe_layer_shard",
+    "moeq_tp_reduce",
 ]
 
 
@@ -92,6 +93,10 @@ def load(path: str = LIB_PATH):
         "moeq_dense_ffn_workspace_size": (_sz, [_i, _i, _i]),
         "moeq_dense_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
         "moeq_stack_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+        "moeq_tp_shard_weights": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "moeq_moe_layer_shard": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
+                                      ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+        "moeq_tp_reduce": (_i, [_vp, _i, _i, _i, _vp, _vp]),
         "moeq_moe_stack": (_i, [_i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp]),
         "moeq_stack_plan": (_i, [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(moeq_route_plan)]),
         "moeq_stack_release_graphs": (_i, []),
@@ -337,3 +342,25 @@ def moeq_stack_plan(ws: Workspace, L, M, H, I, E_routed, top_k, layer) -> RouteP
 
 def moeq_stack_release_graphs() -> None:
     _check("moeq_stack_release_graphs", load().moeq_stack_release_graphs())
+
+
+def moeq_tp_shard_weights(E, H, I, R, rank, w_gu, s_gu, w_d, s_d, w_gu_shard, s_gu_shard, w_d_shard, s_d_shard,
+                          stream=None) -> None:
+    _check("moeq_tp_shard_weights", load().moeq_tp_shard_weights(
+        E, H, I, R, rank, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(w_gu_shard), _p(s_gu_shard), _p(w_d_shard),
+        _p(s_d_shard), _stream(stream)))
+
+
+def moeq_moe_layer_shard(x, logits, H, I_shard, E_routed, top_k, w_gu, s_gu, w_d, s_d, out_partial, ws: Workspace,
+                         plan: RoutePlan | None = None, h=None, q_x=None, s_x=None, q_h=None, s_h=None,
+                         stream=None) -> None:
+    M = x.shape[0]
+    _check("moeq_moe_layer_shard", load().moeq_moe_layer_shard(
+        _p(x), _p(logits), M, H, I_shard, E_routed, top_k, _p(w_gu), _p(s_gu), _p(w_d), _p(s_d), _p(out_partial),
+        ctypes.byref(plan.c) if plan is not None else None, _p(h), _p(q_x), _p(s_x), _p(q_h), _p(s_h),
+        ws.ptr, ws.nbytes, _stream(stream)))
+
+
+def moeq_tp_reduce(partials, out, stream=None) -> None:
+    R, M, H = partials.shape
+    _check("moeq_tp_reduce", load().moeq_tp_reduce(_p(partials), R, M, H, _p(out), _stream(stream)))

@@ -357,6 +357,51 @@ moeq_status moeq_moe_layer(const void* x, const float* logits,
                            void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Tensor parallelism (GLM-5.2 x10, bandwidth model: TP8 splits every       */
+/* expert over 8 cards, each card streaming 1/8 of the layer's bytes).      */
+/* Rank r of R holds, for every expert, the I-slice [r*I/R, (r+1)*I/R) of   */
+/* the gate rows and of the up rows of gate_up, and the same K-slice of     */
+/* down (I/R a multiple of 128): a layer with intermediate I/R.  Its fp32   */
+/* partial out is the sum over its slice; the layer's output is            */
+/* bf16(sum over r = 0 .. R-1, in that order, of the partials).  h groups   */
+/* never straddle slices, so each rank's live quantisation of h is the      */
+/* unsharded one's.                                                         */
+/*                                                                          */
+/* moeq_tp_shard_weights -- rank `rank`'s shard of full tile-major weights  */
+/*   (E experts, the shared one included): w_gu_shard [E, 2I/R, H] (gate    */
+/*   slice then up slice) + s_gu_shard [E, 2I/(128R), H/128], w_d_shard     */
+/*   [E, H, I/R] + s_d_shard [E, H/128, I/(128R)].  Whole 128 x 128 tiles   */
+/*   and their scales are copied (strided device-to-device copies on        */
+/*   `stream`; no arithmetic).                                              */
+/* moeq_moe_layer_shard -- moeq_moe_layer on one rank's shard (I_shard =    */
+/*   I/R), writing the fp32 partial out_partial [M, H] instead of bf16;     */
+/*   routing, x's quantisation and the plan are the full layer's.  Served   */
+/*   by the one-token and multi-token kernels only (H a multiple of 256 up  */
+/*   to 6144, top_k <= 8 at one token): other calls return                  */
+/*   MOEQ_ERR_UNSUPPORTED_SHAPE.  Workspace: moeq_workspace_size(M, H,      */
+/*   I_shard, E_routed + 1, top_k).                                         */
+/* moeq_tp_reduce -- out_bf16 [M, H] = bf16(sum_r partials[r]) over         */
+/*   partials [R, M, H] fp32 (all ranks' partials, gathered in rank order), */
+/*   added in rank order.                                                   */
+/* The exchange of the partials between GPUs (an all-gather) is the        */
+/* caller's (bandwidth_bound_fp8_gb300/tp.py uses torch.distributed).       */
+/* ------------------------------------------------------------------------ */
+moeq_status moeq_tp_shard_weights(int E, int H, int I, int R, int rank,
+                                  const uint8_t* w_gu, const float* s_gu,
+                                  const uint8_t* w_d, const float* s_d,
+                                  uint8_t* w_gu_shard, float* s_gu_shard,
+                                  uint8_t* w_d_shard, float* s_d_shard, void* stream);
+moeq_status moeq_moe_layer_shard(const void* x, const float* logits,
+                                 int M, int H, int I_shard, int E_routed, int top_k,
+                                 const uint8_t* w_gu, const float* s_gu,
+                                 const uint8_t* w_d, const float* s_d,
+                                 float* out_partial, const moeq_route_plan* plan_opt,
+                                 float* h_opt, uint8_t* q_x_opt, float* s_x_opt,
+                                 uint8_t* q_h_opt, float* s_h_opt,
+                                 void* ws, size_t ws_bytes, void* stream);
+moeq_status moeq_tp_reduce(const float* partials, int R, int M, int H, void* out_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* moeq_moe_stack -- one decode step through L MoE layers in sequence, as   */
 /*   ONE CUDA graph (GLM-5.2 x10 §8b: graph replay takes the host's         */
 /*   per-kernel launch cost out of a decode step).  Layer l runs            */
