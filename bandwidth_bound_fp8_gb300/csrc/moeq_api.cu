@@ -75,9 +75,19 @@ bool pdl_enabled() {
     return v;
 }
 // Layers of 2..16 tokens run the multi-token kernel unless
-// MOEQ_MTOK_KERNEL=0 (then the persistent engine does).  Read once.
+// MOEQ_MTOK_KERNEL=0 (then the persistent engine does); MOEQ_MTOK_MIN_TOKENS
+// (default 2) moves its lower end, 1 giving it one-token layers as well.
+// Both read once.
 bool mtok_kernel_enabled() {
     static const bool v = env_flag("MOEQ_MTOK_KERNEL", true);
+    return v;
+}
+int mtok_min_tokens() {
+    static const int v = [] {
+        const char* e = std::getenv("MOEQ_MTOK_MIN_TOKENS");
+        const int x = e ? std::atoi(e) : 0;
+        return x >= 1 ? x : 2;
+    }();
     return v;
 }
 // The standalone GEMM calls spread over every SM; MOEQ_GRID_LIMIT=n (read
@@ -165,9 +175,9 @@ LayerWs layer_ws_layout(int M, int H, int I, int E, int k, int grid) {
     l.tok_tickets = align_up(l.dc + (M == 1 ? sizeof(float) * static_cast<size_t>(mp) * (I / 128) * H : 0), 256);
     const size_t tok_end =
         l.tok_tickets + (M == 1 ? sizeof(int) * (static_cast<size_t>((H + 255) / 256) + kGqUnits) : 0);
-    // M >= 2: the multi-token kernel's counts and flags, split-column slots,
-    // x's codes and scales, and the down partials
-    const bool mt = M >= 2;
+    // the multi-token kernel's counts and flags, split-column slots, x's
+    // codes and scales, and the down partials (for the token counts it serves)
+    const bool mt = M >= mtok_min_tokens();
     l.mt_cnt = align_up(tok_end, 256);
     l.mt_slots = align_up(l.mt_cnt + (mt ? sizeof(int) * (kMtokFlags + grid + 1) : 0), 256);
     l.mt_xq = align_up(l.mt_slots + (mt ? static_cast<size_t>(grid + 1) * kMtokSlotBytes : 0), 256);
@@ -264,13 +274,13 @@ struct LayerCall {
 
 // The fused one-token and multi-token kernels serve a call (the persistent
 // engine serves the rest).
-bool token_path(const LayerCall& c) {
-    return c.M == 1 && (c.out_f32 || c.M < mma_min_tokens()) && !c.y_opt && token_kernel_enabled() &&
-           c.top_k <= kTokenMaxTopK && c.H <= kTokenMaxH && c.H % 256 == 0;
-}
 bool mtok_path(const LayerCall& c) {
-    return c.M >= 2 && !c.y_opt && mtok_kernel_enabled() && c.top_k <= kMtokMaxTopK && c.H <= kTokenMaxH &&
-           c.H % 256 == 0;
+    return c.M >= mtok_min_tokens() && !c.y_opt && mtok_kernel_enabled() && c.top_k <= kMtokMaxTopK &&
+           c.H <= kTokenMaxH && c.H % 256 == 0;
+}
+bool token_path(const LayerCall& c) {
+    return c.M == 1 && !mtok_path(c) && (c.out_f32 || c.M < mma_min_tokens()) && !c.y_opt &&
+           token_kernel_enabled() && c.top_k <= kTokenMaxTopK && c.H <= kTokenMaxH && c.H % 256 == 0;
 }
 
 // Host-side checks of one layer call (nothing is launched).

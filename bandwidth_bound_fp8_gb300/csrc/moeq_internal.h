@@ -173,9 +173,13 @@ struct MtokArgs {
     float* xs;                   // [KB][16]: x's scales
     float* part;                 // [M][H/256][16][top_k + 1][RB][16] down partials
 };
-// counts (ints): CTAs done streaming, CTAs done summing, quantised groups
-// per K group of x, and the split columns' flags (one per CTA boundary)
-constexpr int kMtokDone = 0, kMtokFin = 1, kMtokX = 2, kMtokFlags = kMtokX + kTokenMaxH / 128;
+// counts (ints): CTAs done, quantised groups per K group of x, down partials
+// stored per 256-row output unit, and the split columns' flags (one per CTA
+// boundary).  The counts that every CTA polls sit one per 128-byte line
+// (stride kMtokPad ints), so that the polls spread over L2.
+constexpr int kMtokPad = 32;
+constexpr int kMtokFin = 0, kMtokX = kMtokPad, kMtokU = kMtokX + kMtokPad * (kTokenMaxH / 128),
+              kMtokFlags = kMtokU + kMtokPad * (kTokenMaxH / 256);
 constexpr int kMtokSlotBytes = 18688;
 constexpr int kMtokXGroupBytes = 16 * 128;   // one K group of x's codes for up to 16 tokens
 constexpr int kMtokMaxTopK = 16;

@@ -16,8 +16,11 @@
 // itself -- against every output row (KB/2 stages of two tiles).  The
 // column's tokens are its expert's; its MMAs take every token (N = 16
 // accumulator columns, token n in column n) and the epilogue keeps the
-// column's own.  Every column streams the same bytes whatever its token
-// count, so the launch's stages (ncols x 3KB/2) are dealt out evenly
+// column's own.  The shared expert's columns -- every token's, the costliest
+// to finish -- are spaced evenly among the routed ones, so that they fall on
+// different CTAs.  Every column streams the same bytes
+// whatever its token count, so the launch's stages (ncols x 3KB/2) are dealt
+// out evenly
 // (stream-K): a CTA's range may begin inside one column and end inside
 // another.  The CTA streams the head of the column its range ends in FIRST
 // and publishes what the rest of that column needs (the gate and up sums so
@@ -44,7 +47,12 @@
 //   warps 2-5   epilogue: each thread owns one TMEM lane (a row of the
 //               tiles) and promotes each stage's sums with the block scales;
 //               SwiGLU and h's quantisation; down's partials;
-//   all warps   the sums at the end.
+//   warp 7      tickets: as the epilogue stores down partials it counts each
+//               (column, output unit) in (one gpu-scope fence per batch);
+//   warps 8-11  the sums: each (token, 16 output rows) once its unit's count
+//               shows every column in -- the units complete one after another
+//               as the last columns' down stages pass them, so the sums
+//               overlap the end of the streams.
 // Launched with programmatic dependent launch: before griddepcontrol.wait a
 // CTA only starts its share of the shared expert's weights towards L2.
 #include "moeq_device.cuh"
@@ -57,6 +65,7 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kWarps = kThreads / 32;
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kQuantWarp0 = 6, kQuantWarps = 6;
+constexpr int kTicketWarp = 7, kSumWarp0 = 8, kSumWarps = 4;
 constexpr int kRouteThreads = kQuantWarp0 * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kTile = 16384;
@@ -107,6 +116,7 @@ struct Smem {
     uint64_t full[kStages], empty[kStages], mma_done[kTmemBufs], tmem_empty[kTmemBufs], h_ready;
     uint64_t xq_bar[kMaxKB];
     uint32_t tmem_base;
+    int wdone[kEpiWarps];                       // down stages whose partials each epilogue warp has stored
     int abort_flag;
 };
 
@@ -281,56 +291,107 @@ __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
         fence_proxy_async();   // the codes are read by bulk copies (async proxy)
         __threadfence();       // ... and by other CTAs: released by the count below
         __syncwarp();
-        if (lane == 0) atomicAdd(a.cnt + kMtokX + t, 1);
+        if (lane == 0) atomicAdd(a.cnt + kMtokX + kMtokPad * t, 1);
     }
 }
 
-// Warp 6, once the plan is known: K group by K group, wait (bounded) until
-// all M tokens' groups are in, take their scales into shared memory and
-// release the group to the producer and the epilogue.
+// Warp 6, once the plan is known: lane l watches K groups l and l + 32,
+// each on its own (bounded) -- once a group's count shows all M tokens in,
+// the lane takes its scales into shared memory and releases it to the
+// producer and the epilogue.
 __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
-    for (int t = 0; t < a.KB; ++t) {
-        if (lane == 0) {
-            const unsigned long long t0 = global_timer_ns();
-            while (ld_acquire(a.cnt + kMtokX + t) < a.M) {
-                if (sm.abort_flag) break;
-                if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    record_error(a.status, MOEQ_ERR_TIMEOUT);
-                    sm.abort_flag = 1;
-                    break;
-                }
-                __nanosleep(64);
+    constexpr int kPer = (kMaxKB + 31) / 32;
+    bool done[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) done[i] = lane + 32 * i >= a.KB;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        bool all = true;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            if (done[i]) continue;
+            const int t = lane + 32 * i;
+            if (ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
+                fence_proxy_async();
+                for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
+                mbar_arrive(&sm.xq_bar[t]);
+                done[i] = true;
+            } else {
+                all = false;
             }
-            fence_proxy_async();
         }
-        __syncwarp();
-        if (lane < kN) sm.sx[t][lane] = lane < a.M ? __ldcg(a.xs + t * kN + lane) : 0.0f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.xq_bar[t]);
+        if (all) break;
+        if (sm.abort_flag) break;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_error(a.status, MOEQ_ERR_TIMEOUT);
+            sm.abort_flag = 1;
+            break;
+        }
+        __nanosleep(64);
     }
 }
 
 // ------------------------------------------------------------------ producer
+// Column j's (unique expert slot g, K group kb): the routed experts' columns
+// in expert-major order (each expert's gate rows, then up rows, one run of
+// tiles after another), with the shared expert's columns -- every token's,
+// the costliest to finish -- spaced evenly among them (one after every U - 1
+// routed columns), so that they fall on different CTAs.
+__device__ __forceinline__ void col_of(int j, int U, int RB, int& g, int& kb) {
+    const int b = j / U, o = j - b * U;
+    if (o == U - 1) {
+        g = U - 1;
+        kb = b;
+    } else {
+        const int r = b * (U - 1) + o;
+        g = r / RB;
+        kb = r - g * RB;
+    }
+}
+
 // Returns the number of stages issued (all of the share's, unless aborted).
+// A gate_up stage's weight tiles go out at once; its x group follows as soon
+// as that K group is released (at the start of the launch x may still be on
+// its way), so that x's quantisation overlaps the first tiles' latency.
+// Before the producer blocks on a free stage, every deferred x copy is out.
 __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, const Share& sh, int spc) {
     const uint64_t pol = l2_evict_first_policy();
     const uint32_t xbytes = static_cast<uint32_t>(a.M) * 128;
+    int pend_s[kStages], pend_t[kStages], npend = 0;
+    auto flush = [&]() -> bool {
+        for (int q = 0; q < npend; ++q) {
+            if (!wait_sleep(&sm.xq_bar[pend_t[q]], 0, sm, a.status)) return false;
+            bulk_load(stages + static_cast<size_t>(pend_s[q]) * kStageBytes + 2 * kTile, xq_group(a, pend_t[q]),
+                      xbytes, &sm.full[pend_s[q]], pol);
+        }
+        npend = 0;
+        return true;
+    };
     long long it = 0;
     for (int i = 0; i < sh.np && !sm.abort_flag; ++i) {
-        int j, t0, t1;
+        int j, t0, t1, g, kb;
         piece_at(sh, i, spc, j, t0, t1);
-        const int g = j / a.RB, kb = j - g * a.RB, e = sm.plan.uniq[g];
+        col_of(j, sm.plan.n_uniq, a.RB, g, kb);
+        const int e = sm.plan.uniq[g];
         for (int t = t0; t < t1; ++t, ++it) {
             const int s = static_cast<int>(it % kStages);
-            if (it >= kStages && !wait_sleep(&sm.empty[s], static_cast<uint32_t>((it / kStages - 1) & 1), sm, a.status))
-                return it;
+            if (it >= kStages) {
+                if (!flush()) return it;
+                if (!wait_sleep(&sm.empty[s], static_cast<uint32_t>((it / kStages - 1) & 1), sm, a.status))
+                    return it;
+            }
             uint8_t* dst = stages + static_cast<size_t>(s) * kStageBytes;
             if (t < a.KB) {
-                if (!wait_sleep(&sm.xq_bar[t], 0, sm, a.status)) return it;
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + xbytes);
                 bulk_load(dst, gu_tile(a, e, kb, t), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, gu_tile(a, e, a.RB + kb, t), kTile, &sm.full[s], pol);
-                bulk_load(dst + 2 * kTile, xq_group(a, t), xbytes, &sm.full[s], pol);
+                if (npend == 0 && mbar_try_wait(&sm.xq_bar[t], 0)) {
+                    bulk_load(dst + 2 * kTile, xq_group(a, t), xbytes, &sm.full[s], pol);
+                } else {
+                    pend_s[npend] = s;
+                    pend_t[npend] = t;
+                    ++npend;
+                }
             } else {
                 const int u = t - a.KB;
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
@@ -339,6 +400,7 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
             }
         }
     }
+    flush();
     return it;
 }
 
@@ -401,7 +463,9 @@ __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
     ColInfo& ci = sm.col[i & 1];
     int j, t0, t1;
     piece_at(sh, i, spc, j, t0, t1);
-    const int g = j / a.RB, kb = j - g * a.RB, e = sm.plan.uniq[g];
+    int g, kb;
+    col_of(j, sm.plan.n_uniq, a.RB, g, kb);
+    const int e = sm.plan.uniq[g];
     const int KB = a.KB, NBg = 2 * a.RB;
     for (int q = etid; q < 3 * KB; q += kEpiThreads) {
         const int which = q / KB, t = q - which * KB;
@@ -480,6 +544,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
     const int KB = a.KB, k = a.top_k, c = blockIdx.x;
     const int ustride = (k + 1) * a.RB * 256;   // partials of one output unit, per token
     long long it = 0;
+    int stored = 0;
     if (sh.np > 0) load_col(a, sm, sh, spc, 0, etid);
     for (int i = 0; i < sh.np; ++i) {
         epi_sync();   // piece i's column info is loaded; the previous piece's is no longer read
@@ -625,6 +690,13 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
                     p[128] = __uint_as_float(d1[n]) * (hwn * s1);
                 }
             }
+            // the ticket warp learns of the stored partials
+            ++stored;
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                *reinterpret_cast<volatile int*>(&sm.wdone[warp - kEpiWarp0]) = stored;
+            }
         }
     }
 }
@@ -678,6 +750,84 @@ __device__ void combine_part(const MtokArgs& a, int n, int u, int w, int lane) {
     }
 }
 
+// ------------------------------------------------------------------ counts
+// The unit of this CTA's q-th down stage (its pieces' down stages in order).
+__device__ int unit_of_down_stage(const Share& sh, int spc, int KB, int q) {
+    for (int i = 0; i < sh.np; ++i) {
+        int j, t0, t1;
+        piece_at(sh, i, spc, j, t0, t1);
+        const int d0 = max(t0, KB), nd = max(0, t1 - d0);
+        if (q < nd) return d0 - KB + q;
+        q -= nd;
+    }
+    return 0;
+}
+
+// Warp 7: as the epilogue warps store down partials (their progress
+// counters in shared memory), one gpu-scope fence releases every partial
+// stored so far, then one fire-and-forget add per (column, unit) arrival.
+// A unit is complete once its count reaches ncols.
+__device__ void ticket_warp(const MtokArgs& a, Smem& sm, const Share& sh, int spc, int lane) {
+    const int KB = a.KB;
+    int total = 0;
+    for (int i = 0; i < sh.np; ++i) {
+        int j, t0, t1;
+        piece_at(sh, i, spc, j, t0, t1);
+        total += max(0, t1 - max(t0, KB));
+    }
+    int done = 0;
+    unsigned long long t0 = global_timer_ns();
+    while (done < total && !sm.abort_flag) {
+        const int mine = lane < kEpiWarps ? reinterpret_cast<volatile int*>(sm.wdone)[lane] : 0x7fffffff;
+        const int avail = __reduce_min_sync(0xffffffffu, mine);
+        if (avail <= done) {
+            __nanosleep(64);
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                if (lane == 0) record_error(a.status, MOEQ_ERR_TIMEOUT);
+                sm.abort_flag = 1;
+            }
+            continue;
+        }
+        t0 = global_timer_ns();
+        __threadfence();   // releases the partials stored by every epilogue warp so far
+        for (int q = done + lane; q < avail; q += 32) atomicAdd(a.cnt + kMtokU + kMtokPad * unit_of_down_stage(sh, spc, KB, q), 1);
+        done = avail;
+    }
+}
+
+// Warps 8-11: the sums, in unit order (task p: unit p / (16M), then token,
+// then 16-row part), each once its unit's count shows all ncols columns in
+// (bounded wait).
+__device__ void sum_worker(const MtokArgs& a, Smem& sm, int ncols, int wi, int lane) {
+    const int nu = a.KB / 2, per_unit = a.M * kParts, ntask = nu * per_unit;
+    for (int p = blockIdx.x * kSumWarps + wi; p < ntask; p += gridDim.x * kSumWarps) {
+        const int u = p / per_unit, rem = p - u * per_unit;
+        int ok = 0;
+        if (lane == 0) {
+            const int* cnt = a.cnt + kMtokU + kMtokPad * u;
+            const unsigned long long t0 = global_timer_ns();
+            for (uint32_t i = 0;; ++i) {
+                if (ld_relaxed(cnt) >= ncols) {
+                    ok = ld_acquire(cnt) >= ncols;   // acquires the unit's partials
+                    break;
+                }
+                if ((i & 7u) == 7u) {
+                    if (sm.abort_flag) break;
+                    if (global_timer_ns() - t0 > kWaitLimitNs) {
+                        record_error(a.status, MOEQ_ERR_TIMEOUT);
+                        sm.abort_flag = 1;
+                        break;
+                    }
+                }
+                // few polls while the unit is far from complete
+                __nanosleep(ld_relaxed(cnt) * 4 < ncols * 3 ? 1024 : 64);
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        combine_part(a, rem / kParts, u, rem % kParts, lane);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant__ MtokArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -698,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         sm.abort_flag = 0;
         fence_mbar_init();
     }
+    if (tid < kEpiWarps) sm.wdone[tid] = 0;
     // rows M .. 15 of every stage's x group and all of h's codes stay zero:
     // their accumulator columns are never used, but stay finite
     for (int q = tid; q < kStages * kXGroupBytes / 16; q += kThreads) {
@@ -756,43 +907,25 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
             epilogue<16>(a, sm, sh, spc, warp, lane);
     } else if (warp == kQuantWarp0) {
         x_ready(a, sm, lane);
+    } else if (warp == kTicketWarp) {
+        ticket_warp(a, sm, sh, spc, lane);
+    } else {
+        sum_worker(a, sm, ncols, warp - kSumWarp0, lane);
     }
 
-    // every CTA's partials stored: count this CTA in, wait for all (bounded)
-    __threadfence();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(sm.tmem_base, kTmemCols);
-    if (tid == 0) {
-        atomicAdd(a.cnt + kMtokDone, 1);
-        const unsigned long long t0 = global_timer_ns();
-        while (ld_acquire(a.cnt + kMtokDone) < G) {
-            if (sm.abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
-                record_error(a.status, MOEQ_ERR_TIMEOUT);
-                sm.abort_flag = 1;
-                break;
-            }
-            __nanosleep(256);
-        }
-    }
-    __syncthreads();
-    if (!sm.abort_flag) {
-        const int nu = a.KB / 2, ntask = a.M * nu * kParts;
-        for (int p = blockIdx.x * kWarps + warp; p < ntask; p += G * kWarps) {
-            const int n = p / (nu * kParts), rem = p - n * nu * kParts;
-            combine_part(a, n, rem / kParts, rem % kParts, lane);
-        }
-    }
-    // the last CTA out clears the counts and flags for the next launch
-    __syncthreads();
+    // the last CTA out (every other CTA's counting and summing done) clears
+    // the counts and flags for the next launch
     if (tid == 0) {
         __threadfence();
         if (atomicAdd(a.cnt + kMtokFin, 1) == G - 1) {
             __threadfence();
-            a.cnt[kMtokDone] = 0;
             a.cnt[kMtokFin] = 0;
-            for (int t = 0; t < a.KB; ++t) a.cnt[kMtokX + t] = 0;
+            for (int t = 0; t < a.KB; ++t) a.cnt[kMtokX + kMtokPad * t] = 0;
+            for (int u = 0; u < a.KB / 2; ++u) a.cnt[kMtokU + kMtokPad * u] = 0;
             for (int b = 0; b <= G; ++b) a.cnt[kMtokFlags + b] = 0;
         }
     }
