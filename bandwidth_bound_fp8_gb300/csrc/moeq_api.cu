@@ -74,10 +74,10 @@ bool pdl_enabled() {
     static const bool v = env_flag("MOEQ_PDL", true);
     return v;
 }
-// Layers of 2..16 tokens run the multi-token kernel unless
+// Layers of 1..16 tokens run the multi-token kernel unless
 // MOEQ_MTOK_KERNEL=0 (then the persistent engine does); MOEQ_MTOK_MIN_TOKENS
-// (default 2) moves its lower end, 1 giving it one-token layers as well.
-// Both read once.
+// (default 1) moves its lower end, 2 handing one-token layers to the
+// one-token kernel.  Both read once.
 bool mtok_kernel_enabled() {
     static const bool v = env_flag("MOEQ_MTOK_KERNEL", true);
     return v;
@@ -86,7 +86,7 @@ int mtok_min_tokens() {
     static const int v = [] {
         const char* e = std::getenv("MOEQ_MTOK_MIN_TOKENS");
         const int x = e ? std::atoi(e) : 0;
-        return x >= 1 ? x : 2;
+        return x >= 1 ? x : 1;
     }();
     return v;
 }

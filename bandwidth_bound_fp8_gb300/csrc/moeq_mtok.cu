@@ -250,7 +250,17 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
     p.offs = sm.plan.offs;
     p.pair_tok = sm.plan.pair_tok;
     p.pair_of = sm.plan.pair_of;
-    route_compute<kRouteThreads>(a.logits, a.M, a.E_routed, a.top_k, p, sm.rs, tid, RouteSync{});
+    if (a.M == 1) {
+        // one token: one warp, no block barrier
+        if (tid < 32) {
+            if (a.E_routed <= 256)
+                route_one_token_warp<8>(a.logits, a.E_routed, a.top_k, tid, p, sm.rs.id[0], sm.rs.lv[0]);
+            else
+                route_one_token_warp<kRouteMaxE / 32>(a.logits, a.E_routed, a.top_k, tid, p, sm.rs.id[0], sm.rs.lv[0]);
+        }
+    } else {
+        route_compute<kRouteThreads>(a.logits, a.M, a.E_routed, a.top_k, p, sm.rs, tid, RouteSync{});
+    }
     named_sync(2, kRouteThreads);
     if (blockIdx.x == 0) {
         const int M = a.M, k = a.top_k, U = sm.plan.n_uniq, P = sm.plan.offs[U];
@@ -311,7 +321,7 @@ __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
         for (int i = 0; i < kPer; ++i) {
             if (done[i]) continue;
             const int t = lane + 32 * i;
-            if (ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
+            if (ld_relaxed(a.cnt + kMtokX + kMtokPad * t) >= a.M && ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
                 fence_proxy_async();
                 for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
                 mbar_arrive(&sm.xq_bar[t]);
@@ -833,21 +843,20 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem& sm = *reinterpret_cast<Smem*>(stages + static_cast<size_t>(kStages) * kStageBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, G = gridDim.x;
-    if (tid == 0) {
-        pdl_launch_dependents();
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
-        }
-        for (int b = 0; b < kTmemBufs; ++b) {
-            mbar_init(&sm.mma_done[b], 1);
-            mbar_init(&sm.tmem_empty[b], kEpiWarps);
-        }
+    if (tid == 0) pdl_launch_dependents();
+    if (tid < kStages) {
+        mbar_init(&sm.full[tid], 1);
+        mbar_init(&sm.empty[tid], 1);
+    } else if (tid >= 32 && tid < 32 + kTmemBufs) {
+        mbar_init(&sm.mma_done[tid - 32], 1);
+        mbar_init(&sm.tmem_empty[tid - 32], kEpiWarps);
+    } else if (tid == 64) {
         mbar_init(&sm.h_ready, 1);
-        for (int t = 0; t < kMaxKB; ++t) mbar_init(&sm.xq_bar[t], 1);
         sm.abort_flag = 0;
-        fence_mbar_init();
+    } else if (tid >= 96 && tid < 96 + kMaxKB) {
+        mbar_init(&sm.xq_bar[tid - 96], 1);
     }
+    fence_mbar_init();
     if (tid < kEpiWarps) sm.wdone[tid] = 0;
     // rows M .. 15 of every stage's x group and all of h's codes stay zero:
     // their accumulator columns are never used, but stay finite
@@ -860,6 +869,15 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     if (warp == kMmaWarp) tmem_alloc(&sm.tmem_base, kTmemCols);
     // before the previous kernel is done: this CTA's share of the shared
     // expert's weights towards L2 (nothing writes weights)
+    if (warp == kMmaWarp + 2) {
+        // the logits and x are the previous kernel's to write until
+        // griddepcontrol.wait; their lines can still be brought into L2 now
+        // (L2 is where every SM's writes meet), so the reads after the wait hit
+        const int lg_lines = (a.M * a.E_routed * 4 + 127) / 128, x_lines = (a.M * a.H * 2 + 127) / 128;
+        for (int i = lane; i < lg_lines + x_lines; i += 32)
+            prefetch_l2(i < lg_lines ? reinterpret_cast<const char*>(a.logits) + 128 * i
+                                     : reinterpret_cast<const char*>(a.x) + 128 * (i - lg_lines));
+    }
     if (warp == kProducerWarp) {
         const long long gu_tiles = 2LL * a.RB * a.KB, tiles = gu_tiles + static_cast<long long>(a.KB) * a.RB;
         const long long lo = tiles * blockIdx.x / G, hi = tiles * (blockIdx.x + 1) / G;
@@ -873,44 +891,48 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     pdl_wait();
-    if (warp < kQuantWarp0)
+    if (warp < kQuantWarp0) {
         route_all(a, sm, tid);   // ends with the plan in every CTA's shared memory
-    else
+    } else {
         quantise_x(a, warp - kQuantWarp0, lane);
-    __syncthreads();
-
-    const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.KB + a.KB / 2;
-    const Share sh = share_of(ncols, spc);
-    if (warp == kProducerWarp) {
-        if (lane == 0) {
-            const long long issued = producer(a, sm, stages, sh, spc);
-            if (sm.abort_flag) producer_drain(sm, issued);
-        }
-    } else if (warp == kMmaWarp) {
-        const long long last = mma_issuer(a, sm, stages, sh, spc, lane);
-        if (last >= 0) {
-            // every MMA issued has completed before TMEM is freed (bounded)
-            const unsigned long long t0 = global_timer_ns();
-            while (!mbar_try_wait(&sm.mma_done[last % kTmemBufs], static_cast<uint32_t>((last / kTmemBufs) & 1))) {
-                if (global_timer_ns() - t0 > 100ull * 1000ull * 1000ull) {
-                    if (lane == 0) record_error(a.status, MOEQ_ERR_TIMEOUT);
-                    break;
+    }
+    if (warp == kQuantWarp0) {
+        // warp 6 goes on at once to release x's K groups as the grid's
+        // quantisation completes (it needs no plan); the others wait for it
+        x_ready(a, sm, lane);
+    } else {
+        named_sync(3, kThreads - 32);
+        const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.KB + a.KB / 2;
+        const Share sh = share_of(ncols, spc);
+        if (warp == kProducerWarp) {
+            if (lane == 0) {
+                const long long issued = producer(a, sm, stages, sh, spc);
+                if (sm.abort_flag) producer_drain(sm, issued);
+            }
+        } else if (warp == kMmaWarp) {
+            const long long last = mma_issuer(a, sm, stages, sh, spc, lane);
+            if (last >= 0) {
+                // every MMA issued has completed before TMEM is freed (bounded)
+                const unsigned long long t0 = global_timer_ns();
+                while (!mbar_try_wait(&sm.mma_done[last % kTmemBufs], static_cast<uint32_t>((last / kTmemBufs) & 1))) {
+                    if (global_timer_ns() - t0 > 100ull * 1000ull * 1000ull) {
+                        if (lane == 0) record_error(a.status, MOEQ_ERR_TIMEOUT);
+                        break;
+                    }
                 }
             }
+        } else if (warp < kEpiWarp0 + kEpiWarps) {
+            if (a.M <= 4)
+                epilogue<4>(a, sm, sh, spc, warp, lane);
+            else if (a.M <= 8)
+                epilogue<8>(a, sm, sh, spc, warp, lane);
+            else
+                epilogue<16>(a, sm, sh, spc, warp, lane);
+        } else if (warp == kTicketWarp) {
+            ticket_warp(a, sm, sh, spc, lane);
+        } else {
+            sum_worker(a, sm, ncols, warp - kSumWarp0, lane);
         }
-    } else if (warp < kEpiWarp0 + kEpiWarps) {
-        if (a.M <= 4)
-            epilogue<4>(a, sm, sh, spc, warp, lane);
-        else if (a.M <= 8)
-            epilogue<8>(a, sm, sh, spc, warp, lane);
-        else
-            epilogue<16>(a, sm, sh, spc, warp, lane);
-    } else if (warp == kQuantWarp0) {
-        x_ready(a, sm, lane);
-    } else if (warp == kTicketWarp) {
-        ticket_warp(a, sm, sh, spc, lane);
-    } else {
-        sum_worker(a, sm, ncols, warp - kSumWarp0, lane);
     }
 
     tc_fence_before();

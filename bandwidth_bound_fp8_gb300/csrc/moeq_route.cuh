@@ -88,6 +88,45 @@ __device__ __forceinline__ void route_topk_warp(const float* __restrict__ l, int
     route_topk_keys<NPER>(key, E, k, lane, ids, vals);
 }
 
+// The plan of ONE token by one warp, with no block barrier: top-k as
+// above, the softmax over the picks (the same butterfly and division as
+// route_compute, so the same bits), the picks ascending as the unique list
+// (one pair each, in that order) and the shared expert last.  `ids`/`vals`
+// are k-entry scratch (the warp's own).
+template <int NPER>
+__device__ __forceinline__ void route_one_token_warp(const float* __restrict__ l, int E, int k, int lane,
+                                                     const moeq_route_plan& plan, int* ids, float* vals) {
+    route_topk_warp<NPER>(l, E, k, lane, ids, vals);
+    float ex = 0.0f;
+    int id = 0x7fffffff;
+    if (lane < k) {
+        ex = expf(vals[lane] - vals[0]);
+        id = ids[lane];
+    }
+    float den = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    int rank = 0;
+    for (int i = 0; i < k; ++i) rank += __shfl_sync(0xffffffffu, id, i) < id;
+    if (lane < k) {
+        plan.topk_id[lane] = id;
+        plan.topk_w[lane] = __fdiv_rn(ex, den);
+        plan.uniq[rank] = id;
+        plan.offs[lane] = lane;
+        plan.pair_tok[lane] = 0;
+        plan.pair_of[lane] = rank;
+    }
+    if (lane == 0) {
+        plan.uniq[k] = E;
+        plan.offs[k] = k;
+        plan.offs[k + 1] = k + 1;
+        plan.pair_tok[k] = 0;
+        plan.pair_of[k] = k;
+        *plan.n_uniq = k + 1;
+    }
+    __syncwarp();
+}
+
 // Computes the plan with NT threads (tid in [0, NT)); `sync` is a barrier
 // over exactly those threads.  Writes every plan member to global memory;
 // the caller makes the writes visible (fence + flag) as it needs.

@@ -792,7 +792,7 @@ def main():
 
     k_ms = r["kernel_ms"]
     achieved = r["kernel_bytes"] / (k_ms * 1e-3) / 1e9
-    kname = ("token_kernel (one-token MoE layer: route, gate_up+SwiGLU, down, combine)" if args.M == 1 else
+    kname = ("mtok_kernel (MoE layer: route, quant x, gate_up+SwiGLU on tcgen05, quant h, down, combine)" if args.M <= 16 else
              "stream_kernel (whole MoE layer: route, gate_up+SwiGLU, down, combine)")
     roof = {"bound": "hbm", "kernel": kname,
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy), of {peak_kind}",

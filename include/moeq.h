@@ -307,18 +307,20 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I,
 /*   the activations in front of each GEMM; §4 -- fused into it; §1 --      */
 /*   split-K so that every SM streams; §5-§6 -- tokens verified together     */
 /*   read each expert once.)                                                */
-/*   M == 1 on the CUDA cores, y not asked for, top_k <= 8, H <= 6144 and   */
-/*   H % 256 == 0: the one-token kernel.  One CTA per (expert, 128-wide K   */
-/*   group of down): it streams that h group's gate and up rows, forms and  */
-/*   quantises the group itself, and streams down's K group against every  */
-/*   output row; each column's fp32 partials already carry its routing     */
-/*   weight, and each 256 output rows' partials are summed in a fixed order */
-/*   (and the bf16 output formed) by warps with no stream of their own once */
-/*   the unit's arrival count is full; no stream waits for another CTA.     */
-/*   It is launched with                                                   */
-/*   programmatic dependent launch: the next kernel on the stream may start */
-/*   as its CTAs finish, and waits (griddepcontrol.wait) before it reads    */
-/*   anything this one writes.                                              */
+/*   y not asked for, top_k <= 16, H <= 6144 and H % 256 == 0: the          */
+/*   multi-token kernel, on the tcgen05 tensor cores.  A column is (unique  */
+/*   expert, 128-wide K group of down): the h group's gate and up rows over */
+/*   all of H, then down's K group against every output row; the column's   */
+/*   MMAs take every token and keep its expert's.  The columns' stages are  */
+/*   dealt out evenly over the SMs (a column may be split between two CTAs, */
+/*   whose second part comes last in its CTA's order), x is quantised once  */
+/*   in the grid, and each token's 16 output rows are summed in a fixed     */
+/*   order (and rounded to bf16) by idle warps as soon as their output unit */
+/*   is complete.  It is launched with programmatic dependent launch: the   */
+/*   next kernel on the stream may start as its CTAs finish, and waits      */
+/*   (griddepcontrol.wait) before it reads anything this one writes.  With  */
+/*   MOEQ_MTOK_MIN_TOKENS=2 one token runs the one-token kernel instead     */
+/*   (CUDA cores, top_k <= 8; the kernel of moeq_dense_ffn).                */
 /*   Otherwise: one persistent CTA per SM (cooperative launch).  Every CTA  */
 /*   routes for itself while CTAs whose first blocks are the shared         */
 /*   expert's already stream them; down waits per expert for its h, and the */

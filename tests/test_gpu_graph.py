@@ -6,7 +6,7 @@ workspace and leave it ready for the next launch, so a replay needs no host
 work.  Every layer of a replay matches the oracle's layer fed the GPU's own
 previous bf16 output (SPEC plus half a bf16 ulp), and replaying the graph
 twice gives, bit for bit, the outputs of the same calls made eagerly, at one
-token (the one-token kernel, launched with programmatic dependent launch)
+token (the multi-token kernel, launched with programmatic dependent launch)
 and at four (the persistent engine)."""
 import numpy as np
 import pytest

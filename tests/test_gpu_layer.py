@@ -22,10 +22,10 @@ shared) runs at M = 1 (every output), and at M = 4 and 16 with the whole plan
 and every pair's h and codes checked and the outputs of sampled tokens (tokens
 are independent, a property pinned in the oracle).
 
-One token without the per-pair y output runs the one-token kernel, two to
-sixteen the multi-token kernel; asking for y keeps the persistent engine's
-row-block down path, so every path is checked (and test_gpu_paths re-runs
-the cases without y on the engine).
+Without the per-pair y output a layer of 1..16 tokens runs the multi-token
+kernel; asking for y keeps the persistent engine's row-block down path, so
+both are checked (and test_gpu_paths re-runs the cases without y on the
+engine, and the one-token ones on the one-token kernel).
 """
 import concurrent.futures as cf
 
@@ -143,7 +143,8 @@ def check_layer(orc, lay, x, logits, k, rows=None, with_y=True):
                                               (5, 8, 768, 128, 8, True),
                                               (2, 16, 1024, 256, 4, False), (3, 16, 512, 384, 2, False),
                                               (5, 8, 768, 128, 8, False), (16, 32, 512, 256, 8, False),
-                                              (8, 32, 512, 2560, 8, False), (13, 64, 256, 1280, 6, False)])
+                                              (8, 32, 512, 2560, 8, False), (13, 64, 256, 1280, 6, False),
+                                              (2, 8, 256, 128, 2, False), (3, 4, 512, 256, 2, False)])
 def test_layer_reduced(orc, M, E, H, I, k, with_y):
     # (1, 8, 640, ...): an odd number of output row blocks keeps one token
     # on the persistent engine; (1, 16, 512, 2432, 7): 8 unique experts x 19
@@ -151,7 +152,8 @@ def test_layer_reduced(orc, M, E, H, I, k, with_y):
     # tokens without y run the multi-token kernel: (8, 32, 512, 2560, 8) and
     # (13, 64, 256, 1280, 6) have several hundred columns of 6 (3) stages, so
     # the even split of the stages over the CTAs cuts columns inside gate_up
-    # and inside down
+    # and inside down; (2, 8, 256, 128, 2) and (3, 4, 512, 256, 2) have
+    # fewer columns than SMs: one column per CTA, many CTAs idle
     lay = Layer(E, H, I, seed=50 + M + E)
     x = synth.activations_bf16(M, H, 51 + M, max(1, H // 100), 30.0, device="cuda")
     logits = synth.logits_f32(M, E, 52 + M, device="cuda")

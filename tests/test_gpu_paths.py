@@ -8,11 +8,12 @@ in child processes:
     experts, ragged K tails, split-K at every size);
   * with it at 17, every launch runs on the CUDA cores (16-token experts on
     the shared-memory accumulation mode).
-Layers without the per-pair y output run the one-token kernel (one token)
-and the multi-token kernel (2..16) unless MOEQ_TOKEN_KERNEL=0 and
-MOEQ_MTOK_KERNEL=0 hand them to the persistent engine; the crossover
-children set both, and a third child re-runs the one-token layer tests, the
-full-size one included, and the reduced ones on the engine.
+Layers without the per-pair y output run the multi-token kernel unless
+MOEQ_MTOK_KERNEL=0 (with MOEQ_TOKEN_KERNEL=0) hands them to the persistent
+engine; the crossover children set both, a third child re-runs the
+one-token layer tests, the full-size one included, and the reduced ones on
+the engine, and a fourth the one-token ones on the one-token kernel
+(MOEQ_MTOK_MIN_TOKENS=2).
 The children use the same oracle comparisons and tolerances as the default
 run."""
 import os
@@ -42,3 +43,12 @@ def test_parity_one_token_on_the_persistent_engine():
            os.path.join(HERE, "test_gpu_layer.py"), "-k", "m1 or reduced"]
     r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, f"engine one-token path:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"
+
+
+def test_parity_one_token_on_the_one_token_kernel():
+    env = dict(os.environ, MOEQ_MTOK_MIN_TOKENS="2")
+    cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+           os.path.join(HERE, "test_gpu_layer.py"), os.path.join(HERE, "test_gpu_graph.py"),
+           os.path.join(HERE, "test_gpu_stack.py"), "-k", "m1 or (reduced and 1-) or graph or stack"]
+    r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, f"one-token kernel path:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"

@@ -10,7 +10,7 @@ replay), the eager call (MOEQ_STACK_EAGER) and a chain of moeq_moe_layer
 calls give the same bits: layers after the first route before they wait for
 the layer ahead, which changes when routing happens, not what it computes.
 A stack call made inside the caller's own capture lands in the caller's
-graph.  One token runs the one-token kernel, four the persistent engine, and
+graph.  One and four tokens run the multi-token kernel, and
 the full MoE shape runs two layers at one token."""
 import numpy as np
 import pytest

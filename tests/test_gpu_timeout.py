@@ -9,8 +9,8 @@ the limit.  It then checks the status, re-initialises the workspace and
 checks that a normal call on the same context still matches the oracle.
 A second case does the same to the count that the persistent engine's
 one-token layer waits for before its final combine (the engine serves one
-token when MOEQ_TOKEN_KERNEL=0; by default the one-token kernel does, which
-has no wait on another CTA at all), in a child process with that setting."""
+token when MOEQ_MTOK_KERNEL=0 and MOEQ_TOKEN_KERNEL=0), in a child process
+with that setting."""
 import os
 import subprocess
 import sys
@@ -60,8 +60,8 @@ def test_layer_combine_wait_reports_timeout_and_the_context_survives(orc):
     K group waits for every CTA's count.  With the count set out of reach that
     wait gives up, the status says so, and after a re-initialisation the layer
     is correct."""
-    if os.environ.get("MOEQ_TOKEN_KERNEL") != "0":
-        env = dict(os.environ, MOEQ_TOKEN_KERNEL="0")
+    if os.environ.get("MOEQ_TOKEN_KERNEL") != "0" or os.environ.get("MOEQ_MTOK_KERNEL") != "0":
+        env = dict(os.environ, MOEQ_TOKEN_KERNEL="0", MOEQ_MTOK_KERNEL="0")
         here = os.path.dirname(os.path.abspath(__file__))
         cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
                os.path.abspath(__file__), "-k", "combine_wait"]
