@@ -182,9 +182,12 @@ def kernel_source_hash(which: str):
     return code_hash(texts)
 
 
-def ncu_traffic(kernel: str, M: int):
+def ncu_traffic(kernel: str, M: int, launch_bytes: float | None = None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source; else None.  A record taken on a smaller
+    case (its algorithmic bytes below the launch's) is scaled to the launch
+    by the algorithmic bytes: the traffic follows the unique experts
+    streamed."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -192,7 +195,10 @@ def ncu_traffic(kernel: str, M: int):
         e = d[f"{kernel}_m{M}"]
         if e["source_hash"] != kernel_source_hash(e["sources"]):
             return None
-        return float(e["dram_bytes_per_launch"])
+        t = float(e["dram_bytes_per_launch"])
+        if launch_bytes and e.get("algorithmic_bytes") and abs(launch_bytes - e["algorithmic_bytes"]) > 1:
+            t *= launch_bytes / float(e["algorithmic_bytes"])
+        return t
     except Exception:
         return None
 
@@ -796,7 +802,7 @@ def main():
              "stream_kernel (whole MoE layer: route, gate_up+SwiGLU, down, combine)")
     roof = {"bound": "hbm", "kernel": kname,
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy), of {peak_kind}",
-            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": ncu_traffic("layer", args.M),
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": ncu_traffic("layer", args.M, r["kernel_bytes"]),
             "algorithmic_bytes_per_launch": r["kernel_bytes"], "ms_per_launch": round(k_ms, 5),
             "launch_duration": "timed region / launches (one launch per step, launches back to back)",
             "isolated_launch_ms": round(r["isolated_ms"], 5),

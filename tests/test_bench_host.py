@@ -50,6 +50,11 @@ def test_traffic_reported_only_for_the_hash_it_was_taken_on(tmp_path, monkeypatc
     monkeypatch.setattr(b, "kernel_source_hash", lambda which: "abc" if which == "token" else "zzz")
     assert b.ncu_traffic("layer", 1) == 307.0
     assert b.ncu_traffic("layer", 16) is None        # no record for that workload
+    # a record of a smaller case scales with the launch's algorithmic bytes
+    rec["layer_m1"]["algorithmic_bytes"] = 100
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert b.ncu_traffic("layer", 1, 100) == 307.0
+    assert b.ncu_traffic("layer", 1, 200) == 614.0
     monkeypatch.setattr(b, "kernel_source_hash", lambda which: "def")
     assert b.ncu_traffic("layer", 1) is None          # the kernel changed since the capture
 
