@@ -867,29 +867,40 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
 }
 
 // ------------------------------------------------------------------ dense FFN
-// One token through one dense FFN: the one-token kernel with no routing (the
-// one expert is its "shared" expert).  Workspace: header, h [I], the down
-// partials [I/128, H], the arrival counts and the completion count.
+// M tokens through one dense FFN: the multi-token kernel with no routing
+// (top_k = 0: the one expert serves every token), or, for one token with
+// MOEQ_MTOK_MIN_TOKENS above 1, the one-token kernel with no routing.
+// Workspace: header, h [M, I], then the multi-token kernel's areas (counts,
+// split-column slots, x's codes and scales, partials [M][H/256][1][I/128]
+// [256]) and the one-token kernel's (partials [I/128, H], arrival counts).
 struct DenseWs {
-    size_t h, part, tickets, end;
+    size_t h, mt_cnt, mt_slots, mt_xq, mt_xs, mt_part, part, tickets, end;
 };
 
-DenseWs dense_ws_layout(int H, int I) {
+DenseWs dense_ws_layout(int M, int H, int I, int grid) {
     DenseWs l;
     l.h = kHeader;
-    l.part = align_up(l.h + sizeof(float) * static_cast<size_t>(I), 256);
-    l.tickets = align_up(l.part + sizeof(float) * static_cast<size_t>(I / 128) * H, 256);
+    l.mt_cnt = align_up(l.h + sizeof(float) * static_cast<size_t>(M) * I, 256);
+    l.mt_slots = align_up(l.mt_cnt + sizeof(int) * (kMtokFlags + grid + 1), 256);
+    l.mt_xq = align_up(l.mt_slots + static_cast<size_t>(grid + 1) * kMtokSlotBytes, 256);
+    l.mt_xs = align_up(l.mt_xq + static_cast<size_t>(H / 128) * kMtokXGroupBytes, 256);
+    l.mt_part = align_up(l.mt_xs + sizeof(float) * static_cast<size_t>(H / 128) * 16, 256);
+    l.part = align_up(l.mt_part + sizeof(float) * static_cast<size_t>(M) * H * (I / 128), 256);
+    l.tickets = align_up(l.part + (M == 1 ? sizeof(float) * static_cast<size_t>(I / 128) * H : 0), 256);
     l.end = align_up(l.tickets + sizeof(int) * (static_cast<size_t>(H / 256) + kGqUnits), 256);
     return l;
 }
 
 bool dense_shape_ok(int M, int H, int I) {
-    return M == 1 && H > 0 && I > 0 && H % 256 == 0 && I % 128 == 0 && H <= kTokenMaxH && I <= MOEQ_MAX_K;
+    return M >= 1 && M <= MOEQ_MAX_TOKENS && H > 0 && I > 0 && H % 256 == 0 && I % 128 == 0 && H <= kTokenMaxH &&
+           I <= MOEQ_MAX_K && (M == 1 || (mtok_kernel_enabled() && M >= mtok_min_tokens()));
 }
 
 size_t moeq_dense_ffn_workspace_size(int M, int H, int I) {
     if (!dense_shape_ok(M, H, I)) return 0;
-    return dense_ws_layout(H, I).end;
+    const DeviceInfo dev = current_device();
+    if (!dev.ok) return 0;
+    return dense_ws_layout(M, H, I, dev.sms).end;
 }
 
 moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_gu, const float* s_gu,
@@ -908,9 +919,42 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
     if (!dense_shape_ok(M, H, I)) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
-    const DenseWs l = dense_ws_layout(H, I);
+    const DenseWs l = dense_ws_layout(M, H, I, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < l.end) return MOEQ_ERR_WORKSPACE;
     char* base = static_cast<char*>(ws);
+    float* h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
+    uintptr_t key = stream_key(stream);
+    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+    const bool pdl = pdl_enabled() && !after_weight_write;
+    if (mtok_kernel_enabled() && M >= mtok_min_tokens()) {
+        MtokArgs t = {};
+        t.x = static_cast<const __nv_bfloat16*>(x);
+        t.logits = nullptr;
+        t.M = M;
+        t.H = H;
+        t.I = I;
+        t.KB = H / 128;
+        t.RB = I / 128;
+        t.E_routed = 0;   // expert 0 is the one expert
+        t.top_k = 0;
+        t.w_gu = w_gu;
+        t.s_gu = s_gu;
+        t.w_d = w_d;
+        t.s_d = s_d;
+        t.out = static_cast<__nv_bfloat16*>(out);
+        t.h = h;
+        t.q_x = q_x_opt;
+        t.s_x = s_x_opt;
+        t.q_h = q_h_opt;
+        t.s_h = s_h_opt;
+        t.status = reinterpret_cast<int*>(base + kOffStatus);
+        t.cnt = reinterpret_cast<int*>(base + l.mt_cnt);
+        t.slots = reinterpret_cast<uint8_t*>(base + l.mt_slots);
+        t.xq = reinterpret_cast<uint8_t*>(base + l.mt_xq);
+        t.xs = reinterpret_cast<float*>(base + l.mt_xs);
+        t.part = reinterpret_cast<float*>(base + l.mt_part);
+        return cuda_status(launch_mtok(t, dev.sms, pdl, as_stream(stream)));
+    }
     TokenArgs t = {};
     t.x = static_cast<const __nv_bfloat16*>(x);
     t.logits = nullptr;
@@ -926,7 +970,7 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
     t.w_d = w_d;
     t.s_d = s_d;
     t.out = static_cast<__nv_bfloat16*>(out);
-    t.h = h_opt ? h_opt : reinterpret_cast<float*>(base + l.h);
+    t.h = h;
     t.q_x = q_x_opt;
     t.s_x = s_x_opt;
     t.q_h = q_h_opt;
@@ -935,9 +979,7 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
     t.tickets = reinterpret_cast<int*>(base + l.tickets);
     t.gq = t.tickets + H / 256;
     t.part = reinterpret_cast<float*>(base + l.part);
-    uintptr_t key = stream_key(stream);
-    const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
-    return cuda_status(launch_token(t, dev.sms, pdl_enabled() && !after_weight_write, as_stream(stream)));
+    return cuda_status(launch_token(t, dev.sms, pdl, as_stream(stream)));
 }
 
 moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int M, int top_k, void* out_bf16,

@@ -55,6 +55,9 @@
 //               overlap the end of the streams.
 // Launched with programmatic dependent launch: before griddepcontrol.wait a
 // CTA only starts its share of the shared expert's weights towards L2.
+//
+// With top_k = 0 the same kernel is a dense FFN (no routing): the one expert
+// is the "shared" one, serving every token.
 #include "moeq_device.cuh"
 #include "moeq_internal.h"
 #include "moeq_route.cuh"
@@ -250,6 +253,22 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
     p.offs = sm.plan.offs;
     p.pair_tok = sm.plan.pair_tok;
     p.pair_of = sm.plan.pair_of;
+    if (a.top_k == 0) {
+        // a dense FFN: no routing -- one expert (index E_routed) serving
+        // every token, one pair per token
+        if (tid == 0) {
+            sm.plan.n_uniq = 1;
+            sm.plan.uniq[0] = a.E_routed;
+            sm.plan.offs[0] = 0;
+            sm.plan.offs[1] = a.M;
+        }
+        if (tid < a.M) {
+            sm.plan.pair_tok[tid] = tid;
+            sm.plan.pair_of[tid] = tid;
+        }
+        named_sync(2, kRouteThreads);
+        return;
+    }
     if (a.M == 1) {
         // one token: one warp, no block barrier
         if (tid < 32) {
@@ -878,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
             prefetch_l2(i < lg_lines ? reinterpret_cast<const char*>(a.logits) + 128 * i
                                      : reinterpret_cast<const char*>(a.x) + 128 * (i - lg_lines));
     }
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && a.top_k > 0) {
         const long long gu_tiles = 2LL * a.RB * a.KB, tiles = gu_tiles + static_cast<long long>(a.KB) * a.RB;
         const long long lo = tiles * blockIdx.x / G, hi = tiles * (blockIdx.x + 1) / G;
         for (long long t = lo + lane; t < hi; t += 32) {

@@ -266,29 +266,31 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
                          void* out_bf16, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* moeq_dense_ffn -- one dense FFN for one token, in ONE kernel:            */
+/* moeq_dense_ffn -- one dense FFN for M tokens, in ONE kernel:             */
 /*   out = bf16( down( quant( silu(gate) * up ) ) ), gate/up = gate_up(quant(x)) */
 /*   (GLM-5.2 x10 §4: the live quantisation fused into the GEMMs -- the      */
-/*   "PQ-GEMM" FFN; §1: K split so that every SM streams.)  The one-token    */
-/*   kernel of moeq_moe_layer with no routing: one CTA per 128-wide K group */
-/*   of down streams that group's gate and up rows, forms and quantises the  */
-/*   group, and streams down's K group against every output row; the fp32   */
-/*   partials of each 256 output rows are summed in a fixed order by idle    */
-/*   warps.  Launched with programmatic dependent launch (see               */
+/*   "PQ-GEMM" FFN; §1: K split so that every SM streams.)  The multi-token  */
+/*   kernel of moeq_moe_layer with no routing (top_k = 0): one column per    */
+/*   128-wide K group of down streams that group's gate and up rows for     */
+/*   every token, forms and quantises the group, and streams down's K group */
+/*   against every output row; the fp32 partials of each (token, 16 output  */
+/*   rows) are summed in a fixed order by idle warps.  With                 */
+/*   MOEQ_MTOK_MIN_TOKENS above 1, one token runs the one-token kernel (CUDA */
+/*   cores) instead.  Launched with programmatic dependent launch (see      */
 /*   moeq_moe_layer): the weights must not be written by the kernel right   */
 /*   ahead of this call on the same stream, except by moeq_quant_weight /    */
 /*   moeq_pack_weight, which this library tracks.                          */
-/*   M      1 (other M: MOEQ_ERR_UNSUPPORTED_SHAPE; the GEMM calls serve    */
-/*           them)                                                          */
-/*   x      [1, H] bf16; H a multiple of 256, at most 6144; I a multiple    */
+/*   M      1 .. MOEQ_MAX_TOKENS                                            */
+/*   x      [M, H] bf16; H a multiple of 256, at most 6144; I a multiple    */
 /*           of 128                                                         */
 /*   w_gu/s_gu [1, 2I, H] tile-major + [1, 2I/128, H/128]: gate rows [0, I), */
 /*           up rows [I, 2I); w_d/s_d [1, H, I] + [1, H/128, I/128]          */
-/*   out    [1, H] bf16                                                     */
-/*   h_opt [1, I] f32, q_x_opt/s_x_opt [1, H] u8 + [1, H/128] f32,          */
-/*   q_h_opt/s_h_opt [1, I] u8 + [1, I/128] f32: optional dumps (each pair  */
+/*   out    [M, H] bf16                                                     */
+/*   h_opt [M, I] f32, q_x_opt/s_x_opt [M, H] u8 + [M, H/128] f32,          */
+/*   q_h_opt/s_h_opt [M, I] u8 + [M, I/128] f32: optional dumps (each pair  */
 /*           both or neither) of h and of both live quantisations           */
-/*   ws     moeq_dense_ffn_workspace_size(M, H, I) bytes, zeroed once       */
+/*   ws     moeq_dense_ffn_workspace_size(M, H, I) bytes (0 for shapes out  */
+/*           of range or with no device), zeroed once                       */
 /* ------------------------------------------------------------------------ */
 size_t moeq_dense_ffn_workspace_size(int M, int H, int I);
 moeq_status moeq_dense_ffn(const void* x, int M, int H, int I,

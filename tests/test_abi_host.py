@@ -112,14 +112,14 @@ def test_argument_validation_without_device(lib):
 
 
 def test_dense_ffn_workspace_size_rejects_shapes(lib):
-    """moeq_dense_ffn serves one token, H a multiple of 256 up to 6144, I a
-    multiple of 128: other shapes get a zero workspace size (and the call
+    """moeq_dense_ffn serves 1..16 tokens, H a multiple of 256 up to 6144, I
+    a multiple of 128: other shapes get a zero workspace size (and the call
     MOEQ_ERR_UNSUPPORTED_SHAPE)."""
-    assert lib.moeq_dense_ffn_workspace_size(2, 512, 256) == 0
+    assert lib.moeq_dense_ffn_workspace_size(0, 512, 256) == 0
+    assert lib.moeq_dense_ffn_workspace_size(17, 512, 256) == 0
     assert lib.moeq_dense_ffn_workspace_size(1, 384, 256) == 0
     assert lib.moeq_dense_ffn_workspace_size(1, 8192, 256) == 0
     assert lib.moeq_dense_ffn_workspace_size(1, 512, 200) == 0
-    assert lib.moeq_dense_ffn_workspace_size(1, 512, 256) > 0
 
 
 def test_stack_rejects_layer_count_before_the_device(lib):

@@ -1,13 +1,15 @@
-"""GPU parity of moeq_dense_ffn (one token through a dense FFN: live quant of
+"""GPU parity of moeq_dense_ffn (M tokens through a dense FFN: live quant of
 x, gate_up, SwiGLU, live quant of h, down, bf16) against the oracle.
 
-The call runs the one-token kernel with no routing.  Checked: x's and h's
+The call runs the multi-token kernel with no routing (test_gpu_paths re-runs
+the one-token cases on the one-token kernel).  Checked: x's and h's
 quantisation codes and scales bit for bit (h's against the oracle's
 quantisation of the GPU's own fp32 h), h within the STRICT bound propagated
 through SwiGLU, the bf16 output within SPEC plus half a bf16 ulp at its
 magnitude, and a second call bit-identical.  Shapes: the full dense FFN
-(hidden 6144, intermediate 12288: 96 columns on 152 SMs), a reduced one with
-more columns than SMs (several columns per CTA), and a minimal one.
+(hidden 6144, intermediate 12288: 96 columns on 152 SMs) at 1 and 4 tokens,
+a reduced one with more columns than SMs (columns split between CTAs), and
+minimal ones.
 """
 import numpy as np
 import pytest
@@ -20,8 +22,9 @@ from test_gpu_gemm import h_bound
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H,I,seed", [(6144, 12288, None), (512, 2560 * 8, 71), (256, 128, 72)])
-def test_dense_ffn_matches_oracle(orc, H, I, seed):
+@pytest.mark.parametrize("M,H,I,seed", [(1, 6144, 12288, None), (1, 512, 2560 * 8, 71), (1, 256, 128, 72),
+                                        (4, 6144, 12288, None), (16, 512, 2560, 73), (3, 256, 128, 74)])
+def test_dense_ffn_matches_oracle(orc, M, H, I, seed):
     from bandwidth_bound_fp8_gb300 import moeq
     cfg = synth.DENSE_FFN
     if seed is None:
@@ -30,16 +33,16 @@ def test_dense_ffn_matches_oracle(orc, H, I, seed):
         n_out, scale = max(1, round(0.01 * H)), 30.0
     gu = Experts(1, 2 * I, H, base_seed=seed, which=0)
     dn = Experts(1, H, I, base_seed=seed, which=1)
-    x = synth.activations_bf16(1, H, seed, n_out, scale, device="cuda")
-    ws = moeq.Workspace(moeq.moeq_dense_ffn_workspace_size(1, H, I))
+    x = synth.activations_bf16(M, H, seed + M, n_out, scale, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_dense_ffn_workspace_size(M, H, I))
     outs = []
     for _ in range(2):
-        out = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
-        h = torch.full((1, I), float("nan"), device="cuda")
-        qx = torch.zeros((1, H), dtype=torch.uint8, device="cuda")
-        sx = torch.zeros((1, H // 128), dtype=torch.float32, device="cuda")
-        qh = torch.zeros((1, I), dtype=torch.uint8, device="cuda")
-        sh = torch.zeros((1, I // 128), dtype=torch.float32, device="cuda")
+        out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+        h = torch.full((M, I), float("nan"), device="cuda")
+        qx = torch.zeros((M, H), dtype=torch.uint8, device="cuda")
+        sx = torch.zeros((M, H // 128), dtype=torch.float32, device="cuda")
+        qh = torch.zeros((M, I), dtype=torch.uint8, device="cuda")
+        sh = torch.zeros((M, I // 128), dtype=torch.float32, device="cuda")
         moeq.moeq_dense_ffn(x, H, I, gu.q, gu.s, dn.q, dn.s, out, ws, h=h, q_x=qx, s_x=sx, q_h=qh, s_h=sh)
         torch.cuda.synchronize()
         assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
@@ -52,12 +55,13 @@ def test_dense_ffn_matches_oracle(orc, H, I, seed):
     assert np.array_equal(to_np(sx).view(np.uint32), sx_ref.view(np.uint32)), "x scales"
     qgu, sgu = gu.oracle(orc, 0)
     gy, gT = orc.gemm(qx_ref, sx_ref, qgu, sgu)
-    b = h_bound(gy[0, :I], gy[0, I:], gT[0, :I], gT[0, I:], STRICT)
-    h_ref = orc.swiglu_vec(gy[0, :I], gy[0, I:]).astype(np.float64)
-    hg = to_np(h)[0]
-    err = np.abs(hg.astype(np.float64) - h_ref)
-    assert (err <= b).all(), f"h: worst {np.max(err - b)}"
-    qh_ref, sh_ref = orc.quant_act(hg[None].astype(np.float32))
+    hg = to_np(h)
+    for m in range(M):
+        b = h_bound(gy[m, :I], gy[m, I:], gT[m, :I], gT[m, I:], STRICT)
+        h_ref = orc.swiglu_vec(gy[m, :I], gy[m, I:]).astype(np.float64)
+        err = np.abs(hg[m].astype(np.float64) - h_ref)
+        assert (err <= b).all(), f"h token {m}: worst {np.max(err - b)}"
+    qh_ref, sh_ref = orc.quant_act(hg.astype(np.float32))
     assert np.array_equal(to_np(qh), qh_ref), "h codes"
     assert np.array_equal(to_np(sh).view(np.uint32), sh_ref.view(np.uint32)), "h scales"
 
@@ -65,10 +69,14 @@ def test_dense_ffn_matches_oracle(orc, H, I, seed):
     qd, sd = dn.oracle(orc, 0)
     hq, hs = orc.quant_act(orc.swiglu_vec(gy[:, :I], gy[:, I:]))
     y, T = orc.gemm(hq, hs, qd, sd)
-    ref16 = np.array([orc.f64_to_bf16_bits(v) for v in y[0]], np.uint16)
-    o = orc.bf16_bits_to_f32_array(bf16_bits(outs[0])[0]).astype(np.float64)
+    ref16 = np.array([orc.f64_to_bf16_bits(v) for v in y.ravel()], np.uint16).reshape(M, H)
+    o = orc.bf16_bits_to_f32_array(bf16_bits(outs[0])).astype(np.float64)
     r16 = orc.bf16_bits_to_f32_array(ref16).astype(np.float64)
-    bound = SPEC_REL * T[0] + SPEC_ABS + half_ulp_bf16(o, r16)
-    err = np.abs(o - y[0])
+    bound = SPEC_REL * T + SPEC_ABS + half_ulp_bf16(o, r16)
+    err = np.abs(o - y)
     assert (err <= bound).all(), f"out: {(err > bound).sum()} outside, worst {np.max(err - bound)}"
-    assert np.mean(bf16_bits(outs[0])[0] == ref16) > 0.9
+    # how close in practice: most outputs round to the reference's bf16.
+    # The two sides' h can differ by an fp32 ulp and so, now and then, by an
+    # E4M3 code (within SPEC); the more h values per output, the more often
+    # that moves a bf16 rounding
+    assert np.mean(bf16_bits(outs[0]) == ref16) > (0.9 if I <= 12288 else 0.75)

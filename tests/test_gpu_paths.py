@@ -49,6 +49,7 @@ def test_parity_one_token_on_the_one_token_kernel():
     env = dict(os.environ, MOEQ_MTOK_MIN_TOKENS="2")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            os.path.join(HERE, "test_gpu_layer.py"), os.path.join(HERE, "test_gpu_graph.py"),
-           os.path.join(HERE, "test_gpu_stack.py"), "-k", "m1 or (reduced and 1-) or graph or stack"]
+           os.path.join(HERE, "test_gpu_stack.py"), os.path.join(HERE, "test_gpu_dense.py"),
+           "-k", "m1 or (reduced and 1-) or graph or stack or (dense and 1-)"]
     r = subprocess.run(cmd, env=env, cwd=os.path.dirname(HERE), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, f"one-token kernel path:\n{r.stdout[-3000:]}\n{r.stderr[-2000:]}"
