@@ -615,6 +615,17 @@ size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int t
     return layer_ws_layout(M, H, I, E, top_k, dev.sms).s.end;
 }
 
+size_t moeq_layer_ws_count_offset(int M, int H, int I, int n_experts_incl_shared, int top_k, int which) {
+    const int E = n_experts_incl_shared - 1;
+    if (!moeq_workspace_size(M, H, I, n_experts_incl_shared, top_k) || M < mtok_min_tokens()) return 0;
+    const size_t base = layer_ws_layout(M, H, I, E, top_k, current_device().sms).mt_cnt;
+    switch (which) {
+    case 0: return base + sizeof(int) * kMtokX;   // K group 0 of x: quantised groups in
+    case 1: return base + sizeof(int) * kMtokU;   // output unit 0: down partials stored
+    default: return 0;
+    }
+}
+
 size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up) {
     if (rows_out <= 0 || rows_out % 128 || max_uniq < 1 || K <= 0 || K % 128 || K > MOEQ_MAX_K || rows_in < 1)
         return 0;

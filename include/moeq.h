@@ -135,6 +135,13 @@ size_t moeq_workspace_size(int M, int H, int I, int n_experts_incl_shared, int t
  * K = K, rows_in = max_pairs.  max_uniq as for the plan the call is given.
  * Depends on the current device's SM count; 0 on invalid arguments. */
 size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up);
+/* Diagnostics for failure-injection tests: the byte offset, inside a       */
+/* moeq_moe_layer workspace, of one int count that the multi-token kernel   */
+/* waits on (which = 0: the quantised groups of x's K group 0; 1: the down  */
+/* partials stored for output unit 0), or 0 when the call's shape does not  */
+/* run that kernel.  A count set out of reach makes the kernel's bounded    */
+/* wait run out (MOEQ_ERR_TIMEOUT); re-initialise the workspace after.      */
+size_t moeq_layer_ws_count_offset(int M, int H, int I, int n_experts_incl_shared, int top_k, int which);
 /* Zero the workspace (split-K tickets and the device status word) on
  * `stream`.  Needed once after allocation; kernels leave it zeroed.  After a
  * launch that recorded an error (e.g. a bounded wait that gave up, which

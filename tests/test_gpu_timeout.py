@@ -85,3 +85,37 @@ def test_layer_combine_wait_reports_timeout_and_the_context_survives(orc):
     torch.cuda.synchronize()
     assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
     check_layer(orc, lay, x, logits, k, with_y=False)
+
+
+@pytest.mark.parametrize("M,which", [(1, 0), (4, 0), (2, 1)])
+def test_layer_kernel_wait_reports_timeout_and_the_context_survives(orc, M, which):
+    """The multi-token kernel (every layer of 1..16 tokens by default): one
+    of the counts it waits on -- x's K group 0 (released to the producer
+    once every token's group is in) or output unit 0 (summed once every
+    column's partials are in) -- is set far out of reach in the workspace.
+    The wait gives up after its limit, every role stops and drains, the
+    status says MOEQ_ERR_TIMEOUT, and after a re-initialisation the layer
+    on the same context matches the oracle."""
+    from test_gpu_layer import Layer, check_layer
+    from bandwidth_bound_fp8_gb300 import moeq
+    E, H, I, k = 8, 512, 256, 2
+    off = moeq.moeq_layer_ws_count_offset(M, H, I, E + 1, k, which)
+    if off == 0:
+        pytest.skip("the multi-token kernel does not serve this shape here")
+    lay = Layer(E, H, I, seed=95 + M)
+    x = synth.activations_bf16(M, H, 96 + M, 2, 20.0, device="cuda")
+    logits = synth.logits_f32(M, E, 97 + M, device="cuda")
+    out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    ws = moeq.Workspace(moeq.moeq_workspace_size(M, H, I, E + 1, k))
+    assert off % 4 == 0 and off < ws.nbytes
+    ws.t.view(torch.int32)[off // 4] = -(1 << 30)
+    moeq.moeq_moe_layer(x, logits, H, I, E, k, lay.gu.q, lay.gu.s, lay.dn.q, lay.dn.s, out, ws)
+    torch.cuda.synchronize()   # returns: the kernel gave up instead of hanging
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == moeq.MOEQ_ERR_TIMEOUT
+    moeq.moeq_workspace_init(ws.t, ws.nbytes)
+    ref = check_layer(orc, lay, x, logits, k, with_y=False)   # against the oracle, a fresh workspace
+    moeq.moeq_moe_layer(x, logits, H, I, E, k, lay.gu.q, lay.gu.s, lay.dn.q, lay.dn.s, out, ws)
+    torch.cuda.synchronize()
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))   # the re-initialised one, same bits
+
