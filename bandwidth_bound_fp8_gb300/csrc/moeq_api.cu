@@ -405,6 +405,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         t.xq = reinterpret_cast<uint8_t*>(base + l.mt_xq);
         t.xs = reinterpret_cast<float*>(base + l.mt_xs);
         t.part = reinterpret_cast<float*>(base + l.mt_part);
+        t.route_early = route_early ? 1 : 0;
         if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
             return MOEQ_ERR_CUDA;
         if (launch_mtok(t, dev.sms, pdl_enabled() && allow_pdl, st) != cudaSuccess) return MOEQ_ERR_CUDA;

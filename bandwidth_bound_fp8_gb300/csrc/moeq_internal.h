@@ -171,7 +171,10 @@ struct MtokArgs {
     uint8_t* slots;              // [grid + 1][kMtokSlotBytes]: what a split column's head publishes
     uint8_t* xq;                 // [KB][16 * 128]: x's codes, token n in row n (gate_up's B operand)
     float* xs;                   // [KB][16]: x's scales
-    float* part;                 // [M][H/256][16][top_k + 1][RB][16] down partials
+    float* part;                 // [M][H/256][top_k + 1][RB][256] down partials
+    int route_early;             // 1: the logits are not written by the kernel ahead on the stream, so
+                                 // the tokens are routed (and the first weight tiles issued) before
+                                 // griddepcontrol.wait
 };
 // counts (ints): CTAs done, quantised groups per K group of x, down partials
 // stored per 256-row output unit, and the split columns' flags (one per CTA

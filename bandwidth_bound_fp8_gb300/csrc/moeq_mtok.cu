@@ -130,6 +130,9 @@ __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { named_sync(1, kEpiThreads); }
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Sleeping bounded wait (producer, epilogue); on expiry the launch is
@@ -909,18 +912,27 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    pdl_wait();
+    // Routing reads only the logits.  When they are the caller's inputs (no
+    // kernel ahead writes them, as in a stack of layers), warps 0-5 route
+    // before griddepcontrol.wait, and the producer issues its first weight
+    // tiles before it too (x's codes follow once quantised, after the wait).
+    // Everything that writes global memory or reads the previous kernel's
+    // output waits first.
+    const bool early = a.route_early != 0;
     if (warp < kQuantWarp0) {
-        route_all(a, sm, tid);   // ends with the plan in every CTA's shared memory
+        if (!early) pdl_wait();
+        route_all(a, sm, tid);                 // the plan in every CTA's shared memory (warps 0-5)
+        named_arrive(3, kThreads - 32);        // ... and for warps 7-11
     } else {
+        pdl_wait();
         quantise_x(a, warp - kQuantWarp0, lane);
+        if (warp != kQuantWarp0) named_sync(3, kThreads - 32);
     }
     if (warp == kQuantWarp0) {
         // warp 6 goes on at once to release x's K groups as the grid's
-        // quantisation completes (it needs no plan); the others wait for it
+        // quantisation completes (it needs no plan)
         x_ready(a, sm, lane);
     } else {
-        named_sync(3, kThreads - 32);
         const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.KB + a.KB / 2;
         const Share sh = share_of(ncols, spc);
         if (warp == kProducerWarp) {
@@ -941,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
                 }
             }
         } else if (warp < kEpiWarp0 + kEpiWarps) {
+            if (early) pdl_wait();
             if (a.M <= 4)
                 epilogue<4>(a, sm, sh, spc, warp, lane);
             else if (a.M <= 8)
