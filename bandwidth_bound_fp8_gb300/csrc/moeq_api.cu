@@ -203,6 +203,101 @@ StreamWs gemm_ws_layout(int kind, int RB, int K, int rows_a, int max_uniq, int g
     return stream_ws_layout(kHeader, rows, ks, 1, tk, grid, 0, 0);
 }
 
+// The multi-token kernel's areas for a standalone GEMM call (gate_up alone or
+// down alone), from `base` on: counts and flags, split-column slots (gate_up),
+// the quantised input's codes and scales (gate_up: 16 token rows per K group;
+// down: every pair row), and the down partials [pair][N/256][K/128][256].
+struct MtokGemmWs {
+    size_t cnt, slots, xq, xs, part, end;
+};
+
+MtokGemmWs mtok_gemm_ws(bool gate_up, int rows_out, int K, int rows_in, int grid, size_t base) {
+    MtokGemmWs l;
+    const size_t KX = static_cast<size_t>(K / 128);
+    l.cnt = align_up(base, 256);
+    l.slots = align_up(l.cnt + sizeof(int) * (kMtokFlags + grid + 1), 256);
+    l.xq = align_up(l.slots + (gate_up ? static_cast<size_t>(grid + 1) * kMtokSlotBytes : 0), 256);
+    l.xs = align_up(l.xq + (gate_up ? KX * kMtokXGroupBytes : KX * rows_in * 128), 256);
+    l.part = align_up(l.xs + sizeof(float) * KX * (gate_up ? 16 : rows_in), 256);
+    l.end = align_up(l.part + (gate_up ? 0 : sizeof(float) * rows_in * static_cast<size_t>(rows_out) * KX), 256);
+    return l;
+}
+
+// The standalone calls run the multi-token kernel where it takes them: at
+// most 16 tokens (gate_up; down: at most 16 rows per expert, as the call
+// requires of every plan), K and (down) N up to 6144, N a multiple of 256,
+// and a plan that fits the kernel's shared copy of it.  The kernel checks
+// the plan as the persistent engine does.
+constexpr int kMtokMaxPairs = MOEQ_MAX_TOKENS * (MOEQ_MAX_TOPK + 1);
+constexpr int kMtokMaxSlots = MOEQ_MAX_TOKENS * MOEQ_MAX_TOPK;
+bool gateup_mtok_ok(int M, int H, int max_uniq, int max_pairs) {
+    return mtok_kernel_enabled() && M <= MOEQ_MAX_TOKENS && H <= kTokenMaxH && max_pairs <= kMtokMaxPairs &&
+           max_uniq <= kMtokMaxSlots;
+}
+bool down_mtok_ok(int K, int N, int max_uniq, int max_pairs) {
+    return mtok_kernel_enabled() && N % 256 == 0 && N <= kTokenMaxH && K <= kTokenMaxH &&
+           max_pairs <= kMtokMaxPairs && max_uniq <= kMtokMaxSlots;
+}
+
+// The arguments of the multi-token kernel's standalone modes.
+MtokArgs mtok_gemm_args(bool gate_up, const void* x, int x_f32, int rows, int K, int rows_out, const uint8_t* w,
+                        const float* sw, const int32_t* uniq, const int32_t* offs, const int32_t* pair_tok,
+                        const int32_t* n_uniq, int n_experts, int max_uniq, int max_pairs, float* out,
+                        uint8_t* q_opt, float* s_opt, void* ws, const MtokGemmWs& l) {
+    char* base = static_cast<char*>(ws);
+    MtokArgs t = {};
+    t.x = x;
+    t.x_f32 = x_f32;
+    t.x_ld = K;
+    t.M = rows;
+    t.KX = K / 128;
+    t.top_k = 0;
+    t.E_routed = 0;
+    t.n_experts = n_experts;
+    t.max_uniq = max_uniq;
+    t.max_pairs = max_pairs;
+    t.plan.n_uniq = const_cast<int32_t*>(n_uniq);
+    t.plan.uniq = const_cast<int32_t*>(uniq);
+    t.plan.offs = const_cast<int32_t*>(offs);
+    t.plan.pair_tok = const_cast<int32_t*>(pair_tok);
+    if (gate_up) {
+        // x [M, H]; h [pairs, I]: H = K, I = rows_out / 2
+        t.mode = kMtokGateUp;
+        t.H = K;
+        t.I = rows_out / 2;
+        t.KB = K / 128;
+        t.RB = rows_out / 256;
+        t.GS = t.KB;
+        t.NU = 0;
+        t.ntmax = rows;
+        t.w_gu = w;
+        t.s_gu = sw;
+        t.h = out;
+    } else {
+        // a [pairs, K]; y [pairs, N]: N = rows_out
+        t.mode = kMtokDown;
+        t.H = rows_out;
+        t.I = K;
+        t.KB = rows_out / 128;
+        t.RB = K / 128;
+        t.GS = 0;
+        t.NU = rows_out / 256;
+        t.ntmax = rows < MOEQ_MAX_TOKENS ? rows : MOEQ_MAX_TOKENS;
+        t.w_d = w;
+        t.s_d = sw;
+        t.out_f32 = out;
+    }
+    t.q_x = q_opt;
+    t.s_x = s_opt;
+    t.status = reinterpret_cast<int*>(base + kOffStatus);
+    t.cnt = reinterpret_cast<int*>(base + l.cnt);
+    t.slots = gate_up ? reinterpret_cast<uint8_t*>(base + l.slots) : nullptr;
+    t.xq = reinterpret_cast<uint8_t*>(base + l.xq);
+    t.xs = reinterpret_cast<float*>(base + l.xs);
+    t.part = gate_up ? nullptr : reinterpret_cast<float*>(base + l.part);
+    return t;
+}
+
 struct PlanLayout {
     size_t topk_id, topk_w, n_uniq, uniq, offs, pair_tok, pair_of, end;
 };
@@ -406,6 +501,13 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         t.xs = reinterpret_cast<float*>(base + l.mt_xs);
         t.part = reinterpret_cast<float*>(base + l.mt_part);
         t.route_early = route_early ? 1 : 0;
+        t.mode = kMtokLayer;
+        t.GS = t.KB;
+        t.NU = t.KB / 2;
+        t.KX = t.KB;
+        t.x_ld = H;
+        t.x_f32 = 0;
+        t.ntmax = M;
         if (events_opt && cudaEventRecord(static_cast<cudaEvent_t>(events_opt[0]), st) != cudaSuccess)
             return MOEQ_ERR_CUDA;
         if (launch_mtok(t, dev.sms, pdl_enabled() && allow_pdl, st) != cudaSuccess) return MOEQ_ERR_CUDA;
@@ -627,12 +729,32 @@ size_t moeq_layer_ws_count_offset(int M, int H, int I, int n_experts_incl_shared
     }
 }
 
+size_t moeq_gemm_ws_count_offset(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up, int which) {
+    if (!moeq_gemm_workspace_size(rows_out, K, rows_in, max_uniq, is_gate_up)) return 0;
+    const bool mt = is_gate_up ? gateup_mtok_ok(rows_in, K, max_uniq, rows_in * (MOEQ_MAX_TOPK + 1))
+                               : down_mtok_ok(K, rows_out, max_uniq, rows_in);
+    if (!mt || (which == 1 && is_gate_up)) return 0;
+    const DeviceInfo dev = current_device();
+    const size_t end = gemm_ws_layout(is_gate_up ? 0 : 1, rows_out / 128, K, rows_in, max_uniq, dev.sms).end;
+    const size_t base = mtok_gemm_ws(is_gate_up != 0, is_gate_up ? 2 * rows_out : rows_out, K, rows_in, dev.sms, end).cnt;
+    switch (which) {
+    case 0: return base + sizeof(int) * kMtokX;
+    case 1: return base + sizeof(int) * kMtokU;
+    default: return 0;
+    }
+}
+
 size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up) {
     if (rows_out <= 0 || rows_out % 128 || max_uniq < 1 || K <= 0 || K % 128 || K > MOEQ_MAX_K || rows_in < 1)
         return 0;
     const DeviceInfo dev = current_device();
     if (!dev.sms) return 0;
-    return gemm_ws_layout(is_gate_up ? 0 : 1, rows_out / 128, K, rows_in, max_uniq, dev.sms).end;
+    const size_t end = gemm_ws_layout(is_gate_up ? 0 : 1, rows_out / 128, K, rows_in, max_uniq, dev.sms).end;
+    // room for the multi-token kernel where it may serve the call
+    if (is_gate_up ? gateup_mtok_ok(rows_in, K, max_uniq, rows_in * (MOEQ_MAX_TOPK + 1))
+                   : down_mtok_ok(K, rows_out, max_uniq, rows_in))
+        return mtok_gemm_ws(is_gate_up != 0, is_gate_up ? 2 * rows_out : rows_out, K, rows_in, dev.sms, end).end;
+    return end;
 }
 
 moeq_status moeq_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -700,6 +822,15 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     if (!dev.ok) return MOEQ_ERR_DEVICE;
     const StreamWs wl = gemm_ws_layout(0, I / 128, H, M, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
+    if (gateup_mtok_ok(M, H, max_uniq, max_pairs)) {
+        const MtokGemmWs ml = mtok_gemm_ws(true, 2 * I, H, M, dev.sms, wl.end);
+        if (ws_bytes < ml.end) return MOEQ_ERR_WORKSPACE;
+        const MtokArgs t = mtok_gemm_args(true, x, x_dtype == MOEQ_F32, M, H, 2 * I, w_gu, s_gu, uniq, offs, pair_tok,
+                                          n_uniq_dev, n_experts, max_uniq, max_pairs, h, q_x_opt, s_x_opt, ws, ml);
+        uintptr_t key = stream_key(stream);
+        const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+        return cuda_status(launch_mtok(t, gemm_grid(dev.sms), pdl_enabled() && !after_weight_write, as_stream(stream)));
+    }
     StreamArgs a = {};
     Operand& o = a.op[kKindGU];
     o.quant_input = 1;
@@ -748,6 +879,16 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     if (!dev.ok) return MOEQ_ERR_DEVICE;
     const StreamWs wl = gemm_ws_layout(1, N / 128, K, max_pairs, max_uniq, dev.sms);
     if (!ws || !aligned16(ws) || ws_bytes < wl.end) return MOEQ_ERR_WORKSPACE;
+    if (down_mtok_ok(K, N, max_uniq, max_pairs)) {
+        const MtokGemmWs ml = mtok_gemm_ws(false, N, K, max_pairs, dev.sms, wl.end);
+        if (ws_bytes < ml.end) return MOEQ_ERR_WORKSPACE;
+        const MtokArgs t = mtok_gemm_args(false, a_in, a_dtype == MOEQ_F32, max_pairs, K, N, w_d, s_d, uniq, offs,
+                                          nullptr, n_uniq_dev, n_experts, max_uniq, max_pairs, y, q_a_opt, s_a_opt, ws,
+                                          ml);
+        uintptr_t key = stream_key(stream);
+        const bool after_weight_write = g_weight_write_stream.compare_exchange_strong(key, 0);
+        return cuda_status(launch_mtok(t, gemm_grid(dev.sms), pdl_enabled() && !after_weight_write, as_stream(stream)));
+    }
     StreamArgs a = {};
     Operand& o = a.op[kKindDN];
     o.quant_input = 1;
@@ -830,12 +971,32 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
     if (K <= 0 || N <= 0 || K % 128 || N % 128 || K > MOEQ_MAX_K) return MOEQ_ERR_UNSUPPORTED_SHAPE;
     const DeviceInfo dev = current_device();
     if (!dev.ok) return MOEQ_ERR_DEVICE;
+    void* ws = nullptr;
+    cudaStream_t cs = as_stream(stream);
+    if (down_mtok_ok(K, N, max_uniq, max_pairs)) {
+        // the path moeq_expert_gemm_down takes: the multi-token kernel, its
+        // areas right after the header, its counts zeroed on the stream first
+        const MtokGemmWs ml = mtok_gemm_ws(false, N, K, max_pairs, dev.sms, kHeader);
+        if (ml.end > kNoAllocScratchBytes) return MOEQ_ERR_WORKSPACE;   // beyond the static maximum
+        const moeq_status st = noalloc_scratch(&ws);
+        if (st != MOEQ_OK) return st;
+        if (cudaMemsetAsync(ws, 0, kHeader, cs) != cudaSuccess ||
+            cudaMemsetAsync(static_cast<char*>(ws) + ml.cnt, 0, ml.slots - ml.cnt, cs) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        const MtokArgs t = mtok_gemm_args(false, a_in, a_dtype == MOEQ_F32, max_pairs, K, N, w_d, s_d, uniq, offs,
+                                          nullptr, n_uniq_dev, n_experts, max_uniq, max_pairs, y, q_a_opt, s_a_opt, ws,
+                                          ml);
+        if (launch_mtok(t, gemm_grid(dev.sms), false, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
+        if (device_status_opt &&
+            cudaMemcpyAsync(device_status_opt, static_cast<char*>(ws) + kOffStatus, sizeof(int32_t),
+                            cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+            return MOEQ_ERR_CUDA;
+        return MOEQ_OK;
+    }
     const StreamWs wl = gemm_ws_layout(1, N / 128, K, max_pairs, max_uniq, dev.sms);
     if (wl.end > kNoAllocScratchBytes) return MOEQ_ERR_WORKSPACE;   // beyond the static maximum
-    void* ws = nullptr;
     const moeq_status st = noalloc_scratch(&ws);
     if (st != MOEQ_OK) return st;
-    cudaStream_t cs = as_stream(stream);
     // The counters (header: status word, epoch, input-quantisation count;
     // the split-K tickets) must be zero when a launch starts: zero them on
     // the stream first.  The activation buffers between them need no zeroing.
@@ -965,6 +1126,13 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
         t.xq = reinterpret_cast<uint8_t*>(base + l.mt_xq);
         t.xs = reinterpret_cast<float*>(base + l.mt_xs);
         t.part = reinterpret_cast<float*>(base + l.mt_part);
+        t.mode = kMtokLayer;
+        t.GS = t.KB;
+        t.NU = t.KB / 2;
+        t.KX = t.KB;
+        t.x_ld = H;
+        t.x_f32 = 0;
+        t.ntmax = M;
         return cuda_status(launch_mtok(t, dev.sms, pdl, as_stream(stream)));
     }
     TokenArgs t = {};

@@ -66,7 +66,6 @@ namespace moeq {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kWarps = kThreads / 32;
 constexpr int kProducerWarp = 0, kMmaWarp = 1, kEpiWarp0 = 2, kEpiWarps = 4, kQuantWarp0 = 6, kQuantWarps = 6;
 constexpr int kTicketWarp = 7, kSumWarp0 = 8, kSumWarps = 4;
 constexpr int kRouteThreads = kQuantWarp0 * 32;
@@ -102,6 +101,7 @@ struct PlanSmem {
 struct ColInfo {
     float sw[3][kMaxKB];   // gate and up weight scales per K group of x; down's per row block
     float rw[kN];          // routing weight of the token's pick of this expert (1: the shared one)
+    float xsc[kN];         // down mode: the activation scale of each row at the column's K group
     int pbase[kN];         // the token's partials of this column: offset in `part` of unit 0, row 0
     int pair[kN];          // the (token, expert) pair: row of h and of its dumps
     uint32_t tmask;        // tokens of the column
@@ -121,6 +121,7 @@ struct Smem {
     uint32_t tmem_base;
     int wdone[kEpiWarps];                       // down stages whose partials each epilogue warp has stored
     int abort_flag;
+    int last_cta;                               // this CTA is the last one out
 };
 
 constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Smem);
@@ -184,17 +185,45 @@ __device__ __forceinline__ uint8_t* slot_at(const MtokArgs& a, int b) {
 // ------------------------------------------------------------------ share
 // This CTA's share of the launch's stages: the head of column head_j (stages
 // [0, head_t1)), whole columns [j0, j1), the tail of column tail_j (stages
-// [tail_t0, spc)).  With no more columns than CTAs, one whole column each.
+// [tail_t0, tail_t1)).  With no more columns than CTAs, one whole column
+// each -- unless the stages are independent of one another (down alone:
+// every stage is its own partial), when the stages are dealt evenly over
+// the grid in every case and a CTA's range may lie inside one column (a
+// "tail" that ends before the column does).
 struct Share {
-    int head_j, head_t1, j0, j1, tail_j, tail_t0, np;
+    int head_j, head_t1, j0, j1, tail_j, tail_t0, tail_t1, np;
 };
 
-__device__ Share share_of(int ncols, int spc) {
+__device__ Share share_of(int ncols, int spc, bool independent) {
     const int G = gridDim.x, c = blockIdx.x;
     Share s;
     s.head_j = s.tail_j = -1;
     s.head_t1 = s.tail_t0 = 0;
-    if (ncols <= G) {
+    s.tail_t1 = spc;
+    if (independent && ncols <= G) {
+        const long long S = static_cast<long long>(ncols) * spc;
+        const long long lo = S * c / G, hi = S * (c + 1) / G;
+        const int jx = static_cast<int>(lo / spc), bx = static_cast<int>(lo - static_cast<long long>(jx) * spc);
+        const int jy = static_cast<int>(hi / spc), ey = static_cast<int>(hi - static_cast<long long>(jy) * spc);
+        s.j0 = s.j1 = 0;
+        if (jy == jx) {
+            // inside one column (or empty)
+            if (ey > bx) {
+                s.tail_j = jx;
+                s.tail_t0 = bx;
+                s.tail_t1 = ey;
+            }
+        } else {
+            // the range is no longer than a column here, so it spans at
+            // most two: the end of column jx, then the start of column jy
+            s.tail_j = jx;
+            s.tail_t0 = bx;
+            if (ey > 0) {
+                s.head_j = jy;
+                s.head_t1 = ey;
+            }
+        }
+    } else if (ncols <= G) {
         s.j0 = c < ncols ? c : 0;
         s.j1 = c < ncols ? c + 1 : 0;
     } else {
@@ -238,7 +267,7 @@ __device__ __forceinline__ void piece_at(const Share& s, int i, int spc, int& j,
     }
     j = s.tail_j;
     t0 = s.tail_t0;
-    t1 = spc;
+    t1 = s.tail_t1;
 }
 
 // ------------------------------------------------------------------ routing
@@ -247,6 +276,7 @@ __device__ __forceinline__ void piece_at(const Share& s, int i, int spc, int& j,
 struct RouteSync {
     __device__ void operator()() const { named_sync(2, kRouteThreads); }
 };
+template <int MODE>
 __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
     moeq_route_plan p;
     p.topk_id = sm.plan.topk_id;
@@ -256,6 +286,44 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
     p.offs = sm.plan.offs;
     p.pair_tok = sm.plan.pair_tok;
     p.pair_of = sm.plan.pair_of;
+    if (MODE != kMtokLayer) {
+        // the caller's plan (unique experts, their pair ranges, gate_up: each
+        // pair's token), checked as the persistent engine checks it: an
+        // expert out of range, a pair range that is empty, out of range or
+        // wider than one MMA's 16 rows, or (gate_up) a token out of range or
+        // twice on one expert leaves MOEQ_ERR_INVALID_ARG and no work
+        const int U0 = __ldcg(a.plan.n_uniq);
+        const int U = U0 >= 0 && U0 <= a.max_uniq ? U0 : 0;
+        const int cap = MODE == kMtokGateUp ? a.M : min(a.max_pairs, kN);
+        if (tid == 0) sm.rs.total[0] = U0 != U;
+        for (int i = tid; i < U; i += kRouteThreads) sm.plan.uniq[i] = __ldcg(a.plan.uniq + i);
+        for (int i = tid; i <= U; i += kRouteThreads) sm.plan.offs[i] = __ldcg(a.plan.offs + i);
+        named_sync(2, kRouteThreads);
+        for (int g = tid; g < U; g += kRouteThreads) {
+            const int e = sm.plan.uniq[g], r0 = sm.plan.offs[g], r1 = sm.plan.offs[g + 1];
+            bool ok = e >= 0 && e < a.n_experts && r0 >= 0 && r1 > r0 && r1 - r0 <= cap && r1 <= a.max_pairs;
+            if (MODE == kMtokGateUp && ok) {
+                uint32_t seen = 0;
+                for (int q = r0; q < r1; ++q) {
+                    const int n = __ldcg(a.plan.pair_tok + q);
+                    ok = ok && n >= 0 && n < a.M && !((seen >> n) & 1u);
+                    if (!ok) break;
+                    seen |= 1u << n;
+                    sm.plan.pair_tok[q] = n;
+                }
+            }
+            if (!ok) atomicOr(&sm.rs.total[0], 1);
+        }
+        named_sync(2, kRouteThreads);
+        if (tid == 0) {
+            const bool bad = sm.rs.total[0] != 0;
+            if (bad) record_error(a.status, MOEQ_ERR_INVALID_ARG);
+            sm.plan.n_uniq = bad ? 0 : U;
+            if (bad) sm.plan.offs[0] = 0;
+        }
+        named_sync(2, kRouteThreads);
+        return;
+    }
     if (a.top_k == 0) {
         // a dense FFN: no routing -- one expert (index E_routed) serving
         // every token, one pair per token
@@ -305,20 +373,42 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
 // which writes its codes into row n of K group t of the one copy in L2 (the
 // gate_up stages' B operand: token n in row n of an 8-row, 128-byte-swizzled
 // atom pair) and its scale beside it, then counts itself in K group t.
+// The position of pair row n inside its expert's rows (down mode: row n
+// goes to the MMA as row n - offs[g] of its expert's B operand, so its
+// 128-byte swizzle phase is that position mod 8).  The plan is checked by the
+// routing warps at the same time; a plan that fails that check gets no MMA,
+// so here U only has to stay within the plan's arrays.
+__device__ __forceinline__ int pos_in_expert(const MtokArgs& a, int n) {
+    const int U = min(max(__ldcg(a.plan.n_uniq), 0), a.max_uniq);
+    int lo = 0, hi = U;   // the last g with offs[g] <= n
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldcg(a.plan.offs + mid) <= n) lo = mid; else hi = mid;
+    }
+    return n - __ldcg(a.plan.offs + lo);
+}
+
+template <int MODE>
 __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
-    const int M = a.M, ngroups = M * a.KB;
+    const int M = a.M, ngroups = M * a.KX;
+    constexpr bool down = MODE == kMtokDown;
     for (int q = blockIdx.x * kQuantWarps + wq; q < ngroups; q += gridDim.x * kQuantWarps) {
         const int t = q / M, n = q - t * M;
-        const float4 v = load_act4<false>(a.x, static_cast<size_t>(a.H), n, t * 128 + 4 * lane);
+        const float4 v = a.x_f32 ? load_act4<true>(a.x, static_cast<size_t>(a.x_ld), n, t * 128 + 4 * lane)
+                                 : load_act4<false>(a.x, static_cast<size_t>(a.x_ld), n, t * 128 + 4 * lane);
         float sc;
         float4 dec;
         const uint32_t codes = quant_group_warp(v, &sc, &dec);
-        *reinterpret_cast<uint32_t*>(xq_group(a, t) + n * 128 + (((lane >> 2) ^ (n & 7)) << 4) + (lane & 3) * 4) =
-            codes;
-        if (lane == 0) a.xs[t * kN + n] = sc;
+        // layer and gate_up: token n in row n of K group t's 16 rows; down:
+        // K group t's rows are every pair row, each swizzled for its place
+        // in its expert's chunk of 16
+        const int ph = down ? (pos_in_expert(a, n) & 7) : (n & 7);
+        uint8_t* row = down ? a.xq + (static_cast<size_t>(t) * M + n) * 128 : xq_group(a, t) + n * 128;
+        *reinterpret_cast<uint32_t*>(row + (((lane >> 2) ^ ph) << 4) + (lane & 3) * 4) = codes;
+        if (lane == 0) a.xs[t * (down ? M : kN) + n] = sc;
         if (a.q_x) {
-            *reinterpret_cast<uint32_t*>(a.q_x + static_cast<size_t>(n) * a.H + t * 128 + 4 * lane) = codes;
-            if (lane == 0) a.s_x[n * a.KB + t] = sc;
+            *reinterpret_cast<uint32_t*>(a.q_x + static_cast<size_t>(n) * a.x_ld + t * 128 + 4 * lane) = codes;
+            if (lane == 0) a.s_x[n * a.KX + t] = sc;
         }
         fence_proxy_async();   // the codes are read by bulk copies (async proxy)
         __threadfence();       // ... and by other CTAs: released by the count below
@@ -327,15 +417,17 @@ __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
     }
 }
 
+
 // Warp 6, once the plan is known: lane l watches K groups l and l + 32,
 // each on its own (bounded) -- once a group's count shows all M tokens in,
 // the lane takes its scales into shared memory and releases it to the
 // producer and the epilogue.
+template <int MODE>
 __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
     constexpr int kPer = (kMaxKB + 31) / 32;
     bool done[kPer];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) done[i] = lane + 32 * i >= a.KB;
+    for (int i = 0; i < kPer; ++i) done[i] = lane + 32 * i >= a.KX;
     const unsigned long long t0 = global_timer_ns();
     for (;;) {
         bool all = true;
@@ -345,7 +437,8 @@ __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
             const int t = lane + 32 * i;
             if (ld_relaxed(a.cnt + kMtokX + kMtokPad * t) >= a.M && ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
                 fence_proxy_async();
-                for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
+                if (MODE != kMtokDown)   // (down: each column reads its rows' scales itself)
+                    for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
                 mbar_arrive(&sm.xq_bar[t]);
                 done[i] = true;
             } else {
@@ -386,18 +479,39 @@ __device__ __forceinline__ void col_of(int j, int U, int RB, int& g, int& kb) {
 // as that K group is released (at the start of the launch x may still be on
 // its way), so that x's quantisation overlaps the first tiles' latency.
 // Before the producer blocks on a free stage, every deferred x copy is out.
+template <int MODE>
 __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, const Share& sh, int spc) {
     const uint64_t pol = l2_evict_first_policy();
-    const uint32_t xbytes = static_cast<uint32_t>(a.M) * 128;
-    int pend_s[kStages], pend_t[kStages], npend = 0;
+    constexpr bool down = MODE == kMtokDown;
+    const uint32_t gu_xbytes = static_cast<uint32_t>(a.M) * 128;
+    // a stage's x copy: K group (its release barrier), and (down) source
+    // and size; gate_up's follow from the K group
+    int pend_s[kStages], pend_t[kStages];
+    const uint8_t* pend_src[down ? kStages : 1];
+    uint32_t pend_n[down ? kStages : 1];
+    int npend = 0;
     auto flush = [&]() -> bool {
         for (int q = 0; q < npend; ++q) {
             if (!wait_sleep(&sm.xq_bar[pend_t[q]], 0, sm, a.status)) return false;
-            bulk_load(stages + static_cast<size_t>(pend_s[q]) * kStageBytes + 2 * kTile, xq_group(a, pend_t[q]),
-                      xbytes, &sm.full[pend_s[q]], pol);
+            bulk_load(stages + static_cast<size_t>(pend_s[q]) * kStageBytes + 2 * kTile,
+                      down ? pend_src[q] : xq_group(a, pend_t[q]), down ? pend_n[q] : gu_xbytes, &sm.full[pend_s[q]],
+                      pol);
         }
         npend = 0;
         return true;
+    };
+    auto x_copy = [&](int s, int t, const uint8_t* src, uint32_t bytes) {
+        if (npend == 0 && mbar_try_wait(&sm.xq_bar[t], 0)) {
+            bulk_load(stages + static_cast<size_t>(s) * kStageBytes + 2 * kTile, src, bytes, &sm.full[s], pol);
+        } else {
+            pend_s[npend] = s;
+            pend_t[npend] = t;
+            if (down) {
+                pend_src[npend] = src;
+                pend_n[npend] = bytes;
+            }
+            ++npend;
+        }
     };
     long long it = 0;
     for (int i = 0; i < sh.np && !sm.abort_flag; ++i) {
@@ -405,6 +519,8 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
         piece_at(sh, i, spc, j, t0, t1);
         col_of(j, sm.plan.n_uniq, a.RB, g, kb);
         const int e = sm.plan.uniq[g];
+        // down mode: the column's pair rows of K group kb (B rows 0 .. n - 1)
+        const int r0 = sm.plan.offs[g], nr = min(sm.plan.offs[g + 1] - r0, kN);
         for (int t = t0; t < t1; ++t, ++it) {
             const int s = static_cast<int>(it % kStages);
             if (it >= kStages) {
@@ -413,22 +529,18 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
                     return it;
             }
             uint8_t* dst = stages + static_cast<size_t>(s) * kStageBytes;
-            if (t < a.KB) {
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + xbytes);
+            if (!down && t < a.GS) {
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + gu_xbytes);
                 bulk_load(dst, gu_tile(a, e, kb, t), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, gu_tile(a, e, a.RB + kb, t), kTile, &sm.full[s], pol);
-                if (npend == 0 && mbar_try_wait(&sm.xq_bar[t], 0)) {
-                    bulk_load(dst + 2 * kTile, xq_group(a, t), xbytes, &sm.full[s], pol);
-                } else {
-                    pend_s[npend] = s;
-                    pend_t[npend] = t;
-                    ++npend;
-                }
+                x_copy(s, t, xq_group(a, t), gu_xbytes);
             } else {
-                const int u = t - a.KB;
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                const int u = t - a.GS;
+                const uint32_t xbytes = down ? static_cast<uint32_t>(nr) * 128 : 0;
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + xbytes);
                 bulk_load(dst, dn_tile(a, e, 2 * u, kb), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, dn_tile(a, e, 2 * u + 1, kb), kTile, &sm.full[s], pol);
+                if (down) x_copy(s, kb, a.xq + (static_cast<size_t>(kb) * a.M + r0) * 128, xbytes);
             }
         }
     }
@@ -450,6 +562,7 @@ __device__ void producer_drain(Smem& sm, long long issued) {
 // One lane: per stage, 2 tiles x 4 K steps into accumulator set it % 4
 // (tile 0 at columns 32b .. 32b+15, tile 1 at 32b+16 ..).  gate_up's B is
 // the stage's x group; down's is h's codes, ready once h_ready completes.
+template <int MODE>
 __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stages, const Share& sh, int spc,
                                 int lane) {
     const uint32_t stage0 = smem_u32(stages), hb = smem_u32(sm.hbuf);
@@ -464,14 +577,14 @@ __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stag
             if (it >= kTmemBufs &&
                 !wait_spin(&sm.tmem_empty[b], static_cast<uint32_t>(((it / kTmemBufs) - 1) & 1), sm, a.status))
                 return last;
-            if (t == max(t0, a.KB)) {   // the piece's first down stage: its h codes
+            if (MODE == kMtokLayer && t == max(t0, a.GS)) {   // the piece's first down stage: its h codes
                 if (!wait_spin(&sm.h_ready, static_cast<uint32_t>(hcount & 1), sm, a.status)) return last;
                 ++hcount;
             }
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t sa = stage0 + static_cast<uint32_t>(s * kStageBytes);
-                const uint32_t bb = t < a.KB ? sa + 2 * kTile : hb;
+                const uint32_t bb = (MODE == kMtokDown || t < a.GS) ? sa + 2 * kTile : hb;
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const uint32_t d = sm.tmem_base + static_cast<uint32_t>((b * 2 + tt) * kN);
@@ -491,6 +604,7 @@ __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stag
 
 // ------------------------------------------------------------------ epilogue
 // Column info of piece i (scales, and per token: membership, pick, pair).
+template <int MODE>
 __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, int i, int etid) {
     ColInfo& ci = sm.col[i & 1];
     int j, t0, t1;
@@ -501,6 +615,8 @@ __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
     const int KB = a.KB, NBg = 2 * a.RB;
     for (int q = etid; q < 3 * KB; q += kEpiThreads) {
         const int which = q / KB, t = q - which * KB;
+        if (which < 2 && MODE == kMtokDown) continue;     // no gate_up
+        if (which == 2 && MODE == kMtokGateUp) continue;  // no down
         float v;
         if (which < 2)
             v = __ldg(a.s_gu + (static_cast<size_t>(e) * NBg + which * a.RB + kb) * KB + t);
@@ -509,14 +625,22 @@ __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
         ci.sw[which][t] = v;
     }
     if (etid < 32) {
-        const int n = etid, k = a.top_k, U = sm.plan.n_uniq, nu = KB / 2;
+        const int n = etid, k = a.top_k, U = sm.plan.n_uniq, nu = a.NU;
         int pair = -1, slot = 0;
-        float w = 0.0f;
-        if (n < a.M) {
+        float w = 0.0f, xsc = 0.0f;
+        if (MODE == kMtokDown) {
+            // row n of the column: the chunk's pair row offs[g] + n
+            wait_sleep(&sm.xq_bar[kb], 0, sm, a.status);   // the rows' scales of K group kb
+            if (n < min(sm.plan.offs[g + 1] - sm.plan.offs[g], kN)) {
+                pair = sm.plan.offs[g] + n;
+                w = 1.0f;
+                xsc = __ldcg(a.xs + static_cast<size_t>(kb) * a.M + pair);
+            }
+        } else if (n < a.M) {
             for (int p = sm.plan.offs[g]; p < sm.plan.offs[g + 1]; ++p)
                 if (sm.plan.pair_tok[p] == n) pair = p;
             if (pair >= 0) {
-                if (g == U - 1) {
+                if (MODE == kMtokGateUp || g == U - 1) {
                     slot = k;
                     w = 1.0f;
                 } else {
@@ -530,9 +654,11 @@ __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
         }
         const uint32_t m = __ballot_sync(0xffffffffu, pair >= 0);
         if (n < kN) {
-            // partials: [token][unit][slot][kb][256 rows]
+            // partials: [row][unit][slot][kb][256 rows] (row: token, or down's pair row)
+            const int row = MODE == kMtokDown ? (pair >= 0 ? pair : 0) : n;
             ci.rw[n] = w;
-            ci.pbase[n] = ((n * nu * (k + 1) + slot) * a.RB + kb) * 256;
+            ci.xsc[n] = xsc;
+            ci.pbase[n] = ((row * nu * (k + 1) + slot) * a.RB + kb) * 256;
             ci.pair[n] = pair;
         }
         if (n == 0) {
@@ -568,19 +694,20 @@ __device__ __forceinline__ bool epi_take(const MtokArgs& a, Smem& sm, long long 
     return ok;
 }
 
-template <int NT>
+template <int NT, int MODE>
 __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, int warp, int lane) {
     const int etid = (warp - kEpiWarp0) * 32 + lane, quad = warp & 3;
     const int r = quad * 32 + lane;                       // the TMEM lane: row of the tiles
     const uint32_t tlane = sm.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    const int KB = a.KB, k = a.top_k, c = blockIdx.x;
+    const int GS = a.GS, k = a.top_k, c = blockIdx.x;
+    constexpr bool layer = MODE == kMtokLayer, down_only = MODE == kMtokDown;
     const int ustride = (k + 1) * a.RB * 256;   // partials of one output unit, per token
     long long it = 0;
     int stored = 0;
-    if (sh.np > 0) load_col(a, sm, sh, spc, 0, etid);
+    if (sh.np > 0) load_col<MODE>(a, sm, sh, spc, 0, etid);
     for (int i = 0; i < sh.np; ++i) {
         epi_sync();   // piece i's column info is loaded; the previous piece's is no longer read
-        if (i + 1 < sh.np) load_col(a, sm, sh, spc, i + 1, etid);
+        if (i + 1 < sh.np) load_col<MODE>(a, sm, sh, spc, i + 1, etid);
         const ColInfo& ci = sm.col[i & 1];
         const int t0 = ci.t0, t1 = ci.t1, kb = ci.kb;
         const uint32_t tmask = ci.tmask;
@@ -588,8 +715,8 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
 #pragma unroll
         for (int n = 0; n < NT; ++n) accg[n] = accu[n] = 0.0f;
 
-        // gate_up: stages [t0, min(t1, KB))
-        for (int t = t0; t < min(t1, KB); ++t, ++it) {
+        // gate_up: stages [t0, min(t1, GS))
+        for (int t = t0; t < min(t1, GS); ++t, ++it) {
             uint32_t rg[NT], ru[NT];
             epi_take<NT>(a, sm, it, tlane, rg, ru, lane);
             wait_sleep(&sm.xq_bar[t], 0, sm, a.status);   // x's scales of group t (returns at once after the first)
@@ -607,7 +734,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             }
         }
 
-        if (t0 == 0 && t1 <= KB) {
+        if (!down_only && t0 == 0 && t1 <= GS && t1 < spc) {
             // the head of a column split inside gate_up: publish the sums so far
             float* gu = reinterpret_cast<float*>(slot_at(a, c + 1));
 #pragma unroll
@@ -620,7 +747,9 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             if (etid == 0) st_release(a.cnt + kMtokFlags + c + 1, 1);
             continue;
         }
-        if (t0 <= KB) {
+        if (down_only) {
+            // down alone: the rows' codes come with every stage
+        } else if (t0 <= GS) {
             if (t0 > 0) {
                 // the tail of a column split inside gate_up: head's sums + this CTA's
                 if (etid == 0) wait_flag(a.cnt + kMtokFlags + c, sm, a.status);
@@ -647,6 +776,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
                 }
                 m[n] = fabsf(h[n]);
             }
+            if (!layer) continue;   // gate_up alone: h is the result
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
@@ -703,20 +833,21 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             fence_proxy_async_smem();
             epi_sync();
         }
-        if (etid == 0) mbar_arrive(&sm.h_ready);
+        if (layer && etid == 0) mbar_arrive(&sm.h_ready);
 
-        // down: stages [max(t0, KB), t1), unit u = t - KB; partials scaled by
-        // the token's h scale, routing weight and the block's weight scale
-        for (int t = max(t0, KB); t < t1; ++t, ++it) {
+        // down: stages [max(t0, GS), t1), unit u = t - GS; partials scaled by
+        // the row's activation scale (h's, or down alone: a's), its routing
+        // weight and the block's weight scale
+        for (int t = max(t0, GS); t < t1; ++t, ++it) {
             uint32_t d0[NT], d1[NT];
             epi_take<NT>(a, sm, it, tlane, d0, d1, lane);
-            const int u = t - KB;
+            const int u = t - GS;
             const float s0 = ci.sw[2][2 * u], s1 = ci.sw[2][2 * u + 1];
             float* pu = a.part + static_cast<size_t>(u) * ustride + r;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 if ((tmask >> n) & 1u) {
-                    const float hwn = sm.hw[n];
+                    const float hwn = down_only ? ci.xsc[n] : sm.hw[n];
                     float* p = pu + ci.pbase[n];
                     p[0] = __uint_as_float(d0[n]) * (hwn * s0);
                     p[128] = __uint_as_float(d1[n]) * (hwn * s1);
@@ -740,7 +871,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
 // its columns in order, a fixed butterfly adds the classes, lanes 0..3 round
 // to bf16.
 __device__ void combine_part(const MtokArgs& a, int n, int u, int w, int lane) {
-    const int nu = a.KB / 2, ncol = (a.top_k + 1) * a.RB;
+    const int nu = a.NU, ncol = (a.top_k + 1) * a.RB;
     const float* base = a.part + (static_cast<size_t>(n) * nu + u) * ncol * 256 + 16 * w;
     const int n4 = ncol * 4;
     constexpr int kBatch = 12;
@@ -789,7 +920,7 @@ __device__ int unit_of_down_stage(const Share& sh, int spc, int KB, int q) {
         int j, t0, t1;
         piece_at(sh, i, spc, j, t0, t1);
         const int d0 = max(t0, KB), nd = max(0, t1 - d0);
-        if (q < nd) return d0 - KB + q;
+        if (q < nd) return d0 - KB + q;   // KB: gate_up stages per column
         q -= nd;
     }
     return 0;
@@ -800,12 +931,12 @@ __device__ int unit_of_down_stage(const Share& sh, int spc, int KB, int q) {
 // stored so far, then one fire-and-forget add per (column, unit) arrival.
 // A unit is complete once its count reaches ncols.
 __device__ void ticket_warp(const MtokArgs& a, Smem& sm, const Share& sh, int spc, int lane) {
-    const int KB = a.KB;
+    const int GS = a.GS;
     int total = 0;
     for (int i = 0; i < sh.np; ++i) {
         int j, t0, t1;
         piece_at(sh, i, spc, j, t0, t1);
-        total += max(0, t1 - max(t0, KB));
+        total += max(0, t1 - max(t0, GS));
     }
     int done = 0;
     unsigned long long t0 = global_timer_ns();
@@ -822,7 +953,7 @@ __device__ void ticket_warp(const MtokArgs& a, Smem& sm, const Share& sh, int sp
         }
         t0 = global_timer_ns();
         __threadfence();   // releases the partials stored by every epilogue warp so far
-        for (int q = done + lane; q < avail; q += 32) atomicAdd(a.cnt + kMtokU + kMtokPad * unit_of_down_stage(sh, spc, KB, q), 1);
+        for (int q = done + lane; q < avail; q += 32) atomicAdd(a.cnt + kMtokU + kMtokPad * unit_of_down_stage(sh, spc, GS, q), 1);
         done = avail;
     }
 }
@@ -830,8 +961,12 @@ __device__ void ticket_warp(const MtokArgs& a, Smem& sm, const Share& sh, int sp
 // Warps 8-11: the sums, in unit order (task p: unit p / (16M), then token,
 // then 16-row part), each once its unit's count shows all ncols columns in
 // (bounded wait).
+template <int MODE>
 __device__ void sum_worker(const MtokArgs& a, Smem& sm, int ncols, int wi, int lane) {
-    const int nu = a.KB / 2, per_unit = a.M * kParts, ntask = nu * per_unit;
+    // the rows summed: the tokens, or (down alone) the plan's pair rows
+    const int row0 = MODE == kMtokDown ? sm.plan.offs[0] : 0;
+    const int rows = MODE == kMtokDown ? sm.plan.offs[sm.plan.n_uniq] - row0 : a.M;
+    const int nu = a.NU, per_unit = rows * kParts, ntask = nu * per_unit;
     for (int p = blockIdx.x * kSumWarps + wi; p < ntask; p += gridDim.x * kSumWarps) {
         const int u = p / per_unit, rem = p - u * per_unit;
         int ok = 0;
@@ -856,10 +991,11 @@ __device__ void sum_worker(const MtokArgs& a, Smem& sm, int ncols, int wi, int l
             }
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-        combine_part(a, rem / kParts, u, rem % kParts, lane);
+        combine_part(a, row0 + rem / kParts, u, rem % kParts, lane);
     }
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant__ MtokArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -895,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         // the logits and x are the previous kernel's to write until
         // griddepcontrol.wait; their lines can still be brought into L2 now
         // (L2 is where every SM's writes meet), so the reads after the wait hit
-        const int lg_lines = (a.M * a.E_routed * 4 + 127) / 128, x_lines = (a.M * a.H * 2 + 127) / 128;
+        const int lg_lines = (a.M * a.E_routed * 4 + 127) / 128, x_lines = (a.M * a.x_ld * (a.x_f32 ? 4 : 2) + 127) / 128;
         for (int i = lane; i < lg_lines + x_lines; i += 32)
             prefetch_l2(i < lg_lines ? reinterpret_cast<const char*>(a.logits) + 128 * i
                                      : reinterpret_cast<const char*>(a.x) + 128 * (i - lg_lines));
@@ -921,27 +1057,27 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     const bool early = a.route_early != 0;
     if (warp < kQuantWarp0) {
         if (!early) pdl_wait();
-        route_all(a, sm, tid);                 // the plan in every CTA's shared memory (warps 0-5)
+        route_all<MODE>(a, sm, tid);           // the plan in every CTA's shared memory (warps 0-5)
         named_arrive(3, kThreads - 32);        // ... and for warps 7-11
     } else {
         pdl_wait();
-        quantise_x(a, warp - kQuantWarp0, lane);
+        quantise_x<MODE>(a, warp - kQuantWarp0, lane);
         if (warp != kQuantWarp0) named_sync(3, kThreads - 32);
     }
     if (warp == kQuantWarp0) {
         // warp 6 goes on at once to release x's K groups as the grid's
         // quantisation completes (it needs no plan)
-        x_ready(a, sm, lane);
+        x_ready<MODE>(a, sm, lane);
     } else {
-        const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.KB + a.KB / 2;
-        const Share sh = share_of(ncols, spc);
+        const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.GS + a.NU;
+        const Share sh = share_of(ncols, spc, MODE == kMtokDown);
         if (warp == kProducerWarp) {
             if (lane == 0) {
-                const long long issued = producer(a, sm, stages, sh, spc);
+                const long long issued = producer<MODE>(a, sm, stages, sh, spc);
                 if (sm.abort_flag) producer_drain(sm, issued);
             }
         } else if (warp == kMmaWarp) {
-            const long long last = mma_issuer(a, sm, stages, sh, spc, lane);
+            const long long last = mma_issuer<MODE>(a, sm, stages, sh, spc, lane);
             if (last >= 0) {
                 // every MMA issued has completed before TMEM is freed (bounded)
                 const unsigned long long t0 = global_timer_ns();
@@ -954,16 +1090,16 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
             }
         } else if (warp < kEpiWarp0 + kEpiWarps) {
             if (early) pdl_wait();
-            if (a.M <= 4)
-                epilogue<4>(a, sm, sh, spc, warp, lane);
-            else if (a.M <= 8)
-                epilogue<8>(a, sm, sh, spc, warp, lane);
+            if (a.ntmax <= 4)
+                epilogue<4, MODE>(a, sm, sh, spc, warp, lane);
+            else if (a.ntmax <= 8)
+                epilogue<8, MODE>(a, sm, sh, spc, warp, lane);
             else
-                epilogue<16>(a, sm, sh, spc, warp, lane);
+                epilogue<16, MODE>(a, sm, sh, spc, warp, lane);
         } else if (warp == kTicketWarp) {
             ticket_warp(a, sm, sh, spc, lane);
         } else {
-            sum_worker(a, sm, ncols, warp - kSumWarp0, lane);
+            sum_worker<MODE>(a, sm, ncols, warp - kSumWarp0, lane);
         }
     }
 
@@ -972,16 +1108,22 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(sm.tmem_base, kTmemCols);
     // the last CTA out (every other CTA's counting and summing done) clears
-    // the counts and flags for the next launch
+    // the counts and flags for the next launch, with all its threads (the
+    // next kernel's griddepcontrol.wait waits for this)
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(a.cnt + kMtokFin, 1) == G - 1) {
-            __threadfence();
-            a.cnt[kMtokFin] = 0;
-            for (int t = 0; t < a.KB; ++t) a.cnt[kMtokX + kMtokPad * t] = 0;
-            for (int u = 0; u < a.KB / 2; ++u) a.cnt[kMtokU + kMtokPad * u] = 0;
-            for (int b = 0; b <= G; ++b) a.cnt[kMtokFlags + b] = 0;
+        sm.last_cta = atomicAdd(a.cnt + kMtokFin, 1) == G - 1;
+    }
+    __syncthreads();
+    if (sm.last_cta) {
+        __threadfence();
+        const int n_x = a.KX, n_u = a.NU, n = n_x + n_u + G + 1;
+        for (int i = tid; i < n; i += kThreads) {
+            const int o = i < n_x ? kMtokX + kMtokPad * i
+                                  : (i < n_x + n_u ? kMtokU + kMtokPad * (i - n_x) : kMtokFlags + (i - n_x - n_u));
+            a.cnt[o] = 0;
         }
+        if (tid == 0) a.cnt[kMtokFin] = 0;
     }
 }
 
@@ -989,14 +1131,20 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
 
 size_t mtok_smem_bytes() { return kSmemBytes; }
 
+// One instantiation per mode: the layer path carries none of the
+// standalone modes' branches.
 cudaError_t launch_mtok(const MtokArgs& args, int grid, bool pdl, cudaStream_t stream) {
+    if (args.mode < kMtokLayer || args.mode > kMtokDown) return cudaErrorInvalidValue;
+    void (*const kernels[3])(MtokArgs) = {mtok_kernel<kMtokLayer>, mtok_kernel<kMtokGateUp>, mtok_kernel<kMtokDown>};
     static int configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(mtok_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
+        for (auto k : kernels) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+            if (e != cudaSuccess) return e;
+        }
         configured[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1009,7 +1157,7 @@ cudaError_t launch_mtok(const MtokArgs& args, int grid, bool pdl, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mtok_kernel, args);
+    return cudaLaunchKernelEx(&cfg, kernels[args.mode], args);
 }
 
 }  // namespace moeq

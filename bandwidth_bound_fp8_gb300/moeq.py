@@ -39,7 +39,7 @@ EXPORTS = [
     "moeq_expert_gemm_down", "moeq_combine", "moeq_moe_layer", "moeq_expert_gemm_down_noalloc",
     "moeq_dense_ffn_workspace_size", "moeq_dense_ffn", "moeq_stack_workspace_size", "moeq_moe_stack",
     "moeq_stack_plan", "moeq_stack_release_graphs", "moeq_tp_shard_weights", "moeq_moe_layer_shard",
-    "moeq_tp_reduce", "moeq_layer_ws_count_offset",
+    "moeq_tp_reduce", "moeq_layer_ws_count_offset", "moeq_gemm_ws_count_offset",
 ]
 
 
@@ -98,6 +98,7 @@ def load(path: str = LIB_PATH):
                                       ctypes.POINTER(moeq_route_plan), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
         "moeq_tp_reduce": (_i, [_vp, _i, _i, _i, _vp, _vp]),
         "moeq_layer_ws_count_offset": (_sz, [_i, _i, _i, _i, _i, _i]),
+        "moeq_gemm_ws_count_offset": (_sz, [_i, _i, _i, _i, _i, _i]),
         "moeq_moe_stack": (_i, [_i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp]),
         "moeq_stack_plan": (_i, [_vp, _sz, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(moeq_route_plan)]),
         "moeq_stack_release_graphs": (_i, []),
@@ -369,3 +370,7 @@ def moeq_tp_reduce(partials, out, stream=None) -> None:
 
 def moeq_layer_ws_count_offset(M, H, I, n_experts_incl_shared, top_k, which) -> int:
     return int(load().moeq_layer_ws_count_offset(M, H, I, n_experts_incl_shared, top_k, which))
+
+
+def moeq_gemm_ws_count_offset(rows_out, K, rows_in, max_uniq, is_gate_up, which) -> int:
+    return int(load().moeq_gemm_ws_count_offset(rows_out, K, rows_in, max_uniq, is_gate_up, which))

@@ -8,6 +8,8 @@ several 128-blocks in N and K with ragged group counts, experts with 1, 2,
 3 and 5+ tokens (every accumulation mode), split-K with many contributors
 per row block (few units per CTA) and CTAs spanning several row blocks.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -58,8 +60,12 @@ def oracle_down(orc, a_np, ex, uniq, offs):
     (640, 384, [3, 0, 4], [0, 1, 3, 8]),          # 1, 2, 5 tokens
     (256, 128, [1], [0, 3]),                       # 3 tokens, tiny: T < grid
     (1280, 512, [2, 5, 0, 1, 3, 4], [0, 1, 2, 3, 4, 5, 21]),   # 16 tokens on one expert
+    (768, 512, [2, 0, 1], [0, 5, 21, 28]),         # 16 rows on one expert from pair row 5
 ])
 def test_down_small(orc, dtype, K, N, uniq, offs):
+    # N a multiple of 256 runs the multi-token kernel's down mode (each
+    # expert's rows one MMA's B operand, their codes swizzled for their place
+    # in it); other N the persistent engine
     E = max(uniq) + 1
     ex = Experts(E, N, K, base_seed=11 + K + N, which=1)
     P = offs[-1]
@@ -133,6 +139,7 @@ def check_h(h, g, u, Tg, Tu, h_ref):
     (640, 384, [3, 0, 4, 5], [0, 1, 3, 6, 11], [2, 0, 1, 0, 1, 2, 0, 1, 2, 3, 4], 5),
     (256, 128, [0], [0, 1], [0], 1),
     (1152, 256, [1, 0], [0, 2, 18], [3, 9] + list(range(16)), 16),
+    (512, 10240, [1, 0], [0, 3, 7], [0, 1, 2, 0, 1, 2, 3], 4),   # 160 columns: split between CTAs
 ])
 def test_gateup_small(orc, dtype, H, I, uniq, offs, pair_tok, M):
     E = max(uniq) + 1
@@ -190,3 +197,59 @@ def test_gemm_deterministic(orc):
     h1, _, _ = run_gateup(x, ex, *args)
     h2, _, _ = run_gateup(x, ex, *args)
     assert np.array_equal(h1.view(np.uint32), h2.view(np.uint32))
+
+
+def _status_after(call):
+    from bandwidth_bound_fp8_gb300 import moeq
+    ws = call()
+    torch.cuda.synchronize()
+    return moeq.moeq_read_device_status(ws.t, ws.nbytes)
+
+
+@pytest.mark.skipif(os.environ.get("MOEQ_MTOK_KERNEL") == "0", reason="the multi-token kernel's own plan check")
+@pytest.mark.parametrize("defect", ["expert", "rows", "order", "n_uniq"])
+def test_down_plan_check(defect):
+    """A plan that breaks the down call's contract leaves MOEQ_ERR_INVALID_ARG
+    in the workspace status: an expert out of range, more than 16 rows on
+    one expert, pair ranges out of order, n_uniq above max_uniq."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    K, N = 256, 256
+    ex = Experts(2, N, K, base_seed=5, which=1)
+    uniq, offs, n = {"expert": ([0, 2], [0, 1, 2], 2), "rows": ([1], [0, 17], 1),
+                     "order": ([0, 1], [0, 3, 2], 2), "n_uniq": ([0, 1], [0, 1, 2], 3)}[defect]
+    P = max(offs)
+    a = synth.activations_bf16(P, K, 3, 0, 1.0, device="cuda")
+    du, do, _, _ = device_plan(uniq, offs, [0])
+    dn = torch.tensor([n], dtype=torch.int32, device="cuda")
+    y = torch.zeros((P, N), device="cuda")
+
+    def call():
+        ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, P, len(uniq), 0))
+        moeq.moeq_expert_gemm_down(a, K, N, ex.q, ex.s, ex.E, du, do, dn, len(uniq), P, y, ws)
+        return ws
+    assert _status_after(call) == moeq.MOEQ_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(os.environ.get("MOEQ_MTOK_KERNEL") == "0", reason="the multi-token kernel's own plan check")
+@pytest.mark.parametrize("defect", ["expert", "token", "twice", "n_uniq"])
+def test_gateup_plan_check(defect):
+    """As test_down_plan_check for the gate_up call: an expert out of range,
+    a token out of range, a token twice on one expert, n_uniq above
+    max_uniq."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    H, I, M = 256, 256, 3
+    ex = Experts(2, 2 * I, H, base_seed=7, which=0)
+    uniq, offs, pair_tok, n = {"expert": ([5, 0], [0, 1, 4], [0, 0, 1, 2], 2),
+                               "token": ([1, 0], [0, 1, 4], [3, 0, 1, 2], 2),
+                               "twice": ([1, 0], [0, 2, 5], [1, 1, 0, 1, 2], 2),
+                               "n_uniq": ([1, 0], [0, 1, 4], [0, 0, 1, 2], 3)}[defect]
+    x = synth.activations_bf16(M, H, 9, 0, 1.0, device="cuda")
+    du, do, dp, _ = device_plan(uniq, offs, pair_tok)
+    dn = torch.tensor([n], dtype=torch.int32, device="cuda")
+    h = torch.zeros((offs[-1], I), device="cuda")
+
+    def call():
+        ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(I, H, M, len(uniq), 1))
+        moeq.moeq_expert_gemm_gateup_swiglu(x, H, I, ex.q, ex.s, ex.E, du, do, dp, dn, len(uniq), offs[-1], h, ws)
+        return ws
+    assert _status_after(call) == moeq.MOEQ_ERR_INVALID_ARG

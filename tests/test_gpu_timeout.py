@@ -5,7 +5,8 @@ the kernel draining its copies and returning, so the context stays usable.
 The test makes one wait run out on purpose: the input-quantisation counter
 in the workspace header (byte offset 16) is set far below anything the
 launch can reach, so the chunk-preparing warps of every CTA give up after
-the limit.  It then checks the status, re-initialises the workspace and
+the limit (a down call whose N is not a multiple of 256, which the
+persistent engine serves).  It then checks the status, re-initialises the workspace and
 checks that a normal call on the same context still matches the oracle.
 A second case does the same to the count that the persistent engine's
 one-token layer waits for before its final combine (the engine serves one
@@ -21,7 +22,7 @@ import torch
 
 import synth
 from moeq_testlib import STRICT, Experts, assert_close, device_plan, to_np
-from test_gpu_gemm import oracle_down
+from test_gpu_gemm import check_h, oracle_down, oracle_gateup
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +32,7 @@ A_CNT_INT_OFFSET = 16 // 4   # int32 index of the input-quantisation counter
 @pytest.mark.parametrize("M", [1, 8])
 def test_bounded_wait_reports_timeout_and_the_context_survives(orc, M):
     from bandwidth_bound_fp8_gb300 import moeq
-    K, N = 256, 256
+    K, N = 256, 128
     ex = Experts(1, N, K, base_seed=71, which=1)
     a = synth.activations_bf16(M, K, 73, 2, 20.0, device="cuda")
     du, do, _, dn = device_plan([0], [0, M], [0])
@@ -119,3 +120,46 @@ def test_layer_kernel_wait_reports_timeout_and_the_context_survives(orc, M, whic
     assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))   # the re-initialised one, same bits
 
+
+
+@pytest.mark.parametrize("gate_up,which", [(0, 0), (0, 1), (1, 0)])
+def test_gemm_kernel_wait_reports_timeout_and_the_context_survives(orc, gate_up, which):
+    """The standalone GEMM calls on the multi-token kernel: the count of
+    the input's K group 0, or (down) of output unit 0, set out of reach in
+    the call's workspace.  The wait gives up, the status says
+    MOEQ_ERR_TIMEOUT, and after a re-initialisation the call on the same
+    context matches the oracle."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    K, rows_out, M = 256, 256 if not gate_up else 128, 3
+    off = moeq.moeq_gemm_ws_count_offset(rows_out, K, M, 1, gate_up, which)
+    if off == 0:
+        pytest.skip("the multi-token kernel does not serve this call here")
+    ws = moeq.Workspace(moeq.moeq_gemm_workspace_size(rows_out, K, M, 1, gate_up))
+    assert off % 4 == 0 and off < ws.nbytes
+    a = synth.activations_bf16(M, K, 75 + which, 2, 20.0, device="cuda")
+    if gate_up:
+        ex = Experts(1, 2 * rows_out, K, base_seed=77, which=0)
+        du, do, dp, dn = device_plan([0], [0, M], list(range(M)))
+        out = torch.zeros((M, rows_out), device="cuda")
+        call = lambda: moeq.moeq_expert_gemm_gateup_swiglu(a, K, rows_out, ex.q, ex.s, 1, du, do, dp, dn, 1, M, out, ws)
+    else:
+        ex = Experts(1, rows_out, K, base_seed=79, which=1)
+        du, do, _, dn = device_plan([0], [0, M], [0])
+        out = torch.zeros((M, rows_out), device="cuda")
+        call = lambda: moeq.moeq_expert_gemm_down(a, K, rows_out, ex.q, ex.s, 1, du, do, dn, 1, M, out, ws)
+    ws.t.view(torch.int32)[off // 4] = -(1 << 30)
+    call()
+    torch.cuda.synchronize()   # returns: the kernel gave up instead of hanging
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == moeq.MOEQ_ERR_TIMEOUT
+    moeq.moeq_workspace_init(ws.t, ws.nbytes)
+    out.fill_(float("nan"))
+    call()
+    torch.cuda.synchronize()
+    assert moeq.moeq_read_device_status(ws.t, ws.nbytes) == 0
+    a_np = to_np(a.contiguous().view(torch.uint16))
+    if gate_up:
+        g, u, Tg, Tu, h_ref, _, _ = oracle_gateup(orc, a_np, ex, [0], [0, M], list(range(M)), rows_out)
+        check_h(to_np(out), g, u, Tg, Tu, h_ref)
+    else:
+        y_ref, T, _, _ = oracle_down(orc, a_np, ex, [0], [0, M])
+        assert_close(to_np(out), y_ref, T, STRICT, what="after a timeout")
