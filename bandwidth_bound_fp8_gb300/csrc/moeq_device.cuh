@@ -236,6 +236,13 @@ __device__ __forceinline__ int ld_relaxed(const int* p) {
 
 // Orders generic-proxy memory accesses with async-proxy (bulk copy) ones.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async;" ::: "memory"); }
+// The same, for global memory only: generic writes (or reads acquired) in
+// global memory ordered against bulk copies that read it.  The unqualified
+// fence also covers shared memory, where this CTA's own bulk copies may be
+// landing, and costs more while they are in flight.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Named barrier over the consumer warps only (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int nthreads) {

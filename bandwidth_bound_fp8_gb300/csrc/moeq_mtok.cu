@@ -185,24 +185,32 @@ __device__ __forceinline__ uint8_t* slot_at(const MtokArgs& a, int b) {
 // ------------------------------------------------------------------ share
 // This CTA's share of the launch's stages: the head of column head_j (stages
 // [0, head_t1)), whole columns [j0, j1), the tail of column tail_j (stages
-// [tail_t0, tail_t1)).  With no more columns than CTAs, one whole column
-// each -- unless the stages are independent of one another (down alone:
-// every stage is its own partial), when the stages are dealt evenly over
-// the grid in every case and a CTA's range may lie inside one column (a
-// "tail" that ends before the column does).
+// [tail_t0, tail_t1)).  With more columns than CTAs the stages are dealt
+// evenly (a range then holds at most one head and one tail).  With no more
+// columns than CTAs it depends on the launch:
+//   kShareColumns (the layer): one whole column per CTA;
+//   kShareChain (gate_up alone): the stages dealt evenly over min(G, 2 ncols)
+//     CTAs, so that a range is at least half a column and a column spans at
+//     most three CTAs -- a range may lie inside one column (a "tail" that
+//     ends before the column does: a middle piece, which takes the sums of
+//     the CTA before and hands them on to the CTA after);
+//   kShareFree (down alone, every stage its own partial): dealt evenly over
+//     the whole grid.
+constexpr int kShareColumns = 0, kShareChain = 1, kShareFree = 2;
 struct Share {
     int head_j, head_t1, j0, j1, tail_j, tail_t0, tail_t1, np;
 };
 
-__device__ Share share_of(int ncols, int spc, bool independent) {
+__device__ Share share_of(int ncols, int spc, int kind) {
     const int G = gridDim.x, c = blockIdx.x;
     Share s;
     s.head_j = s.tail_j = -1;
     s.head_t1 = s.tail_t0 = 0;
     s.tail_t1 = spc;
-    if (independent && ncols <= G) {
+    if (kind != kShareColumns && ncols <= G) {
+        const int Gs = kind == kShareChain ? min(G, 2 * ncols) : G;
         const long long S = static_cast<long long>(ncols) * spc;
-        const long long lo = S * c / G, hi = S * (c + 1) / G;
+        const long long lo = S * min(c, Gs) / Gs, hi = S * min(c + 1, Gs) / Gs;
         const int jx = static_cast<int>(lo / spc), bx = static_cast<int>(lo - static_cast<long long>(jx) * spc);
         const int jy = static_cast<int>(hi / spc), ey = static_cast<int>(hi - static_cast<long long>(jy) * spc);
         s.j0 = s.j1 = 0;
@@ -410,7 +418,7 @@ __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
             *reinterpret_cast<uint32_t*>(a.q_x + static_cast<size_t>(n) * a.x_ld + t * 128 + 4 * lane) = codes;
             if (lane == 0) a.s_x[n * a.KX + t] = sc;
         }
-        fence_proxy_async();   // the codes are read by bulk copies (async proxy)
+        fence_proxy_async_global();   // the codes are read by bulk copies (async proxy)
         __threadfence();       // ... and by other CTAs: released by the count below
         __syncwarp();
         if (lane == 0) atomicAdd(a.cnt + kMtokX + kMtokPad * t, 1);
@@ -436,7 +444,7 @@ __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
             if (done[i]) continue;
             const int t = lane + 32 * i;
             if (ld_relaxed(a.cnt + kMtokX + kMtokPad * t) >= a.M && ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
-                fence_proxy_async();
+                fence_proxy_async_global();
                 if (MODE != kMtokDown)   // (down: each column reads its rows' scales itself)
                     for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
                 mbar_arrive(&sm.xq_bar[t]);
@@ -734,8 +742,21 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             }
         }
 
-        if (!down_only && t0 == 0 && t1 <= GS && t1 < spc) {
-            // the head of a column split inside gate_up: publish the sums so far
+        if (!down_only && t0 > 0 && t0 <= GS) {
+            // the tail (or a middle piece) of a column split inside gate_up:
+            // the sums of the CTA before + this CTA's
+            if (etid == 0) wait_flag(a.cnt + kMtokFlags + c, sm, a.status);
+            epi_sync();
+            const float* gu = reinterpret_cast<const float*>(slot_at(a, c));
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                accg[n] = __ldcg(gu + n * 128 + r) + accg[n];
+                accu[n] = __ldcg(gu + (kN + n) * 128 + r) + accu[n];
+            }
+        }
+        if (!down_only && t1 <= GS && t1 < spc) {
+            // the head (or a middle piece) of a column split inside gate_up:
+            // hand the sums so far on to the CTA after
             float* gu = reinterpret_cast<float*>(slot_at(a, c + 1));
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
@@ -750,17 +771,6 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
         if (down_only) {
             // down alone: the rows' codes come with every stage
         } else if (t0 <= GS) {
-            if (t0 > 0) {
-                // the tail of a column split inside gate_up: head's sums + this CTA's
-                if (etid == 0) wait_flag(a.cnt + kMtokFlags + c, sm, a.status);
-                epi_sync();
-                const float* gu = reinterpret_cast<const float*>(slot_at(a, c));
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    accg[n] = __ldcg(gu + n * 128 + r) + accg[n];
-                    accu[n] = __ldcg(gu + (kN + n) * 128 + r) + accu[n];
-                }
-            }
             // SwiGLU and the live quantisation of h (GLM-5.2 x10 §8c): per
             // token of the column, its 128 h values form one group (the
             // rows of the other tokens keep finite codes from before: their
@@ -1070,7 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         x_ready<MODE>(a, sm, lane);
     } else {
         const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.GS + a.NU;
-        const Share sh = share_of(ncols, spc, MODE == kMtokDown);
+        const Share sh =
+            share_of(ncols, spc, MODE == kMtokDown ? kShareFree : (MODE == kMtokGateUp ? kShareChain : kShareColumns));
         if (warp == kProducerWarp) {
             if (lane == 0) {
                 const long long issued = producer<MODE>(a, sm, stages, sh, spc);
