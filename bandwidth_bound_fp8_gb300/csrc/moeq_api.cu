@@ -1126,7 +1126,7 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
         t.xq = reinterpret_cast<uint8_t*>(base + l.mt_xq);
         t.xs = reinterpret_cast<float*>(base + l.mt_xs);
         t.part = reinterpret_cast<float*>(base + l.mt_part);
-        t.mode = kMtokLayer;
+        t.mode = kMtokDense;
         t.GS = t.KB;
         t.NU = t.KB / 2;
         t.KX = t.KB;

@@ -151,13 +151,14 @@ cudaError_t launch_token(const TokenArgs& args, int grid, bool pdl, cudaStream_t
 // tensor cores, H a multiple of 256 up to kTokenMaxH, top_k up to 16.  Its
 // modes: the layer (routing; top_k = 0: a dense FFN), gate_up + SwiGLU
 // alone, and down alone, the last two over a caller's plan.
-constexpr int kMtokLayer = 0, kMtokGateUp = 1, kMtokDown = 2;
+constexpr int kMtokLayer = 0, kMtokGateUp = 1, kMtokDown = 2, kMtokDense = 3;   // kMtokDense: the layer with
+                                                                             // no routing (top_k = 0)
 struct MtokArgs {
     const void* x;               // [M, x_ld] bf16 (or fp32 with x_f32): the layer's x, gate_up's x, down's a
     const float* logits;         // [M, E_routed]
     int M, H, I, KB, RB;         // layer and gate_up: KB = H/128, RB = I/128; down: M pair rows, H = N,
                                  // KB = N/128 row blocks, RB = K/128 K groups, I = K
-    int mode;                    // kMtokLayer, kMtokGateUp or kMtokDown
+    int mode;                    // kMtokLayer, kMtokGateUp, kMtokDown or kMtokDense
     int GS, NU;                  // per column: gate_up stages (KB or 0) and down units of 256 rows (KB/2 or 0)
     int KX, x_ld, x_f32;         // the quantised input's K groups, row length and type
     int ntmax;                   // most rows (tokens or pairs) one column serves: 1..16

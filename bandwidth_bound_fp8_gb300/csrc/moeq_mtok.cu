@@ -188,7 +188,17 @@ __device__ __forceinline__ uint8_t* slot_at(const MtokArgs& a, int b) {
 // [tail_t0, tail_t1)).  With more columns than CTAs the stages are dealt
 // evenly (a range then holds at most one head and one tail).  With no more
 // columns than CTAs it depends on the launch:
-//   kShareColumns (the layer): one whole column per CTA;
+//   kShareColumns (the MoE layer): one column per CTA;
+//   kShareHelp (the dense layer): one column per CTA, and the CTAs left over
+//     (helpers) stream the first g0 gate_up stages of every column, each
+//     helper a few columns' heads in turn, handing their sums on through
+//     the column's own slot; g0 is as large as lets every head be done
+//     before its column's owner has streamed the rest of gate_up: the
+//     busiest helper's h heads take h g0 <= GS - g0 stages, so
+//     g0 = GS / (h + 1) with h = ceil(columns / helpers).  Only while a
+//     helper has at most two heads of at least 8 stages: each piece costs
+//     its CTA a column set-up and a hand-over of about a microsecond or
+//     two, which many small heads would put on the owners' path;
 //   kShareChain (gate_up alone): the stages dealt evenly over min(G, 2 ncols)
 //     CTAs, so that a range is at least half a column and a column spans at
 //     most three CTAs -- a range may lie inside one column (a "tail" that
@@ -196,18 +206,38 @@ __device__ __forceinline__ uint8_t* slot_at(const MtokArgs& a, int b) {
 //     the CTA before and hands them on to the CTA after);
 //   kShareFree (down alone, every stage its own partial): dealt evenly over
 //     the whole grid.
-constexpr int kShareColumns = 0, kShareChain = 1, kShareFree = 2;
+constexpr int kShareColumns = 0, kShareChain = 1, kShareFree = 2, kShareHelp = 3;
 struct Share {
     int head_j, head_t1, j0, j1, tail_j, tail_t0, tail_t1, np;
+    int help;            // kShareHelp with helpers: splits hand on through the column's slot
+    int hj0, hstep, g0;  // a helper's heads: columns hj0, hj0 + hstep, ..., stages [0, g0)
 };
 
-__device__ Share share_of(int ncols, int spc, int kind) {
+__device__ Share share_of(int ncols, int spc, int gs, int kind) {
     const int G = gridDim.x, c = blockIdx.x;
     Share s;
     s.head_j = s.tail_j = -1;
     s.head_t1 = s.tail_t0 = 0;
     s.tail_t1 = spc;
-    if (kind != kShareColumns && ncols <= G) {
+    s.help = s.hj0 = s.hstep = s.g0 = 0;
+    const int nh = G - ncols, hmax = nh > 0 ? (ncols + nh - 1) / nh : 0;
+    const int g0 = kind == kShareHelp && ncols > 0 && nh > 0 ? min(gs / (hmax + 1), gs - 1) : 0;
+    if (g0 >= 8 && hmax <= 2) {
+        s.help = 1;
+        s.g0 = g0;
+        s.j0 = s.j1 = 0;
+        if (c < ncols) {
+            // the owner: the rest of column c
+            s.tail_j = c;
+            s.tail_t0 = g0;
+        } else {
+            s.hj0 = c - ncols;
+            s.hstep = nh;
+        }
+        s.np = c < ncols ? 1 : (ncols - (c - ncols) + nh - 1) / nh;
+        return s;
+    }
+    if ((kind == kShareChain || kind == kShareFree) && ncols <= G) {
         const int Gs = kind == kShareChain ? min(G, 2 * ncols) : G;
         const long long S = static_cast<long long>(ncols) * spc;
         const long long lo = S * min(c, Gs) / Gs, hi = S * min(c + 1, Gs) / Gs;
@@ -256,8 +286,15 @@ __device__ Share share_of(int ncols, int spc, int kind) {
     return s;
 }
 
-// Piece i of the share, in processing order: head, whole columns, tail.
+// Piece i of the share, in processing order: head, whole columns, tail (or
+// a helper's heads).
 __device__ __forceinline__ void piece_at(const Share& s, int i, int spc, int& j, int& t0, int& t1) {
+    if (s.hstep > 0) {
+        j = s.hj0 + i * s.hstep;
+        t0 = 0;
+        t1 = s.g0;
+        return;
+    }
     if (s.head_j >= 0) {
         if (i == 0) {
             j = s.head_j;
@@ -294,7 +331,7 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
     p.offs = sm.plan.offs;
     p.pair_tok = sm.plan.pair_tok;
     p.pair_of = sm.plan.pair_of;
-    if (MODE != kMtokLayer) {
+    if (MODE == kMtokGateUp || MODE == kMtokDown) {
         // the caller's plan (unique experts, their pair ranges, gate_up: each
         // pair's token), checked as the persistent engine checks it: an
         // expert out of range, a pair range that is empty, out of range or
@@ -585,7 +622,7 @@ __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stag
             if (it >= kTmemBufs &&
                 !wait_spin(&sm.tmem_empty[b], static_cast<uint32_t>(((it / kTmemBufs) - 1) & 1), sm, a.status))
                 return last;
-            if (MODE == kMtokLayer && t == max(t0, a.GS)) {   // the piece's first down stage: its h codes
+            if ((MODE == kMtokLayer || MODE == kMtokDense) && t == max(t0, a.GS)) {   // the piece's first down stage: its h codes
                 if (!wait_spin(&sm.h_ready, static_cast<uint32_t>(hcount & 1), sm, a.status)) return last;
                 ++hcount;
             }
@@ -708,7 +745,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
     const int r = quad * 32 + lane;                       // the TMEM lane: row of the tiles
     const uint32_t tlane = sm.tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     const int GS = a.GS, k = a.top_k, c = blockIdx.x;
-    constexpr bool layer = MODE == kMtokLayer, down_only = MODE == kMtokDown;
+    constexpr bool layer = MODE == kMtokLayer || MODE == kMtokDense, down_only = MODE == kMtokDown;
     const int ustride = (k + 1) * a.RB * 256;   // partials of one output unit, per token
     long long it = 0;
     int stored = 0;
@@ -742,12 +779,16 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             }
         }
 
+        // a split inside gate_up hands on through the slot and flag of the
+        // CTA boundary (b before, b + 1 after this CTA), or with helpers
+        // through the column's own
+        const int slot_in = sh.help ? ci.j : c, slot_out = sh.help ? ci.j : c + 1;
         if (!down_only && t0 > 0 && t0 <= GS) {
             // the tail (or a middle piece) of a column split inside gate_up:
             // the sums of the CTA before + this CTA's
-            if (etid == 0) wait_flag(a.cnt + kMtokFlags + c, sm, a.status);
+            if (etid == 0) wait_flag(a.cnt + kMtokFlags + slot_in, sm, a.status);
             epi_sync();
-            const float* gu = reinterpret_cast<const float*>(slot_at(a, c));
+            const float* gu = reinterpret_cast<const float*>(slot_at(a, slot_in));
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 accg[n] = __ldcg(gu + n * 128 + r) + accg[n];
@@ -757,7 +798,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
         if (!down_only && t1 <= GS && t1 < spc) {
             // the head (or a middle piece) of a column split inside gate_up:
             // hand the sums so far on to the CTA after
-            float* gu = reinterpret_cast<float*>(slot_at(a, c + 1));
+            float* gu = reinterpret_cast<float*>(slot_at(a, slot_out));
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 gu[n * 128 + r] = accg[n];
@@ -765,7 +806,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             }
             __threadfence();
             epi_sync();
-            if (etid == 0) st_release(a.cnt + kMtokFlags + c + 1, 1);
+            if (etid == 0) st_release(a.cnt + kMtokFlags + slot_out, 1);
             continue;
         }
         if (down_only) {
@@ -1081,7 +1122,11 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     } else {
         const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.GS + a.NU;
         const Share sh =
-            share_of(ncols, spc, MODE == kMtokDown ? kShareFree : (MODE == kMtokGateUp ? kShareChain : kShareColumns));
+            share_of(ncols, spc, a.GS,
+                     MODE == kMtokDown     ? kShareFree
+                     : MODE == kMtokGateUp ? kShareChain
+                     : MODE == kMtokDense  ? kShareHelp
+                                           : kShareColumns);
         if (warp == kProducerWarp) {
             if (lane == 0) {
                 const long long issued = producer<MODE>(a, sm, stages, sh, spc);
@@ -1145,8 +1190,9 @@ size_t mtok_smem_bytes() { return kSmemBytes; }
 // One instantiation per mode: the layer path carries none of the
 // standalone modes' branches.
 cudaError_t launch_mtok(const MtokArgs& args, int grid, bool pdl, cudaStream_t stream) {
-    if (args.mode < kMtokLayer || args.mode > kMtokDown) return cudaErrorInvalidValue;
-    void (*const kernels[3])(MtokArgs) = {mtok_kernel<kMtokLayer>, mtok_kernel<kMtokGateUp>, mtok_kernel<kMtokDown>};
+    if (args.mode < kMtokLayer || args.mode > kMtokDense) return cudaErrorInvalidValue;
+    void (*const kernels[4])(MtokArgs) = {mtok_kernel<kMtokLayer>, mtok_kernel<kMtokGateUp>, mtok_kernel<kMtokDown>,
+                                          mtok_kernel<kMtokDense>};
     static int configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
