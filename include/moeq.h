@@ -190,6 +190,9 @@ moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k,
 /* GEMM of every unique expert of a plan, split-K over all SMs with a       */
 /* deterministic fp32 reduction, and the SwiGLU epilogue                    */
 /* (GLM-5.2 x10 §1: split-K; §4: quantisation fused into the GEMM).         */
+/* For M <= 16 and H <= 6144 it runs the multi-token kernel's gate_up mode  */
+/* (tcgen05; columns of 128 h rows dealt over the SMs, a split column's     */
+/* sums handed on); otherwise the persistent engine.                        */
 /*   x       [M, H] bf16 or fp32, M <= MOEQ_MAX_TOKENS                      */
 /*   w_gu    n_experts x [2I, H] E4M3 tile-major: gate rows [0, I), up rows */
 /*           [I, 2I)                                                        */
@@ -214,7 +217,9 @@ moeq_status moeq_expert_gemm_gateup_swiglu(
 
 /* ------------------------------------------------------------------------ */
 /* moeq_expert_gemm_down -- quant(a) fused into the down FP8 GEMM of every  */
-/* unique expert, split-K, deterministic fp32 reduction.                    */
+/* unique expert, split-K, deterministic fp32 reduction.  For N a multiple  */
+/* of 256 up to 6144 and K <= 6144 it runs the multi-token kernel's down    */
+/* mode (tcgen05; its stages dealt over every SM); otherwise the engine.    */
 /*   a       [max_pairs, K] bf16 or fp32; row p is the input of pair p      */
 /*           (h from the gate_up call, or x for a dense projection)         */
 /*   w_d     n_experts x [N, K] E4M3 tile-major; s_d [n_experts, N/128,     */
@@ -286,9 +291,11 @@ moeq_status moeq_combine(const float* y, int N, const moeq_route_plan* plan, int
 /*   128-wide K group of down streams that group's gate and up rows for     */
 /*   every token, forms and quantises the group, and streams down's K group */
 /*   against every output row; the fp32 partials of each (token, 16 output  */
-/*   rows) are summed in a fixed order by idle warps.  With                 */
-/*   MOEQ_MTOK_MIN_TOKENS above 1, one token runs the one-token kernel (CUDA */
-/*   cores) instead.  Launched with programmatic dependent launch (see      */
+/*   rows) are summed in a fixed order by idle warps.  With fewer columns   */
+/*   (I/128) than SMs, the SMs left over stream the first part of the       */
+/*   columns' gate_up and hand the sums on.  With MOEQ_MTOK_MIN_TOKENS       */
+/*   above 1, one token runs the one-token kernel (CUDA cores) instead.     */
+/*   Launched with programmatic dependent launch (see                       */
 /*   moeq_moe_layer): the weights must not be written by the kernel right   */
 /*   ahead of this call on the same stream, except by moeq_quant_weight /    */
 /*   moeq_pack_weight, which this library tracks.                          */
