@@ -734,6 +734,7 @@ size_t moeq_gemm_ws_count_offset(int rows_out, int K, int rows_in, int max_uniq,
     const bool mt = is_gate_up ? gateup_mtok_ok(rows_in, K, max_uniq, rows_in * (MOEQ_MAX_TOPK + 1))
                                : down_mtok_ok(K, rows_out, max_uniq, rows_in);
     if (!mt || (which == 1 && is_gate_up)) return 0;
+    if (which == 0 && !is_gate_up) return 0;   // down alone quantises a per piece: no count
     const DeviceInfo dev = current_device();
     const size_t end = gemm_ws_layout(is_gate_up ? 0 : 1, rows_out / 128, K, rows_in, max_uniq, dev.sms).end;
     const size_t base = mtok_gemm_ws(is_gate_up != 0, is_gate_up ? 2 * rows_out : rows_out, K, rows_in, dev.sms, end).cnt;

@@ -110,13 +110,15 @@ struct ColInfo {
 
 struct Smem {
     alignas(1024) uint8_t hbuf[kXGroupBytes];   // h codes: down's B operand (token n in row n, 128B swizzle)
+    alignas(1024) uint8_t abuf[2][kXGroupBytes];   // down alone: a's codes of a piece's K group (B operand),
+                                                   // by piece parity
     float sx[kMaxKB][kN];                       // x scales per (K group, token)
     float hs[kN], hw[kN];                       // h scales; h scale x routing weight
     float amax[kEpiWarps][kN];
     ColInfo col[2];
     PlanSmem plan;
     RouteScratch rs;
-    uint64_t full[kStages], empty[kStages], mma_done[kTmemBufs], tmem_empty[kTmemBufs], h_ready;
+    uint64_t full[kStages], empty[kStages], mma_done[kTmemBufs], tmem_empty[kTmemBufs], h_ready, a_ready[2];
     uint64_t xq_bar[kMaxKB];
     uint32_t tmem_base;
     int wdone[kEpiWarps];                       // down stages whose partials each epilogue warp has stored
@@ -529,32 +531,25 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
     const uint64_t pol = l2_evict_first_policy();
     constexpr bool down = MODE == kMtokDown;
     const uint32_t gu_xbytes = static_cast<uint32_t>(a.M) * 128;
-    // a stage's x copy: K group (its release barrier), and (down) source
-    // and size; gate_up's follow from the K group
+    // a gate_up stage's x copy waits for its K group's release: (stage, K group)
     int pend_s[kStages], pend_t[kStages];
-    const uint8_t* pend_src[down ? kStages : 1];
-    uint32_t pend_n[down ? kStages : 1];
     int npend = 0;
     auto flush = [&]() -> bool {
         for (int q = 0; q < npend; ++q) {
             if (!wait_sleep(&sm.xq_bar[pend_t[q]], 0, sm, a.status)) return false;
-            bulk_load(stages + static_cast<size_t>(pend_s[q]) * kStageBytes + 2 * kTile,
-                      down ? pend_src[q] : xq_group(a, pend_t[q]), down ? pend_n[q] : gu_xbytes, &sm.full[pend_s[q]],
-                      pol);
+            bulk_load(stages + static_cast<size_t>(pend_s[q]) * kStageBytes + 2 * kTile, xq_group(a, pend_t[q]),
+                      gu_xbytes, &sm.full[pend_s[q]], pol);
         }
         npend = 0;
         return true;
     };
-    auto x_copy = [&](int s, int t, const uint8_t* src, uint32_t bytes) {
+    auto x_copy = [&](int s, int t) {
         if (npend == 0 && mbar_try_wait(&sm.xq_bar[t], 0)) {
-            bulk_load(stages + static_cast<size_t>(s) * kStageBytes + 2 * kTile, src, bytes, &sm.full[s], pol);
+            bulk_load(stages + static_cast<size_t>(s) * kStageBytes + 2 * kTile, xq_group(a, t), gu_xbytes,
+                      &sm.full[s], pol);
         } else {
             pend_s[npend] = s;
             pend_t[npend] = t;
-            if (down) {
-                pend_src[npend] = src;
-                pend_n[npend] = bytes;
-            }
             ++npend;
         }
     };
@@ -564,8 +559,6 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
         piece_at(sh, i, spc, j, t0, t1);
         col_of(j, sm.plan.n_uniq, a.RB, g, kb);
         const int e = sm.plan.uniq[g];
-        // down mode: the column's pair rows of K group kb (B rows 0 .. n - 1)
-        const int r0 = sm.plan.offs[g], nr = min(sm.plan.offs[g + 1] - r0, kN);
         for (int t = t0; t < t1; ++t, ++it) {
             const int s = static_cast<int>(it % kStages);
             if (it >= kStages) {
@@ -578,14 +571,12 @@ __device__ long long producer(const MtokArgs& a, Smem& sm, uint8_t* stages, cons
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + gu_xbytes);
                 bulk_load(dst, gu_tile(a, e, kb, t), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, gu_tile(a, e, a.RB + kb, t), kTile, &sm.full[s], pol);
-                x_copy(s, t, xq_group(a, t), gu_xbytes);
+                x_copy(s, t);
             } else {
                 const int u = t - a.GS;
-                const uint32_t xbytes = down ? static_cast<uint32_t>(nr) * 128 : 0;
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile + xbytes);
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
                 bulk_load(dst, dn_tile(a, e, 2 * u, kb), kTile, &sm.full[s], pol);
                 bulk_load(dst + kTile, dn_tile(a, e, 2 * u + 1, kb), kTile, &sm.full[s], pol);
-                if (down) x_copy(s, kb, a.xq + (static_cast<size_t>(kb) * a.M + r0) * 128, xbytes);
             }
         }
     }
@@ -611,6 +602,7 @@ template <int MODE>
 __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stages, const Share& sh, int spc,
                                 int lane) {
     const uint32_t stage0 = smem_u32(stages), hb = smem_u32(sm.hbuf);
+    const uint32_t ab[2] = {smem_u32(sm.abuf[0]), smem_u32(sm.abuf[1])};
     long long it = 0, last = -1;
     int hcount = 0;
     for (int i = 0; i < sh.np; ++i) {
@@ -626,10 +618,13 @@ __device__ long long mma_issuer(const MtokArgs& a, Smem& sm, const uint8_t* stag
                 if (!wait_spin(&sm.h_ready, static_cast<uint32_t>(hcount & 1), sm, a.status)) return last;
                 ++hcount;
             }
+            if (MODE == kMtokDown && t == t0) {   // down alone: the piece's rows of a, quantised by the epilogue
+                if (!wait_spin(&sm.a_ready[i & 1], static_cast<uint32_t>((i >> 1) & 1), sm, a.status)) return last;
+            }
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t sa = stage0 + static_cast<uint32_t>(s * kStageBytes);
-                const uint32_t bb = (MODE == kMtokDown || t < a.GS) ? sa + 2 * kTile : hb;
+                const uint32_t bb = MODE == kMtokDown ? ab[i & 1] : (t < a.GS ? sa + 2 * kTile : hb);
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const uint32_t d = sm.tmem_base + static_cast<uint32_t>((b * 2 + tt) * kN);
@@ -669,17 +664,55 @@ __device__ void load_col(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
             v = __ldg(a.s_d + (static_cast<size_t>(e) * KB + t) * a.RB + kb);
         ci.sw[which][t] = v;
     }
+    if (MODE == kMtokDown) {
+        // down alone: the piece's rows of a at K group kb (the expert's pair
+        // rows offs[g] ..), quantised here into the piece's B operand and
+        // their scales into the column info.  Buffer i & 1 was piece i - 2's,
+        // whose MMAs are complete: this runs before the epilogue takes piece
+        // i - 1's stages, after it took all of piece i - 2's.  The piece
+        // that holds the column's first stage writes the optional dump.
+        const int r0 = sm.plan.offs[g], nr = min(sm.plan.offs[g + 1] - r0, kN);
+        const int w = etid >> 5, lane = etid & 31;
+        uint8_t* b = sm.abuf[i & 1];
+        constexpr int kRows = kN / kEpiWarps;   // a warp's rows: w, w + 4, ...
+        float4 v[kRows];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int n = w + q * kEpiWarps;
+            if (n < nr)
+                v[q] = a.x_f32 ? load_act4<true>(a.x, static_cast<size_t>(a.x_ld), r0 + n, kb * 128 + 4 * lane)
+                               : load_act4<false>(a.x, static_cast<size_t>(a.x_ld), r0 + n, kb * 128 + 4 * lane);
+        }
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int n = w + q * kEpiWarps;
+            if (n < nr) {
+                float sc;
+                float4 dec;
+                const uint32_t codes = quant_group_warp(v[q], &sc, &dec);
+                *reinterpret_cast<uint32_t*>(b + n * 128 + (((lane >> 2) ^ (n & 7)) << 4) + (lane & 3) * 4) = codes;
+                if (lane == 0) ci.xsc[n] = sc;
+                if (a.q_x && t0 == 0) {
+                    *reinterpret_cast<uint32_t*>(a.q_x + static_cast<size_t>(r0 + n) * a.x_ld + kb * 128 + 4 * lane) =
+                        codes;
+                    if (lane == 0) a.s_x[(r0 + n) * a.KX + kb] = sc;
+                }
+            }
+        }
+        fence_proxy_async_smem();   // the codes are read by the MMAs (async proxy)
+        epi_sync();
+        if (etid == 0) mbar_arrive(&sm.a_ready[i & 1]);
+    }
     if (etid < 32) {
         const int n = etid, k = a.top_k, U = sm.plan.n_uniq, nu = a.NU;
         int pair = -1, slot = 0;
         float w = 0.0f, xsc = 0.0f;
         if (MODE == kMtokDown) {
-            // row n of the column: the chunk's pair row offs[g] + n
-            wait_sleep(&sm.xq_bar[kb], 0, sm, a.status);   // the rows' scales of K group kb
+            // row n of the column: the expert's pair row offs[g] + n
             if (n < min(sm.plan.offs[g + 1] - sm.plan.offs[g], kN)) {
                 pair = sm.plan.offs[g] + n;
                 w = 1.0f;
-                xsc = __ldcg(a.xs + static_cast<size_t>(kb) * a.M + pair);
+                xsc = ci.xsc[n];
             }
         } else if (n < a.M) {
             for (int p = sm.plan.offs[g]; p < sm.plan.offs[g + 1]; ++p)
@@ -1061,6 +1094,8 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         mbar_init(&sm.tmem_empty[tid - 32], kEpiWarps);
     } else if (tid == 64) {
         mbar_init(&sm.h_ready, 1);
+        mbar_init(&sm.a_ready[0], 1);
+        mbar_init(&sm.a_ready[1], 1);
         sm.abort_flag = 0;
     } else if (tid >= 96 && tid < 96 + kMaxKB) {
         mbar_init(&sm.xq_bar[tid - 96], 1);
@@ -1074,6 +1109,8 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         *reinterpret_cast<uint4*>(stages + static_cast<size_t>(s) * kStageBytes + 2 * kTile + o) = make_uint4(0, 0, 0, 0);
     }
     for (int q = tid; q < kXGroupBytes / 16; q += kThreads) reinterpret_cast<uint4*>(sm.hbuf)[q] = make_uint4(0, 0, 0, 0);
+    for (int q = tid; q < 2 * kXGroupBytes / 16; q += kThreads)
+        reinterpret_cast<uint4*>(&sm.abuf[0][0])[q] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == kMmaWarp) tmem_alloc(&sm.tmem_base, kTmemCols);
     // before the previous kernel is done: this CTA's share of the shared
@@ -1112,13 +1149,14 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
         named_arrive(3, kThreads - 32);        // ... and for warps 7-11
     } else {
         pdl_wait();
-        quantise_x<MODE>(a, warp - kQuantWarp0, lane);
+        // (down alone: each piece's epilogue quantises its rows of a itself)
+        if (MODE != kMtokDown) quantise_x<MODE>(a, warp - kQuantWarp0, lane);
         if (warp != kQuantWarp0) named_sync(3, kThreads - 32);
     }
     if (warp == kQuantWarp0) {
         // warp 6 goes on at once to release x's K groups as the grid's
         // quantisation completes (it needs no plan)
-        x_ready<MODE>(a, sm, lane);
+        if (MODE != kMtokDown) x_ready<MODE>(a, sm, lane);
     } else {
         const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.GS + a.NU;
         const Share sh =

@@ -143,9 +143,9 @@ size_t moeq_gemm_workspace_size(int rows_out, int K, int rows_in, int max_uniq, 
 /* wait run out (MOEQ_ERR_TIMEOUT); re-initialise the workspace after.      */
 size_t moeq_layer_ws_count_offset(int M, int H, int I, int n_experts_incl_shared, int top_k, int which);
 /* The same for a standalone GEMM call's workspace (the arguments of        */
-/* moeq_gemm_workspace_size): the offset of the count of x's (a's) K group  */
-/* 0 (which = 0) or of output unit 0 (which = 1, down only), or 0 when the  */
-/* call's shape does not run the multi-token kernel.                        */
+/* moeq_gemm_workspace_size): the offset of the count of x's K group 0      */
+/* (which = 0, gate_up only) or of output unit 0 (which = 1, down only),    */
+/* or 0 when the call's shape does not run the multi-token kernel.          */
 size_t moeq_gemm_ws_count_offset(int rows_out, int K, int rows_in, int max_uniq, int is_gate_up, int which);
 /* Zero the workspace (split-K tickets and the device status word) on
  * `stream`.  Needed once after allocation; kernels leave it zeroed.  After a

@@ -122,11 +122,12 @@ def test_layer_kernel_wait_reports_timeout_and_the_context_survives(orc, M, whic
 
 
 
-@pytest.mark.parametrize("gate_up,which", [(0, 0), (0, 1), (1, 0)])
+@pytest.mark.parametrize("gate_up,which", [(0, 1), (1, 0)])
 def test_gemm_kernel_wait_reports_timeout_and_the_context_survives(orc, gate_up, which):
     """The standalone GEMM calls on the multi-token kernel: the count of
-    the input's K group 0, or (down) of output unit 0, set out of reach in
-    the call's workspace.  The wait gives up, the status says
+    x's K group 0 (gate_up), or of output unit 0 (down, whose pieces
+    quantise their own rows of a), set out of reach in the call's
+    workspace.  The wait gives up, the status says
     MOEQ_ERR_TIMEOUT, and after a re-initialisation the call on the same
     context matches the oracle."""
     from bandwidth_bound_fp8_gb300 import moeq
