@@ -204,9 +204,10 @@ StreamWs gemm_ws_layout(int kind, int RB, int K, int rows_a, int max_uniq, int g
 }
 
 // The multi-token kernel's areas for a standalone GEMM call (gate_up alone or
-// down alone), from `base` on: counts and flags, split-column slots (gate_up),
-// the quantised input's codes and scales (gate_up: 16 token rows per K group;
-// down: every pair row), and the down partials [pair][N/256][K/128][256].
+// down alone), from `base` on: counts and flags, and for gate_up the
+// split-column slots and x's codes and scales (16 token rows per K group),
+// for down the partials [pair][N/256][K/128][256] (down quantises its rows
+// of a in shared memory).
 struct MtokGemmWs {
     size_t cnt, slots, xq, xs, part, end;
 };
@@ -217,8 +218,8 @@ MtokGemmWs mtok_gemm_ws(bool gate_up, int rows_out, int K, int rows_in, int grid
     l.cnt = align_up(base, 256);
     l.slots = align_up(l.cnt + sizeof(int) * (kMtokFlags + grid + 1), 256);
     l.xq = align_up(l.slots + (gate_up ? static_cast<size_t>(grid + 1) * kMtokSlotBytes : 0), 256);
-    l.xs = align_up(l.xq + (gate_up ? KX * kMtokXGroupBytes : KX * rows_in * 128), 256);
-    l.part = align_up(l.xs + sizeof(float) * KX * (gate_up ? 16 : rows_in), 256);
+    l.xs = align_up(l.xq + (gate_up ? KX * kMtokXGroupBytes : 0), 256);
+    l.part = align_up(l.xs + (gate_up ? sizeof(float) * KX * 16 : 0), 256);
     l.end = align_up(l.part + (gate_up ? 0 : sizeof(float) * rows_in * static_cast<size_t>(rows_out) * KX), 256);
     return l;
 }

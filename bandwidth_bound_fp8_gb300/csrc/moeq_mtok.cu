@@ -1,4 +1,4 @@
-// The multi-token MoE layer kernel (2..16 tokens: decode batches and draft
+// The multi-token MoE layer kernel (1..16 tokens: decode and draft
 // verification): route, live quantisation of x, gate_up + SwiGLU, live
 // quantisation of h, down and the combine in one launch, the GEMMs on the
 // tcgen05 tensor cores.
@@ -56,8 +56,17 @@
 // Launched with programmatic dependent launch: before griddepcontrol.wait a
 // CTA only starts its share of the shared expert's weights towards L2.
 //
-// With top_k = 0 the same kernel is a dense FFN (no routing): the one expert
-// is the "shared" one, serving every token.
+// One instantiation per mode (the template parameter):
+//   kMtokLayer    the MoE layer, as above;
+//   kMtokDense    a dense FFN (top_k = 0, no routing: the one expert is the
+//                 "shared" one, serving every token); with fewer columns
+//                 than CTAs the CTAs left over stream the columns' first
+//                 gate_up stages (share_of);
+//   kMtokGateUp   gate_up + SwiGLU alone over a caller's plan, h to global;
+//   kMtokDown     down alone over a caller's plan: each piece's epilogue
+//                 quantises its rows of a into a shared-memory B operand,
+//                 and the stages, independent of one another, are dealt
+//                 over every CTA.
 #include "moeq_device.cuh"
 #include "moeq_internal.h"
 #include "moeq_route.cuh"
@@ -420,25 +429,9 @@ __device__ void route_all(const MtokArgs& a, Smem& sm, int tid) {
 // which writes its codes into row n of K group t of the one copy in L2 (the
 // gate_up stages' B operand: token n in row n of an 8-row, 128-byte-swizzled
 // atom pair) and its scale beside it, then counts itself in K group t.
-// The position of pair row n inside its expert's rows (down mode: row n
-// goes to the MMA as row n - offs[g] of its expert's B operand, so its
-// 128-byte swizzle phase is that position mod 8).  The plan is checked by the
-// routing warps at the same time; a plan that fails that check gets no MMA,
-// so here U only has to stay within the plan's arrays.
-__device__ __forceinline__ int pos_in_expert(const MtokArgs& a, int n) {
-    const int U = min(max(__ldcg(a.plan.n_uniq), 0), a.max_uniq);
-    int lo = 0, hi = U;   // the last g with offs[g] <= n
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldcg(a.plan.offs + mid) <= n) lo = mid; else hi = mid;
-    }
-    return n - __ldcg(a.plan.offs + lo);
-}
-
-template <int MODE>
+// (layer, dense and gate_up: down alone quantises its rows of a per piece)
 __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
     const int M = a.M, ngroups = M * a.KX;
-    constexpr bool down = MODE == kMtokDown;
     for (int q = blockIdx.x * kQuantWarps + wq; q < ngroups; q += gridDim.x * kQuantWarps) {
         const int t = q / M, n = q - t * M;
         const float4 v = a.x_f32 ? load_act4<true>(a.x, static_cast<size_t>(a.x_ld), n, t * 128 + 4 * lane)
@@ -446,13 +439,10 @@ __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
         float sc;
         float4 dec;
         const uint32_t codes = quant_group_warp(v, &sc, &dec);
-        // layer and gate_up: token n in row n of K group t's 16 rows; down:
-        // K group t's rows are every pair row, each swizzled for its place
-        // in its expert's chunk of 16
-        const int ph = down ? (pos_in_expert(a, n) & 7) : (n & 7);
-        uint8_t* row = down ? a.xq + (static_cast<size_t>(t) * M + n) * 128 : xq_group(a, t) + n * 128;
-        *reinterpret_cast<uint32_t*>(row + (((lane >> 2) ^ ph) << 4) + (lane & 3) * 4) = codes;
-        if (lane == 0) a.xs[t * (down ? M : kN) + n] = sc;
+        // token n in row n of K group t's 16 rows (128-byte swizzle)
+        *reinterpret_cast<uint32_t*>(xq_group(a, t) + n * 128 + (((lane >> 2) ^ (n & 7)) << 4) + (lane & 3) * 4) =
+            codes;
+        if (lane == 0) a.xs[t * kN + n] = sc;
         if (a.q_x) {
             *reinterpret_cast<uint32_t*>(a.q_x + static_cast<size_t>(n) * a.x_ld + t * 128 + 4 * lane) = codes;
             if (lane == 0) a.s_x[n * a.KX + t] = sc;
@@ -469,7 +459,6 @@ __device__ void quantise_x(const MtokArgs& a, int wq, int lane) {
 // each on its own (bounded) -- once a group's count shows all M tokens in,
 // the lane takes its scales into shared memory and releases it to the
 // producer and the epilogue.
-template <int MODE>
 __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
     constexpr int kPer = (kMaxKB + 31) / 32;
     bool done[kPer];
@@ -484,8 +473,7 @@ __device__ void x_ready(const MtokArgs& a, Smem& sm, int lane) {
             const int t = lane + 32 * i;
             if (ld_relaxed(a.cnt + kMtokX + kMtokPad * t) >= a.M && ld_acquire(a.cnt + kMtokX + kMtokPad * t) >= a.M) {
                 fence_proxy_async_global();
-                if (MODE != kMtokDown)   // (down: each column reads its rows' scales itself)
-                    for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
+                for (int n = 0; n < kN; ++n) sm.sx[t][n] = n < a.M ? __ldcg(a.xs + t * kN + n) : 0.0f;
                 mbar_arrive(&sm.xq_bar[t]);
                 done[i] = true;
             } else {
@@ -1150,13 +1138,13 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     } else {
         pdl_wait();
         // (down alone: each piece's epilogue quantises its rows of a itself)
-        if (MODE != kMtokDown) quantise_x<MODE>(a, warp - kQuantWarp0, lane);
+        if (MODE != kMtokDown) quantise_x(a, warp - kQuantWarp0, lane);
         if (warp != kQuantWarp0) named_sync(3, kThreads - 32);
     }
     if (warp == kQuantWarp0) {
         // warp 6 goes on at once to release x's K groups as the grid's
         // quantisation completes (it needs no plan)
-        if (MODE != kMtokDown) x_ready<MODE>(a, sm, lane);
+        if (MODE != kMtokDown) x_ready(a, sm, lane);
     } else {
         const int U = sm.plan.n_uniq, ncols = U * a.RB, spc = a.GS + a.NU;
         const Share sh =

@@ -741,6 +741,58 @@ def profile_case(M: int, reps: int, Er: int = 8):
                       "unique_experts": U, "algorithmic_bytes": U * EXPERT_BYTES}))
 
 
+def profile_dense(reps: int):
+    """Small launches for ncu captures of the dense configurations: `reps`
+    calls each of the projection K 2048 -> N 4096 (moeq_expert_gemm_down:
+    mtok_kernel<2>) and of the FFN hidden 6144 / intermediate 12288
+    (moeq_dense_ffn: mtok_kernel<3>), on their seeded weights and inputs,
+    with more than L2 written before each call so that the weights come from
+    HBM."""
+    from bandwidth_bound_fp8_gb300 import build as b
+    b.build()
+    from bandwidth_bound_fp8_gb300 import moeq
+    scrub = torch.empty(2 * L2_BYTES // 4 + 1024, dtype=torch.float32, device="cuda")
+    c = synth.DENSE_PROJ
+    K, N = c["K"], c["N"]
+    wq = torch.empty((1, N, K), dtype=torch.uint8, device="cuda")
+    ws_ = torch.empty((1, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    moeq.moeq_quant_weight(synth.weight_f32(N, K, synth.expert_seed(c["seed"], 0, 0, 1), device="cuda")[None], wq, ws_)
+    x = synth.activations_bf16(1, K, c["seed"], c["n_outlier"], c["outlier_scale"], device="cuda")
+    one = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    uq, of, nu = one([0]), one([0, 1]), one([1])
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    wsp = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, 1, 1, 0))
+    for _ in range(reps):
+        scrub.zero_()
+        moeq.moeq_expert_gemm_down(x, K, N, wq, ws_, 1, uq, of, nu, 1, 1, y, wsp)
+    torch.cuda.synchronize()
+    if moeq.moeq_read_device_status(wsp.t, wsp.nbytes) != 0:
+        raise RuntimeError("device status word set")
+    del wq, ws_
+    c = synth.DENSE_FFN
+    Hh, Ii = c["H"], c["I"]
+    gq = torch.empty((1, 2 * Ii, Hh), dtype=torch.uint8, device="cuda")
+    gs = torch.empty((1, 2 * Ii // 128, Hh // 128), dtype=torch.float32, device="cuda")
+    dq = torch.empty((1, Hh, Ii), dtype=torch.uint8, device="cuda")
+    dsc = torch.empty((1, Hh // 128, Ii // 128), dtype=torch.float32, device="cuda")
+    moeq.moeq_quant_weight(synth.weight_f32(2 * Ii, Hh, synth.expert_seed(c["seed"], 0, 0, 0), device="cuda")[None],
+                           gq, gs)
+    moeq.moeq_quant_weight(synth.weight_f32(Hh, Ii, synth.expert_seed(c["seed"], 0, 0, 1), device="cuda")[None],
+                           dq, dsc)
+    x = synth.activations_bf16(1, Hh, c["seed"], c["n_outlier"], c["outlier_scale"], device="cuda")
+    out = torch.empty((1, Hh), dtype=torch.bfloat16, device="cuda")
+    wsd = moeq.Workspace(moeq.moeq_dense_ffn_workspace_size(1, Hh, Ii))
+    for _ in range(reps):
+        scrub.zero_()
+        moeq.moeq_dense_ffn(x, Hh, Ii, gq, gs, dq, dsc, out, wsd)
+    torch.cuda.synchronize()
+    if moeq.moeq_read_device_status(wsd.t, wsd.nbytes) != 0:
+        raise RuntimeError("device status word set")
+    print(json.dumps({"profile_dense": ["dense_proj_m1_k2048_n4096", "dense_ffn_m1_h6144_i12288"], "launches": reps,
+                      "algorithmic_bytes": [N * K + (N // 128) * (K // 128) * 4,
+                                            3 * Hh * Ii + 3 * (Hh // 128) * (Ii // 128) * 4]}))
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -758,11 +810,16 @@ def main():
                     help="run a few launches of the small ncu case (8 routed experts, top-8) and exit")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--profile-experts", type=int, default=8, help="routed experts of the --profile-case layer")
+    ap.add_argument("--profile-dense", action="store_true",
+                    help="a few launches of the dense configurations (for ncu), no timing")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense configurations and the gate_up ladder")
     ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack sweep")
     ap.add_argument("--stack-calls", type=int, default=40)
     ap.add_argument("--ladder-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.profile_dense:
+        profile_dense(args.reps)
+        return
     if args.profile_case:
         profile_case(args.M, args.reps, args.profile_experts)
         return
