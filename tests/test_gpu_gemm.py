@@ -61,6 +61,10 @@ def oracle_down(orc, a_np, ex, uniq, offs):
     (256, 128, [1], [0, 3]),                       # 3 tokens, tiny: T < grid
     (1280, 512, [2, 5, 0, 1, 3, 4], [0, 1, 2, 3, 4, 5, 21]),   # 16 tokens on one expert
     (768, 512, [2, 0, 1], [0, 5, 21, 28]),         # 16 rows on one expert from pair row 5
+    # 64 experts x 8 K groups = 512 one-stage columns on the multi-token
+    # kernel: 3-4 pieces per CTA, so each of its two shared-memory B operands
+    # is quantised into more than once
+    (1024, 256, list(range(63, -1, -1)), [0] + [1 + i + i // 3 for i in range(64)]),
 ])
 def test_down_small(orc, dtype, K, N, uniq, offs):
     # N a multiple of 256 runs the multi-token kernel's down mode (each
@@ -140,6 +144,9 @@ def check_h(h, g, u, Tg, Tu, h_ref):
     (256, 128, [0], [0, 1], [0], 1),
     (1152, 256, [1, 0], [0, 2, 18], [3, 9] + list(range(16)), 16),
     (512, 10240, [1, 0], [0, 3, 7], [0, 1, 2, 0, 1, 2, 3], 4),   # 160 columns: split between CTAs
+    # 100 columns of 12 stages dealt over 152 CTAs (7.9 stages each): ranges
+    # inside one column (middle pieces) take and hand on the sums
+    (1536, 6400, [1, 0], [0, 2, 4], [0, 1, 0, 1], 2),
 ])
 def test_gateup_small(orc, dtype, H, I, uniq, offs, pair_tok, M):
     E = max(uniq) + 1
