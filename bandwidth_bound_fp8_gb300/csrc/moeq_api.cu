@@ -226,9 +226,11 @@ MtokGemmWs mtok_gemm_ws(bool gate_up, int rows_out, int K, int rows_in, int grid
 
 // The standalone calls run the multi-token kernel where it takes them: at
 // most 16 tokens (gate_up; down: at most 16 rows per expert, as the call
-// requires of every plan), K and (down) N up to 6144, N a multiple of 256,
-// and a plan that fits the kernel's shared copy of it.  The kernel checks
-// the plan as the persistent engine does.
+// requires of every plan), gate_up's K up to 6144, down's N up to 6144 and a
+// multiple of 256 (down's K is free: it counts no K group of a, but its
+// partials, rows x N x K/128 floats, stay within 256 MiB), and a plan that
+// fits the kernel's shared copy of it.  The kernel checks the plan as the
+// persistent engine does.
 constexpr int kMtokMaxPairs = MOEQ_MAX_TOKENS * (MOEQ_MAX_TOPK + 1);
 constexpr int kMtokMaxSlots = MOEQ_MAX_TOKENS * MOEQ_MAX_TOPK;
 bool gateup_mtok_ok(int M, int H, int max_uniq, int max_pairs) {
@@ -236,8 +238,9 @@ bool gateup_mtok_ok(int M, int H, int max_uniq, int max_pairs) {
            max_uniq <= kMtokMaxSlots;
 }
 bool down_mtok_ok(int K, int N, int max_uniq, int max_pairs) {
-    return mtok_kernel_enabled() && N % 256 == 0 && N <= kTokenMaxH && K <= kTokenMaxH &&
-           max_pairs <= kMtokMaxPairs && max_uniq <= kMtokMaxSlots;
+    const size_t part_bytes = sizeof(float) * static_cast<size_t>(max_pairs) * N * (K / 128);
+    return mtok_kernel_enabled() && N % 256 == 0 && N <= kTokenMaxH && K <= MOEQ_MAX_K &&
+           max_pairs <= kMtokMaxPairs && max_uniq <= kMtokMaxSlots && part_bytes <= (size_t{256} << 20);
 }
 
 // The arguments of the multi-token kernel's standalone modes.
@@ -975,11 +978,11 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
     if (!dev.ok) return MOEQ_ERR_DEVICE;
     void* ws = nullptr;
     cudaStream_t cs = as_stream(stream);
-    if (down_mtok_ok(K, N, max_uniq, max_pairs)) {
+    const MtokGemmWs ml = mtok_gemm_ws(false, N, K, max_pairs, dev.sms, kHeader);
+    if (down_mtok_ok(K, N, max_uniq, max_pairs) && ml.end <= kNoAllocScratchBytes) {
         // the path moeq_expert_gemm_down takes: the multi-token kernel, its
-        // areas right after the header, its counts zeroed on the stream first
-        const MtokGemmWs ml = mtok_gemm_ws(false, N, K, max_pairs, dev.sms, kHeader);
-        if (ml.end > kNoAllocScratchBytes) return MOEQ_ERR_WORKSPACE;   // beyond the static maximum
+        // areas right after the header, its counts zeroed on the stream
+        // first (when they do not fit the scratch, the engine below)
         const moeq_status st = noalloc_scratch(&ws);
         if (st != MOEQ_OK) return st;
         if (cudaMemsetAsync(ws, 0, kHeader, cs) != cudaSuccess ||

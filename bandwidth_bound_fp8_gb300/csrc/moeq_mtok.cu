@@ -1199,7 +1199,8 @@ __global__ void __launch_bounds__(kThreads, 1) mtok_kernel(const __grid_constant
     __syncthreads();
     if (sm.last_cta) {
         __threadfence();
-        const int n_x = a.KX, n_u = a.NU, n = n_x + n_u + G + 1;
+        // (down alone counts no K group of its input)
+        const int n_x = MODE == kMtokDown ? 0 : a.KX, n_u = a.NU, n = n_x + n_u + G + 1;
         for (int i = tid; i < n; i += kThreads) {
             const int o = i < n_x ? kMtokX + kMtokPad * i
                                   : (i < n_x + n_u ? kMtokU + kMtokPad * (i - n_x) : kMtokFlags + (i - n_x - n_u));

@@ -218,8 +218,9 @@ moeq_status moeq_expert_gemm_gateup_swiglu(
 /* ------------------------------------------------------------------------ */
 /* moeq_expert_gemm_down -- quant(a) fused into the down FP8 GEMM of every  */
 /* unique expert, split-K, deterministic fp32 reduction.  For N a multiple  */
-/* of 256 up to 6144 and K <= 6144 it runs the multi-token kernel's down    */
-/* mode (tcgen05; its stages dealt over every SM); otherwise the engine.    */
+/* of 256 up to 6144 (and its partials, max_pairs x N x K/128 floats,       */
+/* within 256 MiB) it runs the multi-token kernel's down mode (tcgen05; its */
+/* stages dealt over every SM); otherwise the engine.                       */
 /*   a       [max_pairs, K] bf16 or fp32; row p is the input of pair p      */
 /*           (h from the gate_up call, or x for a dense projection)         */
 /*   w_d     n_experts x [N, K] E4M3 tile-major; s_d [n_experts, N/128,     */
@@ -248,15 +249,18 @@ moeq_status moeq_expert_gemm_down(
 /* whose device memory is committed to its own pools and whose decode step   */
 /* may not call cudaMalloc, which can synchronise the device).               */
 /*   Arguments, layouts and results are those of moeq_expert_gemm_down,      */
-/*   without ws / ws_bytes.                                                  */
+/*   without ws / ws_bytes: it runs the kernel that call runs, bit for bit  */
+/*   the same, except where the multi-token kernel's areas would not fit    */
+/*   the scratch below, when it runs the persistent engine instead.         */
 /*   device_status_opt: NULL, or a caller-owned device int32 that receives   */
 /*   the launch's device status word (0 = MOEQ_OK, else a moeq_status) on    */
 /*   the stream after the launch.                                            */
 /* Scratch: the library's own static device array of 8 MiB per device       */
-/*   (decoded activations and scales, split-K tickets and partials).  A      */
-/*   problem whose scratch would exceed it returns MOEQ_ERR_WORKSPACE and    */
-/*   launches nothing; the dense projection (K 2048, N 4096, one token)      */
-/*   needs ~5 MiB, and K = 32768 with 16 rows ~7 MiB.  Its counters must be  */
+/*   (counts and partials; on the engine also decoded activations and       */
+/*   scales, and split-K tickets).  A problem that fits neither kernel's    */
+/*   areas in it returns MOEQ_ERR_WORKSPACE and launches nothing; the dense */
+/*   projection (K 2048, N 4096, one token) needs ~0.3 MiB on the multi-token */
+/*   kernel, and K = 32768 with 16 rows ~7 MiB on the engine.  Its counters must be  */
 /*   zero when a launch starts: every call zeroes them on `stream` itself    */
 /*   (cudaMemsetAsync), so nothing has to be zero beforehand.                */
 /* Set-up: the first call on each device looks up that device's scratch      */
