@@ -170,7 +170,7 @@ struct MtokArgs {
     const float* s_d;            // [E_routed + 1, H/128, I/128]
     __nv_bfloat16* out;          // [M, H]
     float* out_f32;              // or, when set, [M, H] fp32: the unrounded sums (a tensor-parallel shard's partial)
-    moeq_route_plan plan;        // written by CTA 0
+    moeq_route_plan plan;        // the layer: written by CTA 0; gate_up or down alone: the caller's, read
     float* h;                    // [max_pairs, I]
     uint8_t* q_x;                // optional [M, H] and [M, H/128]: x's codes and scales
     float* s_x;
@@ -179,9 +179,10 @@ struct MtokArgs {
     int* status;
     int* cnt;                    // kMtokFlags + grid + 1 ints, zero between launches
     uint8_t* slots;              // [grid + 1][kMtokSlotBytes]: what a split column's head publishes
-    uint8_t* xq;                 // [KB][16 * 128]: x's codes, token n in row n (gate_up's B operand)
-    float* xs;                   // [KB][16]: x's scales
-    float* part;                 // [M][H/256][top_k + 1][RB][256] down partials
+    uint8_t* xq;                 // [KX][16 * 128]: x's codes, token n in row n (gate_up's B operand;
+    float* xs;                   // [KX][16]: x's scales                          unused by down alone)
+    float* part;                 // [M][H/256][top_k + 1][RB][256] down partials (down alone: M pair rows,
+                                 // H = N, top_k = 0, RB = K/128)
     int route_early;             // 1: the logits are not written by the kernel ahead on the stream, so
                                  // the tokens are routed (and the first weight tiles issued) before
                                  // griddepcontrol.wait

@@ -105,8 +105,9 @@ struct PlanSmem {
     int pair_of[kMaxTok * (kRouteMaxK + 1)];
 };
 
-// One piece of a column: stages [t0, t1) of column j (0 .. KB-1 gate_up,
-// KB .. 3KB/2-1 down units), with what the epilogue needs of it.
+// One piece of a column: stages [t0, t1) of column j (0 .. GS-1 gate_up,
+// GS .. GS+NU-1 down's output units; down alone: GS = 0 and the column is
+// an expert's K group), with what the epilogue needs of it.
 struct ColInfo {
     float sw[3][kMaxKB];   // gate and up weight scales per K group of x; down's per row block
     float rw[kN];          // routing weight of the token's pick of this expert (1: the shared one)
