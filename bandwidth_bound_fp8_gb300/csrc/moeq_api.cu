@@ -493,7 +493,7 @@ moeq_status layer_launch(const LayerCall& c, const DeviceInfo& dev, bool route_e
         t.out = static_cast<__nv_bfloat16*>(out);
         t.out_f32 = c.out_f32;
         t.plan = plan;
-        t.h = h;
+        t.h = h_opt;   // h only when asked for (the kernel needs none of its own)
         t.q_x = q_x_opt;
         t.s_x = s_x_opt;
         t.q_h = q_h_opt;
@@ -1120,7 +1120,7 @@ moeq_status moeq_dense_ffn(const void* x, int M, int H, int I, const uint8_t* w_
         t.w_d = w_d;
         t.s_d = s_d;
         t.out = static_cast<__nv_bfloat16*>(out);
-        t.h = h;
+        t.h = h_opt;   // h only when asked for (the kernel needs none of its own)
         t.q_x = q_x_opt;
         t.s_x = s_x_opt;
         t.q_h = q_h_opt;

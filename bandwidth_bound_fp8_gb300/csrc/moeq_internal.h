@@ -171,7 +171,7 @@ struct MtokArgs {
     __nv_bfloat16* out;          // [M, H]
     float* out_f32;              // or, when set, [M, H] fp32: the unrounded sums (a tensor-parallel shard's partial)
     moeq_route_plan plan;        // the layer: written by CTA 0; gate_up or down alone: the caller's, read
-    float* h;                    // [max_pairs, I]
+    float* h;                    // [max_pairs, I], or null: not written (the layer's h dump)
     uint8_t* q_x;                // optional [M, H] and [M, H/128]: x's codes and scales
     float* s_x;
     uint8_t* q_h;                // optional [max_pairs, I] and [max_pairs, I/128]: h's codes and scales

@@ -845,7 +845,7 @@ __device__ void epilogue(const MtokArgs& a, Smem& sm, const Share& sh, int spc, 
                 if ((tmask >> n) & 1u) {
                     const float gv = accg[n];
                     h[n] = __fdiv_rn(gv, 1.0f + expf(-gv)) * accu[n];
-                    a.h[static_cast<size_t>(ci.pair[n]) * a.I + kb * 128 + r] = h[n];
+                    if (a.h) a.h[static_cast<size_t>(ci.pair[n]) * a.I + kb * 128 + r] = h[n];
                 }
                 m[n] = fabsf(h[n]);
             }
