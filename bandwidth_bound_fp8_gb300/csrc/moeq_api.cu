@@ -56,6 +56,18 @@ int mma_min_tokens() {
     }();
     return v;
 }
+// The standalone GEMM calls that fall to the engine are those beyond the
+// multi-token kernel's shapes, chiefly large-N projections (the LM head:
+// 163 us on tcgen05 against 175 us on the CUDA cores at one token, 170
+// against 594 at four), so they take tcgen05 at every row count unless
+// MOEQ_MMA_MIN_TOKENS says otherwise.
+int gemm_mma_min_tokens() {
+    static const bool set = [] {
+        const char* e = std::getenv("MOEQ_MMA_MIN_TOKENS");
+        return e && std::atoi(e) >= 1;
+    }();
+    return set ? mma_min_tokens() : 1;
+}
 
 // The one-token layer kernel serves M = 1 layers on the CUDA cores unless
 // MOEQ_TOKEN_KERNEL=0 (then the persistent engine does, as it does for every
@@ -863,7 +875,7 @@ moeq_status moeq_expert_gemm_gateup_swiglu(const void* x, moeq_dtype x_dtype, in
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = M;   // the pairs of one expert are distinct tokens
-    a.mma = a.max_ntok >= mma_min_tokens();
+    a.mma = a.max_ntok >= gemm_mma_min_tokens();
     a.M = M;
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, gemm_grid(dev.sms), true, as_stream(stream)));
@@ -920,7 +932,7 @@ moeq_status moeq_expert_gemm_down(const void* a_in, moeq_dtype a_dtype, int K, i
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
-    a.mma = a.max_ntok >= mma_min_tokens();
+    a.mma = a.max_ntok >= gemm_mma_min_tokens();
     fill_ws(a, ws, wl, dev.sms);
     return cuda_status(launch_stream(a, gemm_grid(dev.sms), true, as_stream(stream)));
 }
@@ -1034,7 +1046,7 @@ moeq_status moeq_expert_gemm_down_noalloc(const void* a_in, moeq_dtype a_dtype, 
     a.max_uniq = max_uniq;
     a.max_pairs = max_pairs;
     a.max_ntok = max_pairs < MOEQ_MAX_TOKENS ? max_pairs : MOEQ_MAX_TOKENS;
-    a.mma = a.max_ntok >= mma_min_tokens();   // the path moeq_expert_gemm_down takes
+    a.mma = a.max_ntok >= gemm_mma_min_tokens();   // the path moeq_expert_gemm_down takes
     fill_ws(a, ws, wl, dev.sms);
     if (launch_stream(a, dev.sms, true, cs) != cudaSuccess) return MOEQ_ERR_CUDA;
     if (device_status_opt &&

@@ -673,6 +673,37 @@ def bench_dense(peak, reps=50, with_oracle=True):
     return out
 
 
+def bench_lm_head(peak, reps=30):
+    """An FP8 LM head (GLM-5.2 x10 §8b), the vocabulary projection
+    N = 151,552 x K = 6144 (931 MB of E4M3 codes), through the down GEMM call
+    with one expert and the trivial plan, at 1 and 4 tokens; each call timed
+    alone (the weight is larger than L2 and L2 is scrubbed between calls).
+    N is above the multi-token kernel's 6144, so the persistent engine serves
+    it, on tcgen05 at both row counts."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    K, N = 6144, 151552
+    wq = torch.empty((1, N, K), dtype=torch.uint8, device="cuda")
+    ws_ = torch.empty((1, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    rows = 4096   # quantise in slabs of whole 128-row blocks to bound the fp32 draw
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        w32 = synth.weight_f32(r1 - r0, K, synth.expert_seed(3100, 0, r0 // rows, 1), device="cuda")
+        moeq.moeq_quant_weight(w32[None], wq[:, r0:r1], ws_[:, r0 // 128:r1 // 128])
+    del w32
+    one = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    out = {}
+    for M in (1, 4):
+        x = synth.activations_bf16(M, K, 3101 + M, 61, 30.0, device="cuda")
+        uq, of, nu = one([0]), one([0, M]), one([1])
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        wsp = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, M, 1, 0))
+        torch.cuda.synchronize()
+        t = time_scrubbed(lambda: moeq.moeq_expert_gemm_down(x, K, N, wq, ws_, 1, uq, of, nu, 1, M, y, wsp), reps, 5)
+        out[f"M{M}"] = _line(f"lm_head_m{M}_k{K}_n{N}", N * K + (N // 128) * (K // 128) * 4, t, peak)
+        out[f"M{M}"]["call"] = "moeq_expert_gemm_down (one expert; the persistent engine, tcgen05)"
+    return out
+
+
 def gate_up_ladder(peak, variants=("split_all_sms", "quant_launch_first"), reps=30):
     """The one-token gate_up of a layer (the shared expert and 8 routed
     experts: 226.5 MB) in the variants the GLM-5.2 x10 page measured (§1):
@@ -957,6 +988,7 @@ def main():
         ladder = gate_up_ladder(peak)
         ladder["four_ctas"] = gate_up_ladder_child(peak)
         dense["gate_up_ladder"] = ladder
+        dense["lm_head"] = bench_lm_head(peak)
     e2e = e2e_batch = None
     if rank == 0:
         e = bench_e2e(stack, args.M, min(args.e2e_steps, args.steps), seed=9000)

@@ -192,7 +192,8 @@ moeq_status moeq_route(const float* logits, int M, int E_routed, int top_k,
 /* (GLM-5.2 x10 §1: split-K; §4: quantisation fused into the GEMM).         */
 /* For M <= 16 and H <= 6144 it runs the multi-token kernel's gate_up mode  */
 /* (tcgen05; columns of 128 h rows dealt over the SMs, a split column's     */
-/* sums handed on); otherwise the persistent engine.                        */
+/* sums handed on); otherwise the persistent engine (tcgen05 at every row   */
+/* count unless MOEQ_MMA_MIN_TOKENS sets a crossover).                      */
 /*   x       [M, H] bf16 or fp32, M <= MOEQ_MAX_TOKENS                      */
 /*   w_gu    n_experts x [2I, H] E4M3 tile-major: gate rows [0, I), up rows */
 /*           [I, 2I)                                                        */
@@ -220,7 +221,8 @@ moeq_status moeq_expert_gemm_gateup_swiglu(
 /* unique expert, split-K, deterministic fp32 reduction.  For N a multiple  */
 /* of 256 up to 6144 (and its partials, max_pairs x N x K/128 floats,       */
 /* within 256 MiB) it runs the multi-token kernel's down mode (tcgen05; its */
-/* stages dealt over every SM); otherwise the engine.                       */
+/* stages dealt over every SM); otherwise the engine (tcgen05 at every row */
+/* count unless MOEQ_MMA_MIN_TOKENS sets a crossover).                      */
 /*   a       [max_pairs, K] bf16 or fp32; row p is the input of pair p      */
 /*           (h from the gate_up call, or x for a dense projection)         */
 /*   w_d     n_experts x [N, K] E4M3 tile-major; s_d [n_experts, N/128,     */
