@@ -673,6 +673,33 @@ def bench_dense(peak, reps=50, with_oracle=True):
     return out
 
 
+LM_HEAD_K, LM_HEAD_N = 6144, 151552
+
+
+def lm_head_calls():
+    """The LM head's seeded FP8 weight (N x K, quantised from fp32 draws in
+    slabs of 4096 rows) and, for M = 1 and 4, a closure making one
+    moeq_expert_gemm_down call over it: yields (M, call, workspace)."""
+    from bandwidth_bound_fp8_gb300 import moeq
+    K, N = LM_HEAD_K, LM_HEAD_N
+    wq = torch.empty((1, N, K), dtype=torch.uint8, device="cuda")
+    ws_ = torch.empty((1, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    rows = 4096   # whole 128-row blocks per slab; bounds the fp32 draw
+    for r0 in range(0, N, rows):
+        r1 = min(N, r0 + rows)
+        w32 = synth.weight_f32(r1 - r0, K, synth.expert_seed(3100, 0, r0 // rows, 1), device="cuda")
+        moeq.moeq_quant_weight(w32[None], wq[:, r0:r1], ws_[:, r0 // 128:r1 // 128])
+        del w32
+    one = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    for M in (1, 4):
+        x = synth.activations_bf16(M, K, 3101 + M, 61, 30.0, device="cuda")
+        uq, of, nu = one([0]), one([0, M]), one([1])
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        wsp = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, M, 1, 0))
+        yield M, (lambda x=x, uq=uq, of=of, nu=nu, M=M, y=y, wsp=wsp:
+                  moeq.moeq_expert_gemm_down(x, K, N, wq, ws_, 1, uq, of, nu, 1, M, y, wsp)), wsp
+
+
 def bench_lm_head(peak, reps=30):
     """An FP8 LM head (GLM-5.2 x10 §8b), the vocabulary projection
     N = 151,552 x K = 6144 (931 MB of E4M3 codes), through the down GEMM call
@@ -681,24 +708,13 @@ def bench_lm_head(peak, reps=30):
     N is above the multi-token kernel's 6144, so the persistent engine serves
     it, on tcgen05 at both row counts."""
     from bandwidth_bound_fp8_gb300 import moeq
-    K, N = 6144, 151552
-    wq = torch.empty((1, N, K), dtype=torch.uint8, device="cuda")
-    ws_ = torch.empty((1, N // 128, K // 128), dtype=torch.float32, device="cuda")
-    rows = 4096   # quantise in slabs of whole 128-row blocks to bound the fp32 draw
-    for r0 in range(0, N, rows):
-        r1 = min(N, r0 + rows)
-        w32 = synth.weight_f32(r1 - r0, K, synth.expert_seed(3100, 0, r0 // rows, 1), device="cuda")
-        moeq.moeq_quant_weight(w32[None], wq[:, r0:r1], ws_[:, r0 // 128:r1 // 128])
-    del w32
-    one = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    K, N = LM_HEAD_K, LM_HEAD_N
     out = {}
-    for M in (1, 4):
-        x = synth.activations_bf16(M, K, 3101 + M, 61, 30.0, device="cuda")
-        uq, of, nu = one([0]), one([0, M]), one([1])
-        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        wsp = moeq.Workspace(moeq.moeq_gemm_workspace_size(N, K, M, 1, 0))
+    for M, call, wsp in lm_head_calls():
         torch.cuda.synchronize()
-        t = time_scrubbed(lambda: moeq.moeq_expert_gemm_down(x, K, N, wq, ws_, 1, uq, of, nu, 1, M, y, wsp), reps, 5)
+        t = time_scrubbed(call, reps, 5)
+        if moeq.moeq_read_device_status(wsp.t, wsp.nbytes) != 0:
+            raise RuntimeError(f"lm_head M={M}: device status word set")
         out[f"M{M}"] = _line(f"lm_head_m{M}_k{K}_n{N}", N * K + (N // 128) * (K // 128) * 4, t, peak)
         out[f"M{M}"]["call"] = "moeq_expert_gemm_down (one expert; the persistent engine, tcgen05)"
     return out
@@ -842,6 +858,25 @@ def profile_case(M: int, reps: int, Er: int = 8):
                       "unique_experts": U, "algorithmic_bytes": U * EXPERT_BYTES}))
 
 
+def profile_lm_head(reps: int):
+    """Small launch list for ncu captures of the LM head: `reps` calls at
+    one token, then `reps` at four (moeq_expert_gemm_down on the persistent
+    engine's tcgen05 path, one stream_kernel launch each), each after more
+    than L2 has been written, so that the 931 MB weight comes from HBM."""
+    from bandwidth_bound_fp8_gb300 import build as b
+    b.build()
+    from bandwidth_bound_fp8_gb300 import moeq
+    scrub = torch.empty(2 * L2_BYTES // 4 + 1024, dtype=torch.float32, device="cuda")
+    for M, call, wsp in lm_head_calls():
+        for _ in range(reps):
+            scrub.zero_()
+            call()
+        torch.cuda.synchronize()
+        if moeq.moeq_read_device_status(wsp.t, wsp.nbytes) != 0:
+            raise RuntimeError(f"lm_head M={M}: device status word set")
+    print(json.dumps({"profile_lm_head": f"lm_head_k{LM_HEAD_K}_n{LM_HEAD_N}", "M": [1, 4], "launches": reps}))
+
+
 def profile_dense(reps: int):
     """Small launches for ncu captures of the dense configurations: `reps`
     calls each of the projection K 2048 -> N 4096 (moeq_expert_gemm_down:
@@ -913,6 +948,8 @@ def main():
     ap.add_argument("--profile-experts", type=int, default=8, help="routed experts of the --profile-case layer")
     ap.add_argument("--profile-dense", action="store_true",
                     help="a few launches of the dense configurations (for ncu), no timing")
+    ap.add_argument("--profile-lm-head", action="store_true",
+                    help="a few launches of the LM head at 1 and 4 tokens (for ncu), no timing")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense configurations and the gate_up ladder")
     ap.add_argument("--no-stack", action="store_true", help="skip the multi-layer stack sweep")
     ap.add_argument("--stack-calls", type=int, default=40)
@@ -920,6 +957,9 @@ def main():
     args = ap.parse_args()
     if args.profile_dense:
         profile_dense(args.reps)
+        return
+    if args.profile_lm_head:
+        profile_lm_head(args.reps)
         return
     if args.profile_case:
         profile_case(args.M, args.reps, args.profile_experts)
