@@ -1,7 +1,8 @@
 """Both engine paths at every token count.
 
-By default a launch with 8 or more tokens per expert runs on tcgen05 and
-smaller ones on the CUDA cores.  The library reads MOEQ_MMA_MIN_TOKENS once
+By default an engine layer launch with 8 or more tokens per expert runs on
+tcgen05 and smaller ones on the CUDA cores, and the standalone GEMM calls
+run on tcgen05 at every row count.  The library reads MOEQ_MMA_MIN_TOKENS once
 per process, so these tests re-run the GEMM and reduced-layer parity tests
 in child processes:
   * with the crossover at 1, every launch runs on tcgen05 (one-token
