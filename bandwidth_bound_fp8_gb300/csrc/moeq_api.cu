@@ -44,10 +44,11 @@ DeviceInfo current_device() {
     return cache[dev];
 }
 
-// Token count (per expert) from which launches take the tcgen05 path: 8,
-// where it measured faster than the CUDA cores; the environment variable
-// MOEQ_MMA_MIN_TOKENS overrides it (read once; 17 or more keeps every launch
-// on the CUDA cores, 1 sends every launch to the tensor cores).
+// Token count (per expert) from which the engine's layer launches take the
+// tcgen05 path: 8, where it measured faster than the CUDA cores.  The
+// environment variable MOEQ_MMA_MIN_TOKENS overrides it, for the GEMM calls
+// too (read once; 17 or more keeps every launch on the CUDA cores, 1 sends
+// every launch to the tensor cores).
 int mma_min_tokens() {
     static const int v = [] {
         const char* e = std::getenv("MOEQ_MMA_MIN_TOKENS");
